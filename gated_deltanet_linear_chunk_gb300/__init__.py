@@ -1,0 +1,220 @@
+"""GB300 (sm_103a) Gated DeltaNet layer: chunked prefill and recurrent decode.
+
+The compute lives in ``libgdn`` (hand-written CUDA behind the C ABI declared
+in ``include/gdn.h``).  This module is the thin binding: it checks tensor
+shapes and dtypes, marshals device pointers and the current CUDA stream, and
+calls the C entry points of the same names.  Every step of the layer runs in
+the library's kernels; there is no other implementation to fall back on, and
+a missing library raises.
+
+Method: per token ``S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T``,
+``o_t = S_t q_t`` with ``a_t = exp(g_t)`` (Gated DeltaNet, the linear-attention
+layers of the hybrid Qwen3.8-27B model; page "cf-1.com", section "三个优化",
+item 2 "GDN prefill", chunk length 64).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "GDNError", "library", "gdn_chunk_prefill", "gdn_decode_step",
+    "gdn_chunk_prefill_workspace_size", "gdn_status_string", "gdn_version", "Problem",
+    "GDN_BF16", "GDN_F32",
+]
+
+GDN_BF16 = 0
+GDN_F32 = 1
+_DTYPES = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``gdn_problem`` in include/gdn.h."""
+
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("total_tokens", ctypes.c_int64),
+        ("num_k_heads", ctypes.c_int32),
+        ("num_v_heads", ctypes.c_int32),
+        ("head_dim_k", ctypes.c_int32),
+        ("head_dim_v", ctypes.c_int32),
+        ("qkv_dtype", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class GDNError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {gdn_status_string(code)}")
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"the CUDA library {path} is missing: build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    PP = ctypes.POINTER(Problem)
+    lib.gdn_chunk_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.gdn_chunk_prefill_workspace_size.argtypes = [PP]
+    lib.gdn_chunk_prefill.restype = ctypes.c_int
+    lib.gdn_chunk_prefill.argtypes = [PP, P, P, P, P, P, P, P, P, P, P]
+    lib.gdn_decode_step.restype = ctypes.c_int
+    lib.gdn_decode_step.argtypes = [PP, P, P, P, P, P, P, P, P]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_version.restype = ctypes.c_int
+    lib.gdn_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def gdn_status_string(code: int) -> str:
+    return library().gdn_status_string(int(code)).decode()
+
+
+def gdn_version() -> int:
+    return int(library().gdn_version())
+
+
+def make_problem(num_seqs: int, total_tokens: int, Hk: int, Hv: int, dk: int, dv: int,
+                 dtype, workspace: Optional[torch.Tensor] = None) -> Problem:
+    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return Problem(num_seqs, total_tokens, Hk, Hv, dk, dv, code, ws_ptr, ws_bytes)
+
+
+def gdn_chunk_prefill_workspace_size(num_seqs: int, total_tokens: int, Hk: int, Hv: int,
+                                     dk: int, dv: int, dtype=torch.bfloat16) -> int:
+    p = make_problem(num_seqs, total_tokens, Hk, Hv, dk, dv, dtype)
+    return int(library().gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_workspaces = {}
+
+
+def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                      g: torch.Tensor, beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                      initial_state: Optional[torch.Tensor] = None,
+                      out: Optional[torch.Tensor] = None,
+                      final_state: Optional[torch.Tensor] = None,
+                      output_final_state: bool = False,
+                      workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked GDN prefill over packed sequences (see ``gdn_chunk_prefill`` in
+    include/gdn.h).  q, k: [T, Hk, dk]; v: [T, Hv, dv]; g, beta: [T, Hv] fp32;
+    cu_seqlens: [N+1] int32 on the device.  Returns (out, final_state); the
+    final state is returned when ``final_state`` is given or
+    ``output_final_state`` is set."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported q/k/v dtype {dt}")
+    _check(q, "q", dt, (T, Hk, dk))
+    _check(k, "k", dt, (T, Hk, dk))
+    _check(v, "v", dt, (T, Hv, dv))
+    _check(g, "g", torch.float32, (T, Hv))
+    _check(beta, "beta", torch.float32, (T, Hv))
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32, (N, Hv, dv, dk))
+    if out is None:
+        out = torch.empty((T, Hv, dv), dtype=dt, device=q.device)
+    _check(out, "out", dt, (T, Hv, dv))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, Hv, dv, dk), dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, (N, Hv, dv, dk))
+    lib = library()
+    p = make_problem(N, T, Hk, Hv, dk, dv, dt)
+    need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    p = make_problem(N, T, Hk, Hv, dk, dv, dt, workspace)
+    rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(cu_seqlens), _ptr(initial_state), _ptr(out),
+                               _ptr(final_state), _stream(stream))
+    if rc != 0:
+        raise GDNError(rc, "gdn_chunk_prefill")
+    return out, final_state
+
+
+def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    g: torch.Tensor, beta: torch.Tensor, state: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One recurrent step per sequence, updating ``state`` in place (see
+    ``gdn_decode_step`` in include/gdn.h).  q, k: [N, Hk, dk]; v: [N, Hv, dv];
+    g, beta: [N, Hv] fp32; state: [N, Hv, dv, dk] fp32.  Returns out [N, Hv, dv]."""
+    N, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported q/k/v dtype {dt}")
+    _check(q, "q", dt, (N, Hk, dk))
+    _check(k, "k", dt, (N, Hk, dk))
+    _check(v, "v", dt, (N, Hv, dv))
+    _check(g, "g", torch.float32, (N, Hv))
+    _check(beta, "beta", torch.float32, (N, Hv))
+    _check(state, "state", torch.float32, (N, Hv, dv, dk))
+    if out is None:
+        out = torch.empty((N, Hv, dv), dtype=dt, device=q.device)
+    _check(out, "out", dt, (N, Hv, dv))
+    p = make_problem(N, N, Hk, Hv, dk, dv, dt)
+    rc = library().gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
+    if rc != 0:
+        raise GDNError(rc, "gdn_decode_step")
+    return out

@@ -1,0 +1,101 @@
+// api.cu -- the C ABI (include/gdn.h): argument checks and dispatch.
+//
+// Every argument error is caught here, before any launch, so a rejected call
+// writes nothing.  Nothing in this file allocates, frees or synchronises.
+#include <cstring>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace gdn;
+
+bool dims_supported(const gdn_problem &p) {
+    if (p.head_dim_k != p.head_dim_v) return false;
+    if (p.head_dim_k != 64 && p.head_dim_k != 128) return false;
+    if (p.qkv_dtype != GDN_BF16 && p.qkv_dtype != GDN_F32) return false;
+    return p.num_v_heads % p.num_k_heads == 0;
+}
+
+gdn_status check_problem(const gdn_problem *pp) {
+    if (!pp) return GDN_ERR_INVALID_ARG;
+    const gdn_problem &p = *pp;
+    if (p.num_seqs < 0 || p.total_tokens < 0 || p.num_k_heads <= 0 || p.num_v_heads <= 0 ||
+        p.head_dim_k <= 0 || p.head_dim_v <= 0)
+        return GDN_ERR_INVALID_ARG;
+    // Grid dimensions and 32-bit token offsets inside the kernels.
+    if (p.total_tokens > (int64_t)INT32_MAX / 2 || p.num_seqs > 65535 ||
+        p.num_v_heads > 65535 ||
+        (int64_t)p.num_v_heads * p.head_dim_v > (int64_t)1 << 20)
+        return GDN_ERR_INVALID_ARG;
+    if (!dims_supported(p)) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+bool any_misaligned(std::initializer_list<const void *> ptrs) {
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return true;
+    return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem) {
+    if (check_problem(problem) != GDN_OK) return 0;
+    return 0;
+}
+
+GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem, const void *q, const void *k,
+                                     const void *v, const float *g, const float *beta,
+                                     const int32_t *cu_seqlens, const float *initial_state,
+                                     void *out, float *final_state, gdn_stream_t stream) {
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    const gdn_problem &p = *problem;
+    if (p.num_seqs == 0) return p.total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (p.total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
+    if (any_misaligned({q, k, v, g, beta, initial_state, out, final_state}))
+        return GDN_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return GDN_ERR_MISALIGNED;
+    if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
+    const size_t need = gdn_chunk_prefill_workspace_size(problem);
+    if (need > 0) {
+        if (!p.workspace || p.workspace_bytes < need) return GDN_ERR_WORKSPACE;
+        if (!aligned16(p.workspace)) return GDN_ERR_WORKSPACE;
+    }
+    return launch_prefill_simt(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+GDN_API gdn_status gdn_decode_step(const gdn_problem *problem, const void *q, const void *k,
+                                   const void *v, const float *g, const float *beta,
+                                   float *state, void *out, gdn_stream_t stream) {
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    const gdn_problem &p = *problem;
+    if (p.total_tokens != p.num_seqs) return GDN_ERR_INVALID_ARG;
+    if (p.num_seqs == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out) return GDN_ERR_INVALID_ARG;
+    if (any_misaligned({q, k, v, g, beta, state, out})) return GDN_ERR_MISALIGNED;
+    if (out == q || out == k || out == v) return GDN_ERR_INVALID_ARG;
+    return launch_decode(p, q, k, v, g, beta, state, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+GDN_API const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: configuration not supported";
+        case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA launch or runtime error";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+GDN_API int gdn_version(void) { return 100; }
+
+}  // extern "C"

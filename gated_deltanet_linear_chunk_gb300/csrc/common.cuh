@@ -1,0 +1,45 @@
+// common.cuh -- small shared helpers of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Load one element of an input tensor as fp32.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Store an fp32 value in the output dtype (bf16: round to nearest even).
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch helpers return a gdn_status for the last launch on this thread.
+inline gdn_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// Kernel launchers implemented in the .cu files.
+gdn_status launch_decode(const gdn_problem &p, const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, float *state, void *out,
+                         cudaStream_t stream);
+gdn_status launch_prefill_simt(const gdn_problem &p, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens, const float *h0, void *out,
+                               float *hT, cudaStream_t stream);
+
+}  // namespace gdn

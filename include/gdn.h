@@ -1,0 +1,145 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet layer library.
+ *
+ * The layer: for every sequence n and value head h (key head hk = h / (Hv/Hk),
+ * contiguous groups), a dv x dk fp32 state S evolves token by token as
+ *
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   a_t = exp(g_t),
+ *     o_t = S_t q_t                       (updated state, no 1/sqrt(d) scale)
+ *
+ * with L2-normalised q and k, g <= 0 and b in [0, 1].  Source: the Gated
+ * DeltaNet linear-attention layers that make up 48 of the 64 layers of the
+ * hybrid Qwen3.8-27B model; page "cf-1.com", section "三个优化", item 2
+ * ("GDN prefill": chunk length 64; intra-chunk prep, inter-chunk state
+ * recurrence and output), and page "reactapp.top", section "Exploiter
+ * l'architecture hybride" (fixed-size state per conversation, fp32, about
+ * 150 MB per request over 48 layers = 48 value heads x 128 x 128 x 4 B each).
+ *
+ * Layouts (row-major, token-major, sequences packed back to back):
+ *   q, k          [T, Hk, dk]       qkv dtype (bf16 or fp32)
+ *   v, out        [T, Hv, dv]       qkv dtype
+ *   g, beta       [T, Hv]           fp32
+ *   cu_seqlens    [N + 1]           int32, device memory
+ *   state         [N, Hv, dv, dk]   fp32; row i is value dimension i,
+ *                                   contiguous over the dk key dimensions
+ * All pointers are DEVICE pointers unless stated otherwise.
+ *
+ * Ownership and threading: the caller owns every buffer.  The library never
+ * allocates device memory, never frees, never synchronises, and launches only
+ * on the given stream.  Calls are reentrant; the only process-wide state is a
+ * per-device cache of device attributes filled on first use.
+ *
+ * Errors: argument errors are detected on the host before any launch and
+ * leave every output untouched.  Launch failures return GDN_ERR_CUDA.  Faults
+ * inside a kernel surface asynchronously at the caller's next
+ * synchronisation, as for any CUDA launch.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent sizes */
+    GDN_ERR_UNSUPPORTED = 2,  /* head dims, head grouping or dtype not built   */
+    GDN_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned       */
+    GDN_ERR_WORKSPACE = 4,    /* workspace missing, too small or misaligned    */
+    GDN_ERR_CUDA = 5          /* a CUDA runtime call or launch failed          */
+} gdn_status;
+
+typedef enum {
+    GDN_BF16 = 0,  /* q, k, v and out are bf16 (tensor-core path)   */
+    GDN_F32 = 1    /* q, k, v and out are fp32 (FFMA check path)    */
+} gdn_dtype;
+
+/*
+ * Problem descriptor shared by every entry point.
+ *   num_seqs      N >= 0 sequences (decode: the batch, one token each)
+ *   total_tokens  T = cu_seqlens[N] (prefill); must equal N for decode
+ *   num_k_heads   Hk >= 1;  num_v_heads Hv, a multiple of Hk
+ *   head_dim_k    dk, head_dim_v dv: 64 or 128, dk == dv
+ *   qkv_dtype     a gdn_dtype
+ *   workspace     device scratch for the prefill (see the size query);
+ *                 16-byte aligned; ignored by the decode step
+ */
+typedef struct {
+    int32_t num_seqs;
+    int64_t total_tokens;
+    int32_t num_k_heads;
+    int32_t num_v_heads;
+    int32_t head_dim_k;
+    int32_t head_dim_v;
+    int32_t qkv_dtype;
+    void *workspace;
+    size_t workspace_bytes;
+} gdn_problem;
+
+/*
+ * Bytes of device workspace gdn_chunk_prefill needs for this problem (it
+ * depends on N, T, Hk, Hv, the head dims and the dtype).  Returns 0 when the
+ * descriptor is invalid or the configuration needs no workspace.
+ */
+GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem);
+
+/*
+ * Chunked prefill (chunk length 64) over N packed sequences.
+ *   q, k, v        inputs as laid out above (qkv dtype)
+ *   g, beta        fp32 log-decay (<= 0) and write strength per token and
+ *                  value head
+ *   cu_seqlens     device int32 [N + 1]: cu[0] = 0, nondecreasing, cu[N] = T.
+ *                  Zero-length sequences are allowed (their final state is
+ *                  the initial state).  Not checked on the host.
+ *   initial_state  fp32 [N, Hv, dv, dk] or NULL (zero start)
+ *   out            [T, Hv, dv], qkv dtype; must not alias any input
+ *   final_state    fp32 [N, Hv, dv, dk] or NULL (not written); may equal
+ *                  initial_state (in-place resume)
+ * q and k must already be L2-normalised by the caller.  All tensor pointers
+ * must be 16-byte aligned.
+ */
+GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
+                                     const void *q, const void *k, const void *v,
+                                     const float *g, const float *beta,
+                                     const int32_t *cu_seqlens,
+                                     const float *initial_state,
+                                     void *out, float *final_state,
+                                     gdn_stream_t stream);
+
+/*
+ * One recurrent decode step for N sequences (one token each), updating the
+ * state in place:
+ *   q, k   [N, Hk, dk];  v, out [N, Hv, dv] (qkv dtype);  g, beta [N, Hv] fp32
+ *   state  fp32 [N, Hv, dv, dk], read and written in place
+ * problem->total_tokens must equal problem->num_seqs.
+ */
+GDN_API gdn_status gdn_decode_step(const gdn_problem *problem,
+                                   const void *q, const void *k, const void *v,
+                                   const float *g, const float *beta,
+                                   float *state, void *out,
+                                   gdn_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+GDN_API const char *gdn_status_string(gdn_status status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+GDN_API int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

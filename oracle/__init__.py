@@ -122,15 +122,20 @@ def prefill(q, k, v, g, beta, cu_seqlens, initial_state=None,
 
 
 def decode(q, k, v, g, beta, state, heads: Optional[Sequence[int]] = None,
-           num_threads: int = 0, lib=None):
+           num_threads: int = 0, lib=None, inplace: bool = False):
     """One fp64 recurrent step for N sequences.
 
     q, k: [N, Hk, dk]; v: [N, Hv, dv]; g, beta: [N, Hv]; state [N, Hv, dv, dk]
-    (not modified).  Returns (out [N, Hv, dv], new_state).
+    (updated in place when ``inplace`` and it is a C-contiguous float64 array,
+    else copied).  Returns (out [N, Hv, dv], new_state).
     """
     lib = lib or load()
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
-    S = _f64(state).copy()
+    if inplace:
+        S = state
+        assert isinstance(S, np.ndarray) and S.dtype == np.float64 and S.flags.c_contiguous
+    else:
+        S = _f64(state).copy()
     N, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     assert S.shape == (N, Hv, dv, dk) and g.shape == (N, Hv) and beta.shape == (N, Hv)

@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_deltanet_linear_chunk_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA = range(6)
+A = 0x10000  # a 16-byte aligned fake device address; never dereferenced here
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return gdn.library()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ["gdn_chunk_prefill", "gdn_decode_step", "gdn_chunk_prefill_workspace_size",
+              "gdn_status_string", "gdn_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = gdn.gdn_status_string(code)
+        assert s.startswith("GDN_")
+    assert "UNKNOWN" in gdn.gdn_status_string(99)
+    assert gdn.gdn_version() >= 100
+
+
+def prob(N=1, T=64, Hk=1, Hv=1, dk=128, dv=128, dtype=gdn.GDN_BF16, ws=None, wsb=0):
+    return gdn.Problem(N, T, Hk, Hv, dk, dv, dtype, ws, wsb)
+
+
+def prefill(lib, p, q=A, k=A + 4096, v=A + 8192, g=A + 12288, b=A + 16384, cu=A + 20480,
+            h0=None, out=A + 24576, hT=None):
+    return lib.gdn_chunk_prefill(ctypes.byref(p) if p is not None else None, q, k, v, g, b, cu,
+                                 h0, out, hT, None)
+
+
+def decode(lib, p, q=A, k=A + 4096, v=A + 8192, g=A + 12288, b=A + 16384, s=A + 20480,
+           out=A + 24576):
+    return lib.gdn_decode_step(ctypes.byref(p) if p is not None else None, q, k, v, g, b, s,
+                               out, None)
+
+
+def test_prefill_argument_errors(lib):
+    assert prefill(lib, None) == INVALID
+    assert prefill(lib, prob(N=-1)) == INVALID
+    assert prefill(lib, prob(T=-5)) == INVALID
+    assert prefill(lib, prob(Hk=0)) == INVALID
+    assert prefill(lib, prob(dk=96, dv=96)) == UNSUPPORTED
+    assert prefill(lib, prob(dk=128, dv=64)) == UNSUPPORTED
+    assert prefill(lib, prob(Hk=2, Hv=3)) == UNSUPPORTED
+    assert prefill(lib, prob(dtype=7)) == UNSUPPORTED
+    assert prefill(lib, prob(), cu=None) == INVALID
+    assert prefill(lib, prob(), q=None) == INVALID
+    assert prefill(lib, prob(), out=None) == INVALID
+    assert prefill(lib, prob(), q=A + 2) == MISALIGNED
+    assert prefill(lib, prob(), h0=A + 8) == MISALIGNED
+    assert prefill(lib, prob(), hT=A + 4) == MISALIGNED
+    assert prefill(lib, prob(), cu=A + 2) == MISALIGNED
+    assert prefill(lib, prob(), out=A) == INVALID          # aliases q
+    assert prefill(lib, prob(N=0, T=5)) == INVALID
+    assert prefill(lib, prob(N=0, T=0)) == OK              # nothing to do, no launch
+
+
+def test_prefill_workspace_checks(lib):
+    p = prob(N=2, T=5000, Hk=16, Hv=48)
+    need = lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p))
+    if need == 0:
+        pytest.skip("this configuration needs no workspace")
+    assert prefill(lib, p) == WORKSPACE
+    small = prob(N=2, T=5000, Hk=16, Hv=48, ws=A, wsb=need - 16)
+    assert prefill(lib, small) == WORKSPACE
+    mis = prob(N=2, T=5000, Hk=16, Hv=48, ws=A + 8, wsb=need)
+    assert prefill(lib, mis) == WORKSPACE
+
+
+def test_workspace_size_of_invalid_problem_is_zero(lib):
+    p = prob(dk=96, dv=96)
+    assert lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)) == 0
+    assert lib.gdn_chunk_prefill_workspace_size(None) == 0
+
+
+def test_decode_argument_errors(lib):
+    assert decode(lib, None) == INVALID
+    assert decode(lib, prob(N=4, T=5)) == INVALID
+    assert decode(lib, prob(N=4, T=4), s=None) == INVALID
+    assert decode(lib, prob(N=4, T=4), s=A + 4) == MISALIGNED
+    assert decode(lib, prob(N=4, T=4), out=A + 4096) == INVALID   # aliases k
+    assert decode(lib, prob(N=4, T=4, dk=32, dv=32)) == UNSUPPORTED
+    assert decode(lib, prob(N=0, T=0)) == OK
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    x = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gdn.gdn_decode_step(x, x, x, torch.zeros(4, 1), torch.zeros(4, 1),
+                            torch.zeros(4, 1, 128, 128))

@@ -1,0 +1,135 @@
+"""Prefill parity: the CUDA path through the C ABI against the fp64 oracle on
+the same seeded inputs (element by element), plus invariants and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_chunk_gb300 as gdn
+from gated_deltanet_linear_chunk_gb300 import inputs
+from gpu_util import TOL_BF16, TOL_F32, check_prefill, f64, rel, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def test_fp32_single_head_d64():
+    """N=1, T=256 (4 chunks), one head, d=64, fp32 inputs, zero start."""
+    p = inputs.prefill_inputs([256], 1, 1, 64, 64, dtype=torch.float32, seed=0)
+    check_prefill(p, TOL_F32)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_small_varlen_ragged(d, dtype):
+    """Several tiles, ragged tails, an empty and a one-token sequence, GQA 1:3,
+    nonzero initial states."""
+    p = inputs.prefill_inputs([130, 1, 64, 0, 77, 200], 2, 6, d, d, dtype=dtype, seed=1,
+                              initial_state_std=0.02)
+    check_prefill(p, TOL_BF16 if dtype == torch.bfloat16 else TOL_F32)
+
+
+def test_zero_start_without_initial_state():
+    p = inputs.prefill_inputs([191], 1, 3, 128, 128, dtype=torch.bfloat16, seed=2)
+    check_prefill(p, TOL_BF16)
+
+
+def test_t4000_48_heads_sampled():
+    """T=4000 (62 full chunks + 32), 16 key / 48 value heads, d=128, bf16,
+    zero start: every token of three key-head groups (9 value heads)."""
+    p = inputs.prefill_inputs([4000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
+    check_prefill(p, TOL_BF16, key_heads=[0, 7, 15])
+
+
+def test_t20480_initial_state_sampled():
+    """T=20480 (320 chunks), nonzero initial state ~N(0, 0.02^2), final state."""
+    p = inputs.prefill_inputs([20480], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0,
+                              initial_state_std=0.02)
+    check_prefill(p, TOL_BF16, key_heads=[3, 12])
+
+
+def test_varlen_eight_sequences_sampled():
+    """8 packed sequences {512 .. 32768} (T=70904), per-sequence initial states."""
+    lens = [512, 1000, 2048, 4000, 6000, 8192, 16384, 32768]
+    p = inputs.prefill_inputs(lens, 16, 48, 128, 128, dtype=torch.bfloat16, seed=0,
+                              initial_state_std=0.02)
+    check_prefill(p, TOL_BF16, key_heads=[5])
+
+
+def test_split_prefill_equals_whole():
+    """prefill(T1) then prefill(T2) from its final state matches prefill(T1+T2)."""
+    p = inputs.prefill_inputs([300], 1, 3, 128, 128, dtype=torch.bfloat16, seed=3,
+                              initial_state_std=0.02)
+    dev = torch.device("cuda")
+    whole, fin = run_prefill(p)
+    T1 = 100
+    cu1 = torch.tensor([0, T1], dtype=torch.int32, device=dev)
+    cu2 = torch.tensor([0, 300 - T1], dtype=torch.int32, device=dev)
+    a = [x.to(dev) for x in (p.q, p.k, p.v, p.g, p.beta)]
+    o1, f1 = gdn.gdn_chunk_prefill(*[x[:T1].contiguous() for x in a], cu1,
+                                   p.initial_state.to(dev), output_final_state=True)
+    o2, f2 = gdn.gdn_chunk_prefill(*[x[T1:].contiguous() for x in a], cu2, f1,
+                                   output_final_state=True)
+    torch.cuda.synchronize()
+    assert rel(f64(torch.cat([o1, o2])), f64(whole)) <= TOL_BF16
+    assert rel(f64(f2), f64(fin)) <= 1e-3
+
+
+def test_varlen_equals_separate_runs():
+    lens = [70, 130, 5]
+    p = inputs.prefill_inputs(lens, 2, 4, 64, 64, dtype=torch.bfloat16, seed=4,
+                              initial_state_std=0.02)
+    out, fin = run_prefill(p)
+    dev = torch.device("cuda")
+    cu = p.cu_seqlens.tolist()
+    for n in range(len(lens)):
+        s, e = cu[n], cu[n + 1]
+        o1, f1 = gdn.gdn_chunk_prefill(
+            *[x[s:e].contiguous().to(dev) for x in (p.q, p.k, p.v, p.g, p.beta)],
+            torch.tensor([0, e - s], dtype=torch.int32, device=dev),
+            p.initial_state[n:n + 1].contiguous().to(dev), output_final_state=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, out[s:e])
+        assert torch.equal(f1, fin[n:n + 1])
+
+
+def test_in_place_resume_and_empty_sequences():
+    """final_state may alias initial_state; empty sequences keep their state;
+    T = 0 with N > 0 copies the initial state."""
+    p = inputs.prefill_inputs([0, 65, 0], 1, 2, 128, 128, dtype=torch.bfloat16, seed=5,
+                              initial_state_std=0.02)
+    _, fin = run_prefill(p)
+    dev = torch.device("cuda")
+    h = p.initial_state.to(dev).clone()
+    gdn.gdn_chunk_prefill(p.q.to(dev), p.k.to(dev), p.v.to(dev), p.g.to(dev), p.beta.to(dev),
+                          p.cu_seqlens.to(dev), h, final_state=h)
+    torch.cuda.synchronize()
+    assert torch.equal(h, fin)
+    assert torch.equal(fin[0].cpu(), p.initial_state[0])
+    assert torch.equal(fin[2].cpu(), p.initial_state[2])
+    e = inputs.prefill_inputs([0, 0], 1, 1, 64, 64, dtype=torch.float32, seed=6,
+                              initial_state_std=0.5)
+    out, f = run_prefill(e)
+    assert out.numel() == 0 and torch.equal(f.cpu(), e.initial_state)
+
+
+def test_no_initial_state_final_is_computed_from_zero():
+    p = inputs.prefill_inputs([0, 3], 1, 1, 64, 64, dtype=torch.float32, seed=7)
+    _, fin = run_prefill(p)
+    assert torch.count_nonzero(fin[0]) == 0
+    check_prefill(p, TOL_F32)
+
+
+def test_strong_decay_and_saturated_gates():
+    """g very negative (a ~ 0) and beta in {0, 1}: no overflow or NaN."""
+    p = inputs.prefill_inputs([150], 1, 3, 128, 128, dtype=torch.bfloat16, seed=8,
+                              initial_state_std=0.02)
+    p.g[::7] = -30.0
+    p.g[3::11] = -1e4
+    p.beta[::5] = 0.0
+    p.beta[2::5] = 1.0
+    check_prefill(p, TOL_BF16)
