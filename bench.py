@@ -1,0 +1,365 @@
+"""Benchmark of the GDN layer on one GB300 (or N independent replicas).
+
+Workload (the pages' "4000-token layer"): chunked prefill of one sequence of
+T = 4000 tokens, 16 key / 48 value heads, d_k = d_v = 128, bf16 q/k/v, fp32
+g/beta/state, zero initial state.  A step is one prefill call over that
+input.  ``value`` is prefill tokens per second per layer, device-timed with
+CUDA events, inputs resident in HBM, L2 flushed before every step.  The
+decode step (64 sequences x 1 token, 48 heads, fp32 state [64,48,128,128])
+is timed in the same run and reported under ``decode`` against HBM bandwidth.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica on its own GPU; the
+job value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s/layer (T=4000,48 heads) & % bf16 peak; decode % HBM BW"
+UNIT = "tokens/s/layer"
+PREFILL = dict(seqlens=[4000], Hk=16, Hv=48, d=128)
+DECODE = dict(N=64, Hk=16, Hv=48, d=128)
+L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
+# Algorithmic work per token per value head (d = 128, C = 64, G = 3), the
+# triangle-aware chunked count: 6 d^2 + C (dk + dv) + C dv + 2 C dk / G + C^2 / 3.
+FLOPS_PER_TOKEN_HEAD = 6 * 128 ** 2 + 64 * 256 + 64 * 128 + 2 * 64 * 128 // 3 + 64 ** 2 // 3
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def prefill_bytes(T, Hk, Hv, d):
+    """Compulsory HBM bytes of one prefill: q, k, v read, out written (bf16),
+    g and beta read (fp32)."""
+    return T * (2 * Hk * d * 2 + Hv * d * 2 + Hv * d * 2 + 2 * Hv * 4)
+
+
+def decode_bytes(N, Hk, Hv, d):
+    """Compulsory HBM bytes of one decode step: the fp32 state read and
+    written, q/k/v read and out written (bf16), g and beta read (fp32)."""
+    return N * (2 * Hv * d * d * 4 + 2 * Hk * d * 2 + 2 * Hv * d * 2 + 2 * Hv * 4)
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units of every rank over the slowest rank."""
+    return units_per_rank * world / max_seconds
+
+
+def oracle_sample_prefill(tokens: int, num_threads: int = 0):
+    """Times the fp64 oracle on the first ``tokens`` tokens of the prefill
+    workload, all 48 value heads.  Returns (tokens/s/layer, seconds, threads)."""
+    import torch
+
+    import oracle
+    from gated_deltanet_linear_chunk_gb300 import inputs
+    p = inputs.prefill_inputs([tokens], PREFILL["Hk"], PREFILL["Hv"], PREFILL["d"],
+                              PREFILL["d"], dtype=torch.bfloat16, seed=0)
+    arrs = [x.double().numpy() for x in (p.q, p.k, p.v, p.g, p.beta)]
+    threads = num_threads or oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.prefill(*arrs, p.cu_seqlens.numpy(), None, num_threads=threads)
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt, min(threads, PREFILL["Hv"])
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: fp64 CPU, bounded sample per step."""
+    if rank != 0:
+        return
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample_prefill(max(16, tokens // 8))
+    vals, secs = [], []
+    threads = 1
+    for _ in range(args.steps):
+        v, s, threads = oracle_sample_prefill(tokens)
+        vals.append(v)
+        secs.append(s)
+    value = statistics.median(vals)
+    sample = (f"first {tokens} of the 4000 tokens, all 48 value heads, fp64 token "
+              f"recurrence; tokens/s/layer = tokens / wall time")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "GDN prefill T=4000, 16 key / 48 value heads, d=128",
+                   "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import gated_deltanet_linear_chunk_gb300 as gdn
+    from gated_deltanet_linear_chunk_gb300 import inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gdn.library()
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---------------- prefill ----------------
+    P = PREFILL
+    p = inputs.prefill_inputs(P["seqlens"], P["Hk"], P["Hv"], P["d"], P["d"],
+                              dtype=torch.bfloat16, seed=0)
+    T = sum(P["seqlens"])
+    dq, dk_, dv = p.q.to(dev), p.k.to(dev), p.v.to(dev)
+    dg, db, dcu = p.g.to(dev), p.beta.to(dev), p.cu_seqlens.to(dev)
+    out = torch.empty((T, P["Hv"], P["d"]), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def prefill():
+        gdn.gdn_chunk_prefill(dq, dk_, dv, dg, db, dcu, None, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        prefill()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            prefill()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = statistics.mean(step_ms)
+    ms = max_over_ranks(ms_local, dev)
+    value = job_throughput(T, world, ms / 1e3)
+    launches_per_step = gdn.prefill_launches(P["Hv"], P["d"], torch.bfloat16)
+
+    flops = T * P["Hv"] * FLOPS_PER_TOKEN_HEAD
+    peak_tf = peaks["bf16_tflops"]
+    achieved_tf = flops / (ms_local / 1e3) / 1e12
+    pbytes = prefill_bytes(T, P["Hk"], P["Hv"], P["d"])
+
+    # ---------------- end to end through host buffers ----------------
+    hq, hk, hv = (x.pin_memory() for x in (p.q, p.k, p.v))
+    hg, hb, hcu = (x.pin_memory() for x in (p.g, p.beta, p.cu_seqlens))
+    hout = torch.empty_like(out, device="cpu").pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb, hcu))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for dst, src in ((dq, hq), (dk_, hk), (dv, hv), (dg, hg), (db, hb), (dcu, hcu)):
+            dst.copy_(src, non_blocking=True)
+        prefill()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e_s[i].record(stream)
+        e2e_step()
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in zip(e_s, e_e)), dev)
+
+    # ---------------- decode ----------------
+    D = DECODE
+    state = inputs.decode_state(D["N"], D["Hv"], D["d"], D["d"]).to(dev)
+    dsteps = [inputs.decode_step_inputs(s, D["N"], D["Hk"], D["Hv"], D["d"], D["d"])
+              for s in range(args.decode_steps)]
+    dsteps = [[t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta)] for x in dsteps]
+    dout = torch.empty((D["N"], D["Hv"], D["d"]), dtype=torch.bfloat16, device=dev)
+    for s in range(3):
+        x = dsteps[s % len(dsteps)]
+        gdn.gdn_decode_step(*x, state, out=dout)
+    torch.cuda.synchronize()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    d0.record(stream)
+    for s in range(args.decode_steps):
+        gdn.gdn_decode_step(*dsteps[s], state, out=dout)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_us = 1e3 * d0.elapsed_time(d1) / args.decode_steps
+    dbytes = decode_bytes(D["N"], D["Hk"], D["Hv"], D["d"])
+    dec_gbs = dbytes / (dec_us / 1e6) / 1e9
+
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "GDN prefill, 1 sequence, T=4000, 16 key / 48 value heads, "
+                               "d_k=d_v=128, bf16 q/k/v, fp32 g/beta/state, zero initial state",
+                   "l2": "flushed before every step (512 MB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": None,
+                     "peak_kind": f"{peak_kind} bf16 burst",
+                     "flops_per_launch": flops, "algorithmic_bytes": pbytes},
+        "e2e": {"value": job_throughput(T, world, e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "decode": {"workload": "64 sequences x 1 token, 16 key / 48 value heads, d=128, "
+                               "fp32 state, bf16 q/k/v",
+                   "us_per_step": dec_us, "steps": args.decode_steps,
+                   "bytes_per_step": dbytes, "achieved_gbs": dec_gbs,
+                   "peak_gbs": peaks["hbm_gbs"], "frac": dec_gbs / peaks["hbm_gbs"],
+                   "frac_of_8tbs": dec_gbs / 8000.0, "peak_kind": peak_kind},
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, s, threads = oracle_sample_prefill(args.ref_tokens)
+        line["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {args.ref_tokens} of the 4000 tokens, all 48 value heads "
+                      f"(fp64 token recurrence, {s:.1f} s wall)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=1000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world, local)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

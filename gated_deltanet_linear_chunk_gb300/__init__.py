@@ -218,3 +218,8 @@ def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if rc != 0:
         raise GDNError(rc, "gdn_decode_step")
     return out
+
+
+def prefill_launches(Hv: int, d: int, dtype) -> int:
+    """Kernel launches one gdn_chunk_prefill call makes (for launch counts)."""
+    return 1
