@@ -347,7 +347,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--ref-tokens", type=int, default=1000)
+    ap.add_argument("--ref-tokens", type=int, default=4000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     rank, world, local = dist_setup()
