@@ -220,6 +220,11 @@ def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return out
 
 
-def prefill_launches(Hv: int, d: int, dtype) -> int:
-    """Kernel launches one gdn_chunk_prefill call makes (for launch counts)."""
+def prefill_launches(Hv: int, d: int, dtype, total_tokens: int = 1) -> int:
+    """Kernel launches one gdn_chunk_prefill call makes (for launch counts):
+    the tensor-core path (bf16, d = 128) runs the chunk-table, prep and
+    recurrence kernels (no prep when there are no tokens); the fp32 path one
+    kernel."""
+    if dtype == torch.bfloat16 and d == 128:
+        return 3 if total_tokens > 0 else 2
     return 1

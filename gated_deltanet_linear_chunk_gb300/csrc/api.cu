@@ -44,7 +44,7 @@ extern "C" {
 
 GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem) {
     if (check_problem(problem) != GDN_OK) return 0;
-    return 0;
+    return prefill_tc_supported(*problem) ? prefill_tc_workspace_size(*problem) : 0;
 }
 
 GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem, const void *q, const void *k,
@@ -66,8 +66,12 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem, const void *q, 
         if (!p.workspace || p.workspace_bytes < need) return GDN_ERR_WORKSPACE;
         if (!aligned16(p.workspace)) return GDN_ERR_WORKSPACE;
     }
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    if (prefill_tc_supported(p))
+        return launch_prefill_tc(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                                 st_);
     return launch_prefill_simt(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
-                               reinterpret_cast<cudaStream_t>(stream));
+                               st_);
 }
 
 GDN_API gdn_status gdn_decode_step(const gdn_problem *problem, const void *q, const void *k,

@@ -42,4 +42,10 @@ gdn_status launch_prefill_simt(const gdn_problem &p, const void *q, const void *
                                const int32_t *cu_seqlens, const float *h0, void *out,
                                float *hT, cudaStream_t stream);
 
+size_t prefill_tc_workspace_size(const gdn_problem &p);
+bool prefill_tc_supported(const gdn_problem &p);
+gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
+                             const float *g, const float *beta, const int32_t *cu_seqlens,
+                             const float *h0, void *out, float *hT, cudaStream_t stream);
+
 }  // namespace gdn

@@ -1,0 +1,54 @@
+"""The tcgen05 operand layouts (K-major and MN-major 128-byte-swizzled bf16
+tiles, negated A, accumulate) that the prefill kernels use, each checked
+against a plain matmul on one 128-row tile."""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+PKG = os.path.join(os.path.dirname(HERE), "gated_deltanet_linear_chunk_gb300")
+
+
+@pytest.fixture(scope="module")
+def probe(tmp_path_factory):
+    out = str(tmp_path_factory.mktemp("probe") / "libtc_probe.so")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
+                    "-shared", "-Xcompiler", "-fPIC", "-I", os.path.join(PKG, "csrc"),
+                    "-I", os.path.join(os.path.dirname(HERE), "include"),
+                    os.path.join(HERE, "csrc", "tc_probe.cu"), "-o", out], check=True)
+    lib = ctypes.CDLL(out)
+    lib.tc_probe_run.restype = ctypes.c_int
+    lib.tc_probe_run.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_void_p]
+    return lib
+
+
+def bf(x):
+    return torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+def test_layout(probe, mode):
+    rng = np.random.default_rng(mode)
+    K = 64 if mode in (1, 2) else 128
+    N = 128 if mode == 2 else 64
+    a = rng.standard_normal((K, 128) if mode == 1 else (128, K)).astype(np.float32)
+    b = rng.standard_normal((K, N) if mode in (2, 4) else (N, K)).astype(np.float32)
+    A = bf(a).T if mode == 1 else bf(a)
+    B = bf(b) if mode in (2, 4) else bf(b).T
+    ref = A @ B
+    if mode == 3:
+        ref = ref - ref
+    da = torch.from_numpy(a).cuda()
+    db = torch.from_numpy(b).cuda()
+    dd = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe_run(da.data_ptr(), db.data_ptr(), dd.data_ptr(), mode, st.data_ptr())
+    assert rc == 0 and int(st.item()) == 0
+    got = dd.cpu().double().numpy()
+    assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(A @ B).max())
