@@ -63,4 +63,6 @@ def check_prefill(p: inputs.PrefillInputs, tol: float, key_heads=None):
     assert np.isfinite(f64(out)).all(), "non-finite output"
     assert e_out <= tol, f"out rel err {e_out:.3e} > {tol:.0e}"
     assert e_fin <= tol, f"final state rel err {e_fin:.3e} > {tol:.0e}"
+    print(f"[parity] T={p.q.shape[0]} N={p.cu_seqlens.shape[0] - 1} dtype={p.q.dtype} "
+          f"d={p.q.shape[2]} out {e_out:.3e} final {e_fin:.3e} (tol {tol:.0e})")
     return e_out, e_fin

@@ -6,7 +6,7 @@ import torch
 
 import gated_deltanet_linear_chunk_gb300 as gdn
 from gated_deltanet_linear_chunk_gb300 import inputs
-from gpu_util import TOL_BF16, TOL_F32, check_prefill, f64, rel, run_prefill
+from gpu_util import TOL_BF16, TOL_F32, check_prefill, f64, oracle_prefill, rel, run_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -75,8 +75,13 @@ def test_split_prefill_equals_whole():
     o2, f2 = gdn.gdn_chunk_prefill(*[x[T1:].contiguous() for x in a], cu2, f1,
                                    output_final_state=True)
     torch.cuda.synchronize()
-    assert rel(f64(torch.cat([o1, o2])), f64(whole)) <= TOL_BF16
-    assert rel(f64(f2), f64(fin)) <= 1e-3
+    # Different chunk boundaries round differently: both runs are held to the
+    # oracle's tolerance, and to each other at twice that.
+    o_ref, f_ref, _ = oracle_prefill(p)
+    assert rel(f64(torch.cat([o1, o2])), o_ref) <= TOL_BF16
+    assert rel(f64(f2), f_ref) <= TOL_BF16
+    assert rel(f64(torch.cat([o1, o2])), f64(whole)) <= 2 * TOL_BF16
+    assert rel(f64(f2), f64(fin)) <= 2 * TOL_BF16
 
 
 def test_varlen_equals_separate_runs():
