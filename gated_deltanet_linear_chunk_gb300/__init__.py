@@ -24,7 +24,8 @@ from . import build as _build
 
 __all__ = [
     "GDNError", "library", "gdn_chunk_prefill", "gdn_decode_step",
-    "gdn_chunk_prefill_workspace_size", "gdn_status_string", "gdn_version", "Problem",
+    "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
+    "gdn_version", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
@@ -75,6 +76,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_chunk_prefill_workspace_size.argtypes = [PP]
     lib.gdn_chunk_prefill.restype = ctypes.c_int
     lib.gdn_chunk_prefill.argtypes = [PP, P, P, P, P, P, P, P, P, P, P]
+    lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_noalloc.argtypes = [PP, P, P, P, P, P, P, P, P, P, P]
     lib.gdn_decode_step.restype = ctypes.c_int
     lib.gdn_decode_step.argtypes = [PP, P, P, P, P, P, P, P, P]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -189,6 +192,47 @@ def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                _ptr(final_state), _stream(stream))
     if rc != 0:
         raise GDNError(rc, "gdn_chunk_prefill")
+    return out, final_state
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def gdn_chunk_prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                              g: torch.Tensor, beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                              initial_state: Optional[torch.Tensor] = None,
+                              out: torch.Tensor = None,
+                              final_state: Optional[torch.Tensor] = None,
+                              stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``gdn_chunk_prefill`` for callers that cannot allocate device memory at
+    call time: the library's built-in 64 MiB scratch array replaces the
+    workspace, and ``out`` (and ``final_state`` if wanted) must be given, so
+    this wrapper allocates nothing either.  Problems needing more than 64 MiB
+    of workspace raise GDNError(GDN_ERR_WORKSPACE).  Calls that may overlap on
+    the GPU share the scratch and must be ordered by the caller."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported q/k/v dtype {dt}")
+    if out is None:
+        raise ValueError("gdn_chunk_prefill_noalloc needs a preallocated out")
+    for t, name, tdt, shape in ((q, "q", dt, (T, Hk, dk)), (k, "k", dt, (T, Hk, dk)),
+                                (v, "v", dt, (T, Hv, dv)), (g, "g", torch.float32, (T, Hv)),
+                                (beta, "beta", torch.float32, (T, Hv)),
+                                (cu_seqlens, "cu_seqlens", torch.int32, (N + 1,)),
+                                (out, "out", dt, (T, Hv, dv))):
+        _check(t, name, tdt, shape)
+    for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
+        if t is not None:
+            _check(t, name, torch.float32, (N, Hv, dv, dk))
+    p = make_problem(N, T, Hk, Hv, dk, dv, dt)
+    rc = library().gdn_chunk_prefill_noalloc(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+        _ptr(initial_state), _ptr(out), _ptr(final_state), _stream(stream))
+    if rc != 0:
+        raise GDNError(rc, "gdn_chunk_prefill_noalloc")
     return out, final_state
 
 

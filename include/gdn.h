@@ -132,6 +132,33 @@ GDN_API gdn_status gdn_decode_step(const gdn_problem *problem,
                                    float *state, void *out,
                                    gdn_stream_t stream);
 
+/*
+ * gdn_chunk_prefill without caller-provided scratch.  (The paper has no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * when they call the layer -- engines that reserve nearly all device memory
+ * for their own pools at start-up, plug-ins inside a framework that owns the
+ * allocator, latency-critical paths that cannot afford cudaMalloc's
+ * device-wide synchronisation.)
+ *
+ * Same arguments and results as gdn_chunk_prefill; problem->workspace and
+ * problem->workspace_bytes are ignored.  The scratch is one 64 MiB array in
+ * device memory, built into the library and held by every GPU that loads it
+ * until the process exits.  Problems whose workspace size (see
+ * gdn_chunk_prefill_workspace_size) exceeds 64 MiB are rejected with
+ * GDN_ERR_WORKSPACE before any launch.  The first call on a device, with that
+ * device current, looks up the array's device address; make that first call
+ * before any stream capture.  All calls share the array: calls that may run
+ * at the same time on the GPU (unordered streams) race and must be ordered by
+ * the caller.  Nothing is allocated or freed.
+ */
+GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_problem *problem,
+                                             const void *q, const void *k, const void *v,
+                                             const float *g, const float *beta,
+                                             const int32_t *cu_seqlens,
+                                             const float *initial_state,
+                                             void *out, float *final_state,
+                                             gdn_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);
 
