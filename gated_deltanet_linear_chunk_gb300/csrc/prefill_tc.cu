@@ -5,31 +5,37 @@
 //      (sequence, first token, length) table of all chunks and the order in
 //      which the recurrence CTAs take sequences (longest first).
 //   2. gdn_prep_kernel         one CTA per (chunk, key head), all chunks at
-//      once: the intra-chunk prep.  [K; Q] K^T on the tensor cores (one
-//      M = 128 MMA gives K K^T and Q K^T), then for each value head of the
-//      key head: gamma = cumsum(g), A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i)
-//      for i < t, T = (I + A)^-1 by fp32 forward substitution, and the two
-//      64 x 64 bf16 tiles the recurrence needs, T diag(b) and
-//      P = M o Q K^T (M_ri = e^{gamma_r - gamma_i}, i <= r), written to the
-//      workspace in the swizzled image of a shared-memory tile.
+//      once: the intra-chunk prep, for every value head of the key head:
+//        gamma = cumsum(g); [K; Q] K^T in one M = 128 MMA (K K^T and Q K^T);
+//        A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i), i < t;
+//        T = (I + A)^-1 as  T = D' - (D' E) D',  where D' holds the inverses
+//          of the two 32 x 32 diagonal blocks of I + A (fp32 forward
+//          substitution) and E the lower-left block of A (two MMAs; with
+//          only two blocks, (D' E)^2 = 0, so the series stops there);
+//        W^T = K^T (T diag(b e^gamma))^T  (MMA, M = 128);
+//        P = M o Q K^T,  M_ri = e^{gamma_r - gamma_i} for i <= r;
+//      and stores W^T, T diag(b), P (bf16, as swizzled shared-memory tile
+//      images), e^gamma and e^{gamma_L - gamma} in the workspace.
 //   3. gdn_chain_kernel        one CTA per (sequence, value head): the
-//      inter-chunk recurrence and the output.  The fp32 state S (dv x dk)
-//      stays in tensor memory for the whole sequence; per chunk, with a bf16
-//      copy of S0 in shared memory as the MMA operand:
-//         U^T   = V^T (T diag b)^T                 (TMEM, fp32)
-//         W^T   = K^T (T diag(b e^gamma))^T        (TMEM -> bf16 smem)
-//         Delta^T = U^T - S0 W^T                   (accumulated onto U^T)
-//         O1^T  = S0 Q^T,  O2^T = Delta^T P^T,  o_t = e^{gamma_t} O1 + O2
-//         S     = e^{gamma_L} S0 + (diag(e^{gamma_L - gamma}) Delta)^T K
-//      The next chunk's tiles arrive by TMA while the current one is used.
+//      inter-chunk recurrence and the output, warp-specialised: one thread
+//      issues TMA loads, one issues MMAs, eight warps run the epilogues.  The
+//      fp32 state S (dv x dk) stays in tensor memory for the whole sequence;
+//      per chunk, with a bf16 copy S0 of the chunk's start state in shared
+//      memory as the MMA operand:
+//         Delta^T = V^T (T diag b)^T - S0 W^T       (both MMAs into one tile)
+//         S      <- e^{gamma_L} S + (diag(e^{gamma_L - gamma}) Delta)^T K
+//         O^T     = diag(e^gamma)-scaled S0 Q^T + Delta^T P^T
+//      The two MMAs that carry the state from chunk to chunk (S0 W^T, then
+//      the update of S) and their epilogues are the critical path; the output
+//      MMAs and the next chunk's loads run beside them.
 //
 // The algorithm is the chunked (WY/UT) form of the Gated DeltaNet recurrence
 // with chunk length 64, split into intra-chunk prep, inter-chunk state
 // recurrence and output, as the page "cf-1.com" (section "三个优化", item 2
 // "GDN prefill") describes its three kernels; that page keeps the state in
 // mma accumulator registers on Turing, here it lives in Blackwell tensor
-// memory.  Every MMA has M = 128 (the value or key dimension, or 64 keys
-// plus 64 queries), so no tensor-core issue slot is half empty.
+// memory and the next chunk's inputs arrive by TMA while the current one is
+// used.
 //
 // Tokens past the end of a sequence inside its last chunk get b = 0 and
 // g = 0, which zeroes their rows of W, U and Delta and keeps gamma_L at the
@@ -50,11 +56,19 @@ using namespace ptx;
 constexpr int C = 64;           // chunk length
 constexpr int D = 128;          // head dim (dk = dv)
 constexpr int kTile = 8192;     // bytes of one 64 x 64 bf16 swizzled tile
-constexpr int kPrepThreads = 192;
-constexpr int kChainThreads = 128;
+constexpr int kThreads = 320;   // 10 warps: 0 loads, 1 MMAs, 2-9 epilogue
+constexpr int kEpiThreads = 256;
 constexpr int kMaxSortSeqs = 4096;
 
 enum DeviceError : int { kErrNone = 0, kErrCuSeqlens = 1, kErrTimeout = 2 };
+
+// Per (chunk, value head) slot written by the prep kernel.
+constexpr int kSlotWT = 0;                    // W^T  [128 dk][64 tokens], MN-major B image
+constexpr int kSlotTB = kSlotWT + 2 * kTile;  // T diag(b) [64 out][64 in], K-major B image
+constexpr int kSlotP = kSlotTB + kTile;       // P [64 out][64 in], K-major B image
+constexpr int kSlotEG = kSlotP + kTile;       // e^{gamma_t}, fp32 [64]
+constexpr int kSlotDEC = kSlotEG + 256;       // e^{gamma_L - gamma_t}, fp32 [64]
+constexpr int kSlotBytes = kSlotDEC + 256;    // 33280
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
@@ -72,7 +86,7 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.order = align_up(w.chunk_off + 4 * (size_t)(p.num_seqs + 1), 256);
     w.table = align_up(w.order + 4 * (size_t)p.num_seqs, 256);
     w.tiles = align_up(w.table + 16 * (size_t)w.max_chunks, 1024);
-    w.total = w.tiles + (size_t)w.max_chunks * p.num_v_heads * 2 * kTile;
+    w.total = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
     return w;
 }
 
@@ -155,16 +169,6 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
     }
 }
 
-// ------------------------------------------------------------------ kernel 2
-struct PrepSmem {
-    uint8_t kq[4 * kTile];            // atom 0: K rows 0-63, Q rows 64-127; atom 1 likewise
-    float A[3][C][C + 4];             // A, then T, per value head of the round
-    float gam[3][C];
-    float beta[3][C];
-    uint64_t tma_bar;
-    uint64_t mma_bar;
-    uint32_t tmem;
-};
 
 // Inclusive prefix sum of g over one chunk (lane holds tokens 2l, 2l+1),
 // with g = 0 past the end of the sequence.  Optionally also b (0 past the
@@ -199,11 +203,59 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
     }
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+// ------------------------------------------------------------------ kernel 2
+constexpr int kPrepHeads = 3;  // value heads handled per round
+
+struct PrepSmem {
+    uint8_t kq[4 * kTile];                // atom 0: K rows 0-63 | Q rows 64-127; atom 1 likewise
+    uint8_t e[kPrepHeads][kTile];         // E (lower-left block of A), then T diag(b)
+    uint8_t dp[kPrepHeads][kTile];        // D' = blockdiag((I + A_bb)^-1)
+    uint8_t n[kPrepHeads][kTile];         // N = D' E, then T diag(b e^gamma)
+    float ad[kPrepHeads][2][32][36];      // the two diagonal 32 x 32 blocks of A, fp32
+    float gam[kPrepHeads][C];
+    float beta[kPrepHeads][C];
+    float eg[kPrepHeads][C];
+    float dec[kPrepHeads][C];
+    uint64_t tma_bar;
+    uint64_t mma_bar;
+    uint32_t tmem;
+};
+
+// TMEM columns of the prep kernel.
+constexpr uint32_t kPColKQ = 0;    // [K K^T; Q K^T], M = 128, 64 columns
+constexpr uint32_t kPColProd = 64; // + 64 j: N then Y = N D' of head j (M = 64 layout)
+constexpr uint32_t kPColW = 256;   // + 64 j: W^T of head j (M = 128)
+
+// Writes 8 floats as one 16-byte bf16 chunk.
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                      pack_bf16(x[6], x[7]));
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float *x) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&u[k]);
+        const float2 f = __bfloat1622float2(b2);
+        x[2 * k] = f.x;
+        x[2 * k + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float *__restrict__ g, const float *__restrict__ beta,
                 const int *__restrict__ chunk_off, const int4 *__restrict__ table,
-                uint8_t *__restrict__ tiles, int *__restrict__ err, int N, int Hk, int Hv) {
+                uint8_t *__restrict__ slots, int *__restrict__ err, int N, int Hk, int Hv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,6 +265,10 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int4 e = table[ch];
     const int tok0 = e.y, L = e.z;
     const int G = Hv / Hk;
+    // Epilogue warps 2-9: TMEM quadrant q (lanes 32q..32q+31), column half.
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int c0 = 32 * half;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 
     if (tid == 0) {
         prefetch_tensormap(&tm_q);
@@ -222,7 +278,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&sm.tmem, 64);
+        tmem_alloc(&sm.tmem, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -237,6 +293,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_3d(sm.kq + 3 * kTile, &tm_q, 64, hk, tok0, &sm.tma_bar);
     }
     bool bad = !mbar_wait(&sm.tma_bar, 0);
+    uint32_t mph = 0;
     if (tid == 0 && !bad) {
         tc_fence_after();
         const uint32_t base = smem_u32(sm.kq);
@@ -244,215 +301,295 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k / 4) * (2 * kTile) + (k % 4) * 32;
-            mma_bf16(tmem, smem_desc(base + off, 16, 1024), smem_desc(base + off, 16, 1024), id,
-                     k > 0);
+            mma_bf16(tmem + kPColKQ, smem_desc(base + off, 16, 1024),
+                     smem_desc(base + off, 16, 1024), id, k > 0);
         }
         mma_commit(&sm.mma_bar);
     }
-    bad |= !mbar_wait(&sm.mma_bar, 0);
-    tc_fence_after();
-    if (__syncthreads_or(bad)) {
-        if (tid == 0) atomicExch(err, kErrTimeout);
-        goto done;
-    }
-    {
-        // Rows of [K K^T; Q K^T]: warps 0-1 hold K K^T rows 0-63 (lanes 0-63),
-        // warps 2-3 hold Q K^T rows 0-63 (lanes 64-127).
-        float row[C];
-        if (warp < 4) {
-            uint32_t r[32];
-            const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16);
-            tmem_ld32(ta, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) row[j] = __uint_as_float(r[j]);
-            tmem_ld32(ta + 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) row[32 + j] = __uint_as_float(r[j]);
+    for (int j0 = 0; j0 < G; j0 += kPrepHeads) {
+        const int nh = min(kPrepHeads, G - j0);
+        if (warp >= 1 && warp <= nh) {
+            const int j = warp - 1, h = hk * G + j0 + j;
+            chunk_gamma(g, tok0, L, Hv, h, sm.gam[j], sm.beta[j], beta, sm.eg[j], sm.dec[j]);
+            float *slot_f = reinterpret_cast<float *>(slots + ((size_t)ch * Hv + h) * kSlotBytes);
+            slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[j][2 * lane];
+            slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
+            slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
+            slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
         }
-        const int rr = (warp & 1) * 32 + lane;  // row index 0..63 within K K^T or Q K^T
-        for (int j0 = 0; j0 < G; j0 += 3) {
-            const int nh = min(3, G - j0);
-            __syncthreads();  // previous round done with A / gam
-            if (warp < nh) {
-                const int h = hk * G + j0 + warp;
-                chunk_gamma(g, tok0, L, Hv, h, sm.gam[warp], sm.beta[warp], beta);
-            }
-            __syncthreads();
-            if (warp < 2) {
-                // A rows (strictly lower): A_ti = b_t e^{gamma_t - gamma_i} kk_ti.
+        if (j0 == 0) {
+            bad |= !mbar_wait(&sm.mma_bar, mph);
+            mph ^= 1;
+        }
+        tc_fence_after();
+        if (__syncthreads_or(bad)) break;
+        // ---- A blocks, E and P from the rows of [K K^T; Q K^T].
+        if (warp >= 2) {
+            const int row = 32 * q + lane;
+            float x[32];
+            tmem_ld32f(tmem + lane_base + kPColKQ + c0, x);
+            if (q < 2) {
+                const int t = row;
                 for (int j = 0; j < nh; ++j) {
-                    const float gt = sm.gam[j][rr], bt = sm.beta[j][rr];
+                    const float gt = sm.gam[j][t], bt = sm.beta[j][t];
 #pragma unroll
-                    for (int i = 0; i < C; ++i)
-                        sm.A[j][rr][i] = i < rr ? bt * expf(gt - sm.gam[j][i]) * row[i] : 0.f;
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float ev[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = c0 + 8 * cc + u;
+                            const float a = i < t ? bt * expf(gt - sm.gam[j][i]) * x[8 * cc + u] : 0.f;
+                            if ((t >> 5) == (i >> 5)) sm.ad[j][t >> 5][t & 31][i & 31] = a;
+                            ev[u] = (t >= 32 && i < 32) ? a : 0.f;
+                        }
+                        *reinterpret_cast<uint4 *>(sm.e[j] + swz(t, (c0 >> 3) + cc)) = pack8(ev);
+                    }
                 }
-            } else if (warp < 4) {
-                // P rows: P_ri = e^{gamma_r - gamma_i} qk_ri for i <= r, bf16, swizzled.
+            } else {
+                const int r = row - 64;
                 for (int j = 0; j < nh; ++j) {
                     const int h = hk * G + j0 + j;
-                    const float gr = sm.gam[j][rr];
-                    uint8_t *dst = tiles + (((size_t)ch * Hv + h) * 2 + 1) * kTile;
+                    const float gr = sm.gam[j][r];
+                    uint8_t *pdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotP;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w[4];
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float pv[8];
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const int i0 = 8 * c + 2 * x, i1 = i0 + 1;
-                            const float p0 = i0 <= rr ? expf(gr - sm.gam[j][i0]) * row[i0] : 0.f;
-                            const float p1 = i1 <= rr ? expf(gr - sm.gam[j][i1]) * row[i1] : 0.f;
-                            w[x] = pack_bf16(p0, p1);
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = c0 + 8 * cc + u;
+                            pv[u] = i <= r ? expf(gr - sm.gam[j][i]) * x[8 * cc + u] : 0.f;
                         }
-                        *reinterpret_cast<uint4 *>(dst + swz(rr, c)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv);
                     }
-                }
-            }
-            __syncthreads();
-            // T = (I + A)^-1, one column per thread, forward substitution.
-            const int j = tid / C, col = tid % C;
-            float tcol[C];
-            if (j < nh) {
-#pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    float a0 = (t == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                    const float *Arow = sm.A[j][t];
-#pragma unroll
-                    for (int i = 0; i < (t & ~3); i += 4) {
-                        const float4 av = *reinterpret_cast<const float4 *>(Arow + i);
-                        a0 = fmaf(-av.x, tcol[i], a0);
-                        a1 = fmaf(-av.y, tcol[i + 1], a1);
-                        a2 = fmaf(-av.z, tcol[i + 2], a2);
-                        a3 = fmaf(-av.w, tcol[i + 3], a3);
-                    }
-#pragma unroll
-                    for (int i = (t & ~3); i < t; ++i) a0 = fmaf(-Arow[i], tcol[i], a0);
-                    tcol[t] = (a0 + a1) + (a2 + a3);
-                }
-            }
-            __syncthreads();  // every column solve done reading A
-            if (j < nh) {
-#pragma unroll
-                for (int t = 0; t < C; ++t) sm.A[j][t][col] = tcol[t];
-            }
-            __syncthreads();
-            // T diag(b) rows -> bf16 swizzled tile.
-            if (j < nh) {
-                const int h = hk * G + j0 + j, t = col;
-                uint8_t *dst = tiles + (((size_t)ch * Hv + h) * 2 + 0) * kTile;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 x0 = *reinterpret_cast<const float4 *>(&sm.A[j][t][8 * c]);
-                    const float4 x1 = *reinterpret_cast<const float4 *>(&sm.A[j][t][8 * c + 4]);
-                    const float *b = &sm.beta[j][8 * c];
-                    *reinterpret_cast<uint4 *>(dst + swz(t, c)) = make_uint4(
-                        pack_bf16(x0.x * b[0], x0.y * b[1]), pack_bf16(x0.z * b[2], x0.w * b[3]),
-                        pack_bf16(x1.x * b[4], x1.y * b[5]), pack_bf16(x1.z * b[6], x1.w * b[7]));
                 }
             }
         }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- D' = blockdiag((I + A_bb)^-1): one column of one block per thread.
+        if (tid >= 64 && tid < 64 + 64 * nh) {
+            const int idx = tid - 64, j = idx >> 6, blk = (idx >> 5) & 1, col = idx & 31;
+            float xc[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                float a0 = (t == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                const float *Ar = sm.ad[j][blk][t];
+#pragma unroll
+                for (int i = 0; i < (t & ~3); i += 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(Ar + i);
+                    a0 = fmaf(-av.x, xc[i], a0);
+                    a1 = fmaf(-av.y, xc[i + 1], a1);
+                    a2 = fmaf(-av.z, xc[i + 2], a2);
+                    a3 = fmaf(-av.w, xc[i + 3], a3);
+                }
+#pragma unroll
+                for (int i = (t & ~3); i < t; ++i) a0 = fmaf(-Ar[i], xc[i], a0);
+                xc[t] = (a0 + a1) + (a2 + a3);
+            }
+            const int ccol = 32 * blk + col;
+            uint8_t *dp = sm.dp[j];
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                const float val = ((t >> 5) == blk) ? xc[t & 31] : 0.f;
+                *reinterpret_cast<__nv_bfloat16 *>(dp + swz(t, ccol >> 3) + 2 * (ccol & 7)) =
+                    __float2bfloat16_rn(val);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- N = D' E  (M = 64, N = 64, K = 64)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+            for (int j = 0; j < nh; ++j) {
+                const uint32_t a = smem_u32(sm.dp[j]), b = smem_u32(sm.e[j]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
+                             smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
+            }
+            mma_commit(&sm.mma_bar);
+        }
+        bad |= !mbar_wait(&sm.mma_bar, mph);
+        mph ^= 1;
+        tc_fence_after();
+        if (warp >= 2) {
+            for (int j = 0; j < nh; ++j) {
+                float x[32];
+                tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, x);
+                if (lane < 16) {
+                    const int r = 16 * q + lane;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        *reinterpret_cast<uint4 *>(sm.n[j] + swz(r, (c0 >> 3) + cc)) =
+                            pack8(x + 8 * cc);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(bad)) break;
+        // ---- Y = N D'  (M = 64, N = 64, K = 64), into the same columns
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+            for (int j = 0; j < nh; ++j) {
+                const uint32_t a = smem_u32(sm.n[j]), b = smem_u32(sm.dp[j]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
+                             smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
+            }
+            mma_commit(&sm.mma_bar);
+        }
+        bad |= !mbar_wait(&sm.mma_bar, mph);
+        mph ^= 1;
+        tc_fence_after();
+        // ---- T = D' - Y;  T diag(b) -> e (and the workspace), T diag(b e^gamma) -> n
+        if (warp >= 2) {
+            for (int j = 0; j < nh; ++j) {
+                float y[32];
+                tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, y);
+                if (lane < 16) {
+                    const int r = 16 * q + lane, h = hk * G + j0 + j;
+                    uint8_t *tdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotTB;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t off = swz(r, (c0 >> 3) + cc);
+                        float dv[8], tb[8], tbg[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(sm.dp[j] + off), dv);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = c0 + 8 * cc + u;
+                            tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[j][i];
+                            tbg[u] = tb[u] * sm.eg[j][i];
+                        }
+                        const uint4 wtb = pack8(tb);
+                        *reinterpret_cast<uint4 *>(sm.e[j] + off) = wtb;
+                        *reinterpret_cast<uint4 *>(sm.n[j] + off) = pack8(tbg);
+                        *reinterpret_cast<uint4 *>(tdst + off) = wtb;
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(bad)) break;
+        // ---- W^T = K^T (T diag(b e^gamma))^T  (M = 128 dk, N = 64, K = 64 tokens)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(128, 64, true, false);
+            const uint32_t a = smem_u32(sm.kq);
+            for (int j = 0; j < nh; ++j) {
+                const uint32_t b = smem_u32(sm.n[j]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + kPColW + 64 * j, smem_desc(a + 2048 * k, 2 * kTile, 1024),
+                             smem_desc(b + 32 * k, 16, 1024), id, k > 0);
+            }
+            mma_commit(&sm.mma_bar);
+        }
+        bad |= !mbar_wait(&sm.mma_bar, mph);
+        mph ^= 1;
+        tc_fence_after();
+        if (warp >= 2) {
+            const int row = 32 * q + lane;  // key dimension
+            for (int j = 0; j < nh; ++j) {
+                const int h = hk * G + j0 + j;
+                float x[32];
+                tmem_ld32f(tmem + lane_base + kPColW + 64 * j + c0, x);
+                uint8_t *wdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotWT;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(wdst + swz(row, (c0 >> 3) + cc)) = pack8(x + 8 * cc);
+            }
+        }
+        tc_fence_before();
+        if (__syncthreads_or(bad)) break;
     }
-done:
+    if (bad && tid == 0) atomicExch(err, kErrTimeout);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ kernel 3
 struct ChainStage {
-    uint8_t k[2 * kTile];   // K tile: [64 tokens][128 dk] as two 64-column atoms
-    uint8_t q[2 * kTile];
-    uint8_t v[2 * kTile];
-    uint8_t tb[kTile];      // T diag(b)       [64 out tokens][64 in tokens]
-    uint8_t p[kTile];       // M o Q K^T       [64 out tokens][64 in tokens]
+    uint8_t k[2 * kTile];   // K [64 tokens][128 dk] as two 64-column atoms
+    uint8_t q[2 * kTile];   // Q, likewise
+    uint8_t v[2 * kTile];   // V [64 tokens][128 dv]
+    uint8_t wt[2 * kTile];  // W^T [128 dk][64 tokens], MN-major B image
+    uint8_t tb[kTile];      // T diag(b)
+    uint8_t p[kTile];       // P = M o Q K^T
 };
 
 struct ChainSmem {
     ChainStage st[2];
-    uint8_t tbg[kTile];     // T diag(b e^gamma)
-    uint8_t s16[4 * kTile]; // S0 bf16, K-major: [128 dv][128 dk] as two atoms
-    uint8_t wt[2 * kTile];  // W^T bf16, MN-major B operand: [128 dk rows][64 tokens]
-    uint8_t dt[2 * kTile];  // Delta^T bf16: [128 dv][64 tokens]
-    uint8_t dts[2 * kTile]; // Delta^T diag(e^{gamma_L - gamma})
-    float gam[2][C];
-    float eg[2][C];         // e^{gamma_t}
-    float dec[2][C];        // e^{gamma_L - gamma_t}
-    uint64_t full[2];
-    uint64_t mma_bar;
+    uint8_t s16[4 * kTile];  // S0 bf16, K-major: [128 dv][128 dk] as two atoms
+    uint8_t dt[2 * kTile];   // Delta^T bf16 [128 dv][64 tokens]
+    uint8_t dts[2 * kTile];  // Delta^T diag(e^{gamma_L - gamma})
+    float egdec[2][2 * C];   // per stage: e^{gamma_t} then e^{gamma_L - gamma_t}
+    uint64_t full[2];        // stage loaded (TMA transaction count)
+    uint64_t empty[2];       // stage consumed (1 MMA commit + 256 epilogue threads)
+    uint64_t s16_ready;      // epilogue: S0 copy (and pre-scaled S) ready
+    uint64_t dt_ready;       // epilogue: Delta^T copies ready
+    uint64_t o_free;         // epilogue: output accumulators read
+    uint64_t d_done;         // MMA: Delta^T complete
+    uint64_t s_done;         // MMA: state update complete
+    uint64_t o_done;         // MMA: output accumulators complete
+    uint64_t fin;            // MMA: everything issued has completed
     uint32_t tmem;
+    int abort;
+    int issued;
 };
 
-// TMEM columns
-constexpr uint32_t kColU = 0, kColW = 64, kColO1 = 128, kColO2 = 192, kColS = 256;
+constexpr uint32_t kStageBytes = 6 * kTile + 2 * kTile + 512;  // tiles + W^T + e^gamma/dec
+// TMEM columns of the chain kernel.
+constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColS = 256;
 
-__device__ __forceinline__ void chain_issue_loads(ChainSmem &sm, int s, const CUtensorMap *tq,
-                                                  const CUtensorMap *tk, const CUtensorMap *tv,
-                                                  const uint8_t *tiles, int ch, int h, int hk,
-                                                  int Hv, int tok0) {
-    ChainStage &st = sm.st[s];
-    uint64_t *bar = &sm.full[s];
-    mbar_arrive_expect_tx(bar, 8 * kTile);
-    tma_load_3d(st.k, tk, 0, hk, tok0, bar);
-    tma_load_3d(st.k + kTile, tk, 64, hk, tok0, bar);
-    tma_load_3d(st.q, tq, 0, hk, tok0, bar);
-    tma_load_3d(st.q + kTile, tq, 64, hk, tok0, bar);
-    tma_load_3d(st.v, tv, 0, h, tok0, bar);
-    tma_load_3d(st.v + kTile, tv, 64, h, tok0, bar);
-    const uint8_t *src = tiles + ((size_t)ch * Hv + h) * 2 * kTile;
-    bulk_load(st.tb, src, kTile, bar);
-    bulk_load(st.p, src + kTile, kTile, bar);
-}
-
-// Loads the 64 columns [col, col + 64) of this thread's TMEM lane as floats.
-__device__ __forceinline__ void tmem_row64(uint32_t taddr, float (&x)[64]) {
-    uint32_t r[32];
-    tmem_ld32(taddr, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-    tmem_ld32(taddr + 32, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(r[j]);
-}
-
-// Writes 64 floats as one bf16 swizzled row (128 bytes) of a K-major or
-// MN-major atom column.
-__device__ __forceinline__ void store_row_bf16(uint8_t *atom, int row, const float (&x)[64]) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4 *>(atom + swz(row, c)) =
-            make_uint4(pack_bf16(x[8 * c], x[8 * c + 1]), pack_bf16(x[8 * c + 2], x[8 * c + 3]),
-                       pack_bf16(x[8 * c + 4], x[8 * c + 5]), pack_bf16(x[8 * c + 6], x[8 * c + 7]));
+// Bounded wait that also gives up as soon as another role of the CTA has.
+__device__ __forceinline__ bool chain_wait(ChainSmem &sm, uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    volatile int *ab = &sm.abort;
+    while (!mbar_try_wait(bar, parity)) {
+        if (*ab) return false;
+        if (clock64() - t0 > 4000000000ll) {
+            *ab = 1;
+            return false;
+        }
     }
+    return true;
 }
 
-__global__ void __launch_bounds__(kChainThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
-                 const int *__restrict__ chunk_off, const int *__restrict__ order,
-                 const int4 *__restrict__ table, const uint8_t *__restrict__ tiles,
-                 const float *__restrict__ h0, __nv_bfloat16 *__restrict__ out,
-                 float *__restrict__ hT, int *__restrict__ err, int N, int Hk, int Hv) {
+                 const __grid_constant__ CUtensorMap tm_v, const int *__restrict__ chunk_off,
+                 const int *__restrict__ order, const int4 *__restrict__ table,
+                 const uint8_t *__restrict__ slots, const float *__restrict__ h0,
+                 __nv_bfloat16 *__restrict__ out, float *__restrict__ hT,
+                 int *__restrict__ err, int N, int Hk, int Hv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = order[blockIdx.x / Hv], h = blockIdx.x % Hv;
     const int hk = h / (Hv / Hk);
     const int c_begin = chunk_off[n], nc = chunk_off[n + 1] - c_begin;
     const size_t state_off = ((size_t)n * Hv + h) * D * D;
-    const int j = tid;  // the TMEM lane / state row this thread owns
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    // Epilogue warps 2-9: TMEM quadrant q, state row j, column half.
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int j = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 
     if (nc == 0) {
         // Empty sequence (or a rejected chunk table): final state = initial state.
         if (hT && !(chunk_off[N] == 0 && *err != kErrNone)) {
-            for (int c = 0; c < D; c += 4) {
-                float4 x = h0 ? *reinterpret_cast<const float4 *>(h0 + state_off + j * D + c)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(hT + state_off + j * D + c) = x;
+            for (int i = tid; i < D * D / 4; i += kThreads) {
+                const float4 x = h0 ? reinterpret_cast<const float4 *>(h0 + state_off)[i]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(hT + state_off)[i] = x;
             }
         }
         return;
@@ -462,9 +599,19 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
-        mbar_init(&sm.full[0], 1);
-        mbar_init(&sm.full[1], 1);
-        mbar_init(&sm.mma_bar, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1 + kEpiThreads);
+        }
+        mbar_init(&sm.s16_ready, kEpiThreads);
+        mbar_init(&sm.dt_ready, kEpiThreads);
+        mbar_init(&sm.o_free, kEpiThreads);
+        mbar_init(&sm.d_done, 1);
+        mbar_init(&sm.s_done, 1);
+        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.fin, 1);
+        sm.abort = 0;
+        sm.issued = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -475,228 +622,219 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
-    const uint32_t tS = tmem + lane_off + kColS;
 
-    int issued = 0;   // chunks whose loads have been issued
-    if (tid == 0) {
-        for (; issued < min(2, nc); ++issued) {
-            const int4 e = table[c_begin + issued];
-            chain_issue_loads(sm, issued, &tm_q, &tm_k, &tm_v, tiles, c_begin + issued, h, hk, Hv,
-                              e.y);
-        }
-    }
     if (warp == 0) {
-        const int4 e0 = table[c_begin];
-        chunk_gamma(g, e0.y, e0.z, Hv, h, sm.gam[0], nullptr, nullptr, sm.eg[0], sm.dec[0]);
-        if (nc > 1) {
-            const int4 e1 = table[c_begin + 1];
-            chunk_gamma(g, e1.y, e1.z, Hv, h, sm.gam[1], nullptr, nullptr, sm.eg[1], sm.dec[1]);
+        // ---------------- producer: TMA tiles and the prep kernel's slot
+        if (lane == 0) {
+            for (int c = 0; c < nc; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !chain_wait(sm, &sm.empty[s], ((c >> 1) + 1) & 1)) break;
+                const int ch = c_begin + c;
+                const int tok0 = table[ch].y;
+                ChainStage &st = sm.st[s];
+                uint64_t *bar = &sm.full[s];
+                const uint8_t *slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
+                mbar_arrive_expect_tx(bar, kStageBytes);
+                tma_load_3d(st.k, &tm_k, 0, hk, tok0, bar);
+                tma_load_3d(st.k + kTile, &tm_k, 64, hk, tok0, bar);
+                tma_load_3d(st.q, &tm_q, 0, hk, tok0, bar);
+                tma_load_3d(st.q + kTile, &tm_q, 64, hk, tok0, bar);
+                tma_load_3d(st.v, &tm_v, 0, h, tok0, bar);
+                tma_load_3d(st.v + kTile, &tm_v, 64, h, tok0, bar);
+                bulk_load(st.wt, slot + kSlotWT, 2 * kTile, bar);
+                bulk_load(st.tb, slot + kSlotTB, kTile, bar);
+                bulk_load(st.p, slot + kSlotP, kTile, bar);
+                bulk_load(sm.egdec[s], slot + kSlotEG, 512, bar);
+                sm.issued = c + 1;
+            }
         }
-    }
-    __syncthreads();
-    // Initial state: bf16 copy to smem, fp32 copy (pre-scaled by the first
-    // chunk's total decay) to TMEM.
-    {
-        const float scale = expf(sm.gam[0][C - 1]);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t s16 = smem_u32(sm.s16), dt = smem_u32(sm.dt), dts = smem_u32(sm.dts);
+            for (int c = 0; c < nc; ++c) {
+                const int s = c & 1;
+                ChainStage &st = sm.st[s];
+                const uint32_t kt = smem_u32(st.k), qt = smem_u32(st.q), vt = smem_u32(st.v),
+                               wt = smem_u32(st.wt), tb = smem_u32(st.tb), pt = smem_u32(st.p);
+                if (!chain_wait(sm, &sm.full[s], (c >> 1) & 1)) break;
+                tc_fence_after();
+                // U^T = V^T (T diag b)^T                  [M=128 dv, N=64, K=64]
+                constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + kColD, smem_desc(vt + 2048 * k, kTile, 1024),
+                             smem_desc(tb + 32 * k, 16, 1024), id_u, k > 0);
+                if (!chain_wait(sm, &sm.s16_ready, c & 1)) break;
+                tc_fence_after();
+                // Delta^T = U^T - S0 W^T                 [M=128 dv, N=64, K=128 dk]
+                constexpr uint32_t id_d = idesc_bf16(128, 64, false, true, true);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + kColD,
+                             smem_desc(s16 + (k / 4) * 2 * kTile + (k % 4) * 32, 16, 1024),
+                             smem_desc(wt + 2048 * k, kTile, 1024), id_d, 1);
+                mma_commit(&sm.d_done);
+                if (c > 0 && !chain_wait(sm, &sm.o_free, (c - 1) & 1)) break;
+                tc_fence_after();
+                // O1^T = S0 Q^T                          [M=128 dv, N=64, K=128 dk]
+                constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + kColO1,
+                             smem_desc(s16 + (k / 4) * 2 * kTile + (k % 4) * 32, 16, 1024),
+                             smem_desc(qt + (k / 4) * kTile + (k % 4) * 32, 16, 1024), id_o,
+                             k > 0);
+                if (!chain_wait(sm, &sm.dt_ready, c & 1)) break;
+                tc_fence_after();
+                // S += (diag(e^{gamma_L - gamma}) Delta)^T K   [M=128 dv, N=128 dk, K=64]
+                constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + kColS, smem_desc(dts + 32 * k, 16, 1024),
+                             smem_desc(kt + 2048 * k, kTile, 1024), id_s, 1);
+                mma_commit(&sm.s_done);
+                // O2^T = Delta^T P^T                     [M=128 dv, N=64, K=64]
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + kColO2, smem_desc(dt + 32 * k, 16, 1024),
+                             smem_desc(pt + 32 * k, 16, 1024), id_o, k > 0);
+                mma_commit(&sm.o_done);
+                mma_commit(&sm.empty[s]);
+            }
+            mma_commit(&sm.fin);
+        }
+    } else {
+        // ---------------- epilogue warps 2-9: row j of every 128-row tile,
+        // columns [32 half, 32 half + 32) of the 64-wide ones and
+        // [64 half, 64 half + 64) of the state.
+        const int c32 = 32 * half, c64 = 64 * half;
+        bool ok = chain_wait(sm, &sm.full[0], 0);
+        if (ok) {
+            // Initial state: bf16 copy for S0, fp32 copy pre-scaled by the
+            // first chunk's total decay e^{gamma_L}.
+            const float scale = sm.egdec[0][C - 1];
             float x[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
                 const float4 v4 = h0 ? *reinterpret_cast<const float4 *>(
-                                           h0 + state_off + (size_t)j * D + half * 64 + c)
+                                           h0 + state_off + (size_t)j * D + c64 + c)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[c] = v4.x; x[c + 1] = v4.y; x[c + 2] = v4.z; x[c + 3] = v4.w;
             }
-            store_row_bf16(sm.s16 + half * 2 * kTile, j, x);
-            uint32_t r[32];
+            uint8_t *atom = sm.s16 + half * 2 * kTile;
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(atom + swz(j, cc)) = pack8(x + 8 * cc);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(scale * x[32 * q2 + c]);
-                tmem_st32(tS + half * 64 + 32 * q2, r);
-            }
-        }
-        tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    uint32_t mma_phase = 0;
-    bool bad = false;
-    const uint32_t s16 = smem_u32(sm.s16), wt = smem_u32(sm.wt), dt = smem_u32(sm.dt),
-                   dts = smem_u32(sm.dts), tbg = smem_u32(sm.tbg);
-    for (int c = 0; c < nc; ++c) {
-        const int s = c & 1;
-        ChainStage &st = sm.st[s];
-        const int4 e = table[c_begin + c];
-        const int tok0 = e.y, L = e.z;
-        const float *eg = sm.eg[s];
-        const float *dec = sm.dec[s];
-        bad |= !mbar_wait(&sm.full[s], (c >> 1) & 1);
-        // T diag(b e^gamma) from T diag(b): scale column i by e^{gamma_i}.
-        if (tid < C) {
+            for (int p2 = 0; p2 < 2; ++p2) {
+                uint32_t r[32];
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                uint4 w = *reinterpret_cast<const uint4 *>(st.tb + swz(tid, cc));
-                uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&wp[x]);
-                    const float2 f = __bfloat1622float2(b2);
-                    wp[x] = pack_bf16(f.x * eg[8 * cc + 2 * x], f.y * eg[8 * cc + 2 * x + 1]);
-                }
-                *reinterpret_cast<uint4 *>(sm.tbg + swz(tid, cc)) = w;
-            }
-        }
-        fence_proxy_async_smem();
-        if (__syncthreads_or(bad)) break;
-        const uint32_t kt = smem_u32(st.k), qt = smem_u32(st.q), vt = smem_u32(st.v),
-                       tb = smem_u32(st.tb), pt = smem_u32(st.p);
-        if (tid == 0) {
-            tc_fence_after();
-            // U^T = V^T (T diag b)^T ; W^T = K^T (T diag(b e^gamma))^T   [M=128, N=64, K=64]
-            constexpr uint32_t id = idesc_bf16(128, 64, true, false);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + kColU, smem_desc(vt + k * 2048, kTile, 1024),
-                         smem_desc(tb + k * 32, 16, 1024), id, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + kColW, smem_desc(kt + k * 2048, kTile, 1024),
-                         smem_desc(tbg + k * 32, 16, 1024), id, k > 0);
-            mma_commit(&sm.mma_bar);
-        }
-        bad |= !mbar_wait(&sm.mma_bar, mma_phase);
-        mma_phase ^= 1;
-        tc_fence_after();
-        {
-            float w[64];
-            tmem_row64(tmem + lane_off + kColW, w);
-            store_row_bf16(sm.wt, j, w);   // row = key dim j, 64 tokens
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            // Delta^T = U^T - S0 W^T   [M=128 dv, N=64 tokens, K=128 dk]
-            constexpr uint32_t idn = idesc_bf16(128, 64, false, true, true);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_bf16(tmem + kColU, smem_desc(s16 + (k / 4) * 2 * kTile + (k % 4) * 32, 16, 1024),
-                         smem_desc(wt + k * 2048, kTile, 1024), idn, 1);
-            // O1^T = S0 Q^T   [M=128 dv, N=64 tokens, K=128 dk]
-            constexpr uint32_t id = idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_bf16(tmem + kColO1,
-                         smem_desc(s16 + (k / 4) * 2 * kTile + (k % 4) * 32, 16, 1024),
-                         smem_desc(qt + (k / 4) * kTile + (k % 4) * 32, 16, 1024), id, k > 0);
-            mma_commit(&sm.mma_bar);
-        }
-        bad |= !mbar_wait(&sm.mma_bar, mma_phase);
-        mma_phase ^= 1;
-        tc_fence_after();
-        {
-            float d[64];
-            tmem_row64(tmem + lane_off + kColU, d);
-            store_row_bf16(sm.dt, j, d);
-#pragma unroll
-            for (int t = 0; t < 64; ++t) d[t] *= dec[t];
-            store_row_bf16(sm.dts, j, d);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            // O2^T = Delta^T P^T   [M=128 dv, N=64 tokens, K=64 tokens]
-            constexpr uint32_t id = idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + kColO2, smem_desc(dt + k * 32, 16, 1024),
-                         smem_desc(pt + k * 32, 16, 1024), id, k > 0);
-            // S += (diag(e^{gamma_L - gamma}) Delta)^T K   [M=128 dv, N=128 dk, K=64 tokens]
-            constexpr uint32_t ids = idesc_bf16(128, 128, false, true);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + kColS, smem_desc(dts + k * 32, 16, 1024),
-                         smem_desc(kt + k * 2048, kTile, 1024), ids, 1);
-            mma_commit(&sm.mma_bar);
-        }
-        bad |= !mbar_wait(&sm.mma_bar, mma_phase);
-        mma_phase ^= 1;
-        tc_fence_after();
-        {
-            // Output: o_t = e^{gamma_t} O1 + O2, this thread's value dim j.
-            float o1[64], o2[64];
-            tmem_row64(tmem + lane_off + kColO1, o1);
-            tmem_row64(tmem + lane_off + kColO2, o2);
-            __nv_bfloat16 *op = out + ((size_t)tok0 * Hv + h) * D + j;
-            const size_t tstride = (size_t)Hv * D;
-#pragma unroll
-            for (int t = 0; t < 64; ++t)
-                if (t < L) op[t * tstride] = __float2bfloat16_rn(fmaf(eg[t], o1[t], o2[t]));
-        }
-        {
-            // State: bf16 copy for the next chunk and pre-scale by its decay,
-            // or the final state after the last chunk.
-            const bool last = (c == nc - 1);
-            const float scale = last ? 1.f : expf(sm.gam[s ^ 1][C - 1]);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float x[64];
-                tmem_row64(tS + half * 64, x);
-                if (last) {
-                    if (hT) {
-                        float *dst = hT + state_off + (size_t)j * D + half * 64;
-#pragma unroll
-                        for (int cc = 0; cc < 64; cc += 4)
-                            *reinterpret_cast<float4 *>(dst + cc) =
-                                make_float4(x[cc], x[cc + 1], x[cc + 2], x[cc + 3]);
-                    }
-                } else {
-                    store_row_bf16(sm.s16 + half * 2 * kTile, j, x);
-                    uint32_t r[32];
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-#pragma unroll
-                        for (int cc = 0; cc < 32; ++cc)
-                            r[cc] = __float_as_uint(scale * x[32 * q2 + cc]);
-                        tmem_st32(tS + half * 64 + 32 * q2, r);
-                    }
-                }
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(scale * x[32 * p2 + i]);
+                tmem_st32(tmem + lane_base + kColS + c64 + 32 * p2, r);
             }
             tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.s16_ready);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) break;
-        // Stage s is free: prefetch chunk c + 2 into it.
-        if (c + 2 < nc) {
-            const int4 e2 = table[c_begin + c + 2];
-            if (tid == 0) {
-                chain_issue_loads(sm, s, &tm_q, &tm_k, &tm_v, tiles, c_begin + c + 2, h, hk, Hv,
-                                  e2.y);
-                ++issued;
+        for (int c = 0; ok && c < nc; ++c) {
+            const int s = c & 1;
+            const int4 e = table[c_begin + c];
+            const int tok0 = e.y, L = e.z;
+            const float *eg = sm.egdec[s];
+            const float *dec = sm.egdec[s] + C;
+            // E3: Delta^T row j -> bf16 copies (plain and decayed to the chunk end)
+            if (!(ok = chain_wait(sm, &sm.d_done, c & 1))) break;
+            tc_fence_after();
+            {
+                float d[32];
+                tmem_ld32f(tmem + lane_base + kColD + c32, d);
+                float ds[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) ds[t] = d[t] * dec[c32 + t];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    *reinterpret_cast<uint4 *>(sm.dt + swz(j, 4 * half + cc)) = pack8(d + 8 * cc);
+                    *reinterpret_cast<uint4 *>(sm.dts + swz(j, 4 * half + cc)) = pack8(ds + 8 * cc);
+                }
             }
-            if (warp == 1)
-                chunk_gamma(g, e2.y, e2.z, Hv, h, sm.gam[s], nullptr, nullptr, sm.eg[s], sm.dec[s]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.dt_ready);
+            // E6: the updated state -> next chunk's S0 and pre-scaled fp32 state,
+            // or the final state after the last chunk.
+            if (!(ok = chain_wait(sm, &sm.s_done, c & 1))) break;
+            tc_fence_after();
+            {
+                float x[64];
+                {
+                    float a[32], b[32];
+                    tmem_ld32f(tmem + lane_base + kColS + c64, a);
+                    tmem_ld32f(tmem + lane_base + kColS + c64 + 32, b);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) { x[i] = a[i]; x[32 + i] = b[i]; }
+                }
+                if (c == nc - 1) {
+                    if (hT) {
+                        float *dst = hT + state_off + (size_t)j * D + c64;
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                    }
+                } else {
+                    uint8_t *atom = sm.s16 + half * 2 * kTile;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4 *>(atom + swz(j, cc)) = pack8(x + 8 * cc);
+                    if (!(ok = chain_wait(sm, &sm.full[s ^ 1], ((c + 1) >> 1) & 1))) break;
+                    const float scale = sm.egdec[s ^ 1][C - 1];
+#pragma unroll
+                    for (int p2 = 0; p2 < 2; ++p2) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(scale * x[32 * p2 + i]);
+                        tmem_st32(tmem + lane_base + kColS + c64 + 32 * p2, r);
+                    }
+                    tmem_st_wait();
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&sm.s16_ready);
+                }
+            }
+            // E5: output o_t = e^{gamma_t} O1 + O2 for value dim j.
+            if (!(ok = chain_wait(sm, &sm.o_done, c & 1))) break;
+            tc_fence_after();
+            {
+                float o1[32], o2[32];
+                tmem_ld32f(tmem + lane_base + kColO1 + c32, o1);
+                tmem_ld32f(tmem + lane_base + kColO2 + c32, o2);
+                __nv_bfloat16 *op = out + ((size_t)(tok0 + c32) * Hv + h) * D + j;
+                const size_t tstride = (size_t)Hv * D;
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (c32 + t < L)
+                        op[t * tstride] = __float2bfloat16_rn(fmaf(eg[c32 + t], o1[t], o2[t]));
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.o_free);
+            mbar_arrive(&sm.empty[s]);
         }
-        __syncthreads();
     }
-    if (bad) {
+    __syncthreads();
+    if (sm.abort) {
         if (tid == 0) {
             atomicExch(err, kErrTimeout);
             // Let loads still in flight land before the CTA leaves.
-            for (int c = 0; c < nc && c < issued; ++c) mbar_wait(&sm.full[c & 1], (c >> 1) & 1, 100000000ll);
+            for (int c = max(0, sm.issued - 2); c < sm.issued; ++c)
+                mbar_wait(&sm.full[c & 1], (c >> 1) & 1, 200000000ll);
         }
     }
+    if (tid == 32) mbar_wait(&sm.fin, 0, 200000000ll);
     tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -747,7 +885,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     int *chunk_off = reinterpret_cast<int *>(ws + w.chunk_off);
     int *order = reinterpret_cast<int *>(ws + w.order);
     int4 *table = reinterpret_cast<int4 *>(ws + w.table);
-    uint8_t *tiles = ws + w.tiles;
+    uint8_t *slots = ws + w.tiles;
 
     CUtensorMap tq, tk, tv;
     if (p.total_tokens > 0) {
@@ -771,17 +909,17 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
                                  (int)smem) != cudaSuccess)
             return GDN_ERR_CUDA;
         dim3 grid((unsigned)w.max_chunks, p.num_k_heads);
-        gdn_prep_kernel<<<grid, kPrepThreads, smem, stream>>>(tq, tk, g, beta, chunk_off, table,
-                                                              tiles, err, p.num_seqs,
-                                                              p.num_k_heads, p.num_v_heads);
+        gdn_prep_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, g, beta, chunk_off, table, slots,
+                                                          err, p.num_seqs, p.num_k_heads,
+                                                          p.num_v_heads);
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
     const size_t smem = sizeof(ChainSmem) + 1024;
     if (cudaFuncSetAttribute(gdn_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
-    gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
-        tq, tk, tv, g, chunk_off, order, table, tiles, h0, static_cast<__nv_bfloat16 *>(out), hT,
+    gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kThreads, smem, stream>>>(
+        tq, tk, tv, chunk_off, order, table, slots, h0, static_cast<__nv_bfloat16 *>(out), hT,
         err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -10,6 +10,8 @@
 //   2: A K-major [128 x K], B MN-major (B stored [K][N])      (K = 64,  N = 128)
 //   3: mode 0 with A negated, accumulated onto mode 0's result
 //   4: A K-major [128 x K], B MN-major (B stored [K][N])      (K = 128, N = 64)
+//   5: M = 64: A K-major [64 x K], B MN-major [K][N]          (K = 64,  N = 64);
+//      all 128 TMEM lanes are dumped so the host can map rows to lanes
 // Inputs (host-provided, row-major fp32, rounded to bf16 here):
 //   a: mode 0/2/3/4: [128][K];  mode 1: [K][128]  (i.e. A^T)
 //   b: mode 0/1/3:   [N][K];    mode 2/4: [K][N]
@@ -40,16 +42,19 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t tslot;
     const int tid = threadIdx.x, warp = tid / 32;
-    const int K = (mode == 1 || mode == 2) ? 64 : 128;
+    const int K = (mode == 1 || mode == 2 || mode == 5) ? 64 : 128;
+    const int M = (mode == 5) ? 64 : 128;
     const int N = (mode == 2) ? 128 : 64;
 
+    if (mode == 5)
+        for (int i = tid; i < 128 * 64; i += 128) d[i] = 0.f;
     // Stage operands.
     if (mode == 1) {            // A^T stored [K rows][128 M]: MN-major, atoms over M
         for (int i = tid; i < K * 128; i += 128) put(sa, K, i / 128, i % 128, a[i]);
-    } else {                    // A [128 rows][K]: K-major, atoms over K
-        for (int i = tid; i < 128 * K; i += 128) put(sa, 128, i / K, i % K, a[i]);
+    } else {                    // A [M rows][K]: K-major, atoms over K
+        for (int i = tid; i < M * K; i += 128) put(sa, M, i / K, i % K, a[i]);
     }
-    if (mode == 2 || mode == 4) {  // B stored [K rows][N]: MN-major, atoms over N
+    if (mode == 2 || mode == 4 || mode == 5) {  // B stored [K rows][N]: MN-major, atoms over N
         for (int i = tid; i < K * N; i += 128) put(sb, K, i / N, i % N, b[i]);
     } else {                    // B [N rows][K]: K-major
         for (int i = tid; i < N * K; i += 128) put(sb, N, i / K, i % K, b[i]);
@@ -76,12 +81,12 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
                 if (mode == 1)
                     ad = smem_desc(a0 + k * 2048, K * 128, 1024);
                 else
-                    ad = smem_desc(a0 + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024);
-                if (mode == 2 || mode == 4)
+                    ad = smem_desc(a0 + (k / 4) * (M * 128) + (k % 4) * 32, 16, 1024);
+                if (mode == 2 || mode == 4 || mode == 5)
                     bd = smem_desc(b0 + k * 2048, K * 128, 1024);
                 else
                     bd = smem_desc(b0 + (k / 4) * (N * 128) + (k % 4) * 32, 16, 1024);
-                const uint32_t id = idesc_bf16(128, N, mode == 1, mode == 2 || mode == 4,
+                const uint32_t id = idesc_bf16(M, N, mode == 1, mode == 2 || mode == 4 || mode == 5,
                                                rep == 1);
                 mma_bf16(tmem, ad, bd, id, (k > 0 || rep > 0) ? 1u : 0u);
             }

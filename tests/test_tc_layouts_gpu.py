@@ -52,3 +52,27 @@ def test_layout(probe, mode):
     assert rc == 0 and int(st.item()) == 0
     got = dd.cpu().double().numpy()
     assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(A @ B).max())
+
+
+def test_m64_lane_layout(probe):
+    """M = 64: find which TMEM lane holds each row of D, and check the values.
+    The mapping found is printed; rows must land on distinct lanes."""
+    rng = np.random.default_rng(5)
+    a = rng.standard_normal((64, 64)).astype(np.float32)
+    b = rng.standard_normal((64, 64)).astype(np.float32)
+    ref = bf(a) @ bf(b)
+    da = torch.from_numpy(a).cuda()
+    db = torch.from_numpy(b).cuda()
+    dd = torch.full((128, 64), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe_run(da.data_ptr(), db.data_ptr(), dd.data_ptr(), 5, st.data_ptr())
+    assert rc == 0 and int(st.item()) == 0
+    got = dd.cpu().double().numpy()
+    lanes = []
+    for r in range(64):
+        err = np.abs(got - ref[r][None, :]).max(axis=1)
+        lane = int(np.argmin(err))
+        assert err[lane] <= 1e-4 * max(1.0, np.abs(ref).max()), f"row {r} not found"
+        lanes.append(lane)
+    print("M=64 row->lane:", lanes)
+    assert len(set(lanes)) == 64
