@@ -544,7 +544,7 @@ struct ChainSmem {
     int issued;
 };
 
-constexpr uint32_t kStageBytes = 6 * kTile + 2 * kTile + 512;  // tiles + W^T + e^gamma/dec
+constexpr uint32_t kStageBytes = 10 * kTile + 512;  // K, Q, V, W^T, T diag b, P, e^gamma/dec
 // TMEM columns of the chain kernel.
 constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColS = 256;
 
