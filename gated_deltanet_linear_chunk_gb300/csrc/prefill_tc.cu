@@ -57,8 +57,8 @@ constexpr int C = 64;           // chunk length
 constexpr int D = 128;          // head dim (dk = dv)
 constexpr int kTile = 8192;     // bytes of one 64 x 64 bf16 swizzled tile
 constexpr int kThreads = 320;   // 10 warps: 0 loads, 1 MMAs, 2-9 epilogue
-constexpr int kEpiThreads = 256;
 constexpr int kMaxSortSeqs = 4096;
+constexpr float kLog2e = 1.4426950408889634f;
 
 enum DeviceError : int { kErrNone = 0, kErrCuSeqlens = 1, kErrTimeout = 2 };
 
@@ -292,7 +292,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_3d(sm.kq + 2 * kTile, &tm_k, 64, hk, tok0, &sm.tma_bar);
         tma_load_3d(sm.kq + 3 * kTile, &tm_q, 64, hk, tok0, &sm.tma_bar);
     }
-    bool bad = !mbar_wait(&sm.tma_bar, 0);
+    bool bad = !warp_wait(&sm.tma_bar, 0, nullptr);
     uint32_t mph = 0;
     if (tid == 0 && !bad) {
         tc_fence_after();
@@ -318,7 +318,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
         }
         if (j0 == 0) {
-            bad |= !mbar_wait(&sm.mma_bar, mph);
+            bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
             mph ^= 1;
         }
         tc_fence_after();
@@ -338,7 +338,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const int i = c0 + 8 * cc + u;
-                            const float a = i < t ? bt * expf(gt - sm.gam[j][i]) * x[8 * cc + u] : 0.f;
+                            const float a = i < t ? bt * exp2f((gt - sm.gam[j][i]) * kLog2e) * x[8 * cc + u] : 0.f;
                             if ((t >> 5) == (i >> 5)) sm.ad[j][t >> 5][t & 31][i & 31] = a;
                             ev[u] = (t >= 32 && i < 32) ? a : 0.f;
                         }
@@ -357,7 +357,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const int i = c0 + 8 * cc + u;
-                            pv[u] = i <= r ? expf(gr - sm.gam[j][i]) * x[8 * cc + u] : 0.f;
+                            pv[u] = i <= r ? exp2f((gr - sm.gam[j][i]) * kLog2e) * x[8 * cc + u] : 0.f;
                         }
                         *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv);
                     }
@@ -411,7 +411,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(&sm.mma_bar);
         }
-        bad |= !mbar_wait(&sm.mma_bar, mph);
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
         mph ^= 1;
         tc_fence_after();
         if (warp >= 2) {
@@ -443,7 +443,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(&sm.mma_bar);
         }
-        bad |= !mbar_wait(&sm.mma_bar, mph);
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
         mph ^= 1;
         tc_fence_after();
         // ---- T = D' - Y;  T diag(b) -> e (and the workspace), T diag(b e^gamma) -> n
@@ -490,7 +490,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(&sm.mma_bar);
         }
-        bad |= !mbar_wait(&sm.mma_bar, mph);
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
         mph ^= 1;
         tc_fence_after();
         if (warp >= 2) {
@@ -515,6 +515,10 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ kernel 3
+constexpr int kChainThreads = 448;  // 14 warps: 0 loads, 1 MMAs, 2-9 state, 10-13 output
+constexpr int kStateThreads = 256;
+constexpr int kOutThreads = 128;
+
 struct ChainStage {
     uint8_t k[2 * kTile];   // K [64 tokens][128 dk] as two 64-column atoms
     uint8_t q[2 * kTile];   // Q, likewise
@@ -526,50 +530,65 @@ struct ChainStage {
 
 struct ChainSmem {
     ChainStage st[2];
-    uint8_t s16[4 * kTile];  // S0 bf16, K-major: [128 dv][128 dk] as two atoms
-    uint8_t dt[2 * kTile];   // Delta^T bf16 [128 dv][64 tokens]
-    uint8_t dts[2 * kTile];  // Delta^T diag(e^{gamma_L - gamma})
-    float egdec[2][2 * C];   // per stage: e^{gamma_t} then e^{gamma_L - gamma_t}
-    uint64_t full[2];        // stage loaded (TMA transaction count)
-    uint64_t empty[2];       // stage consumed (1 MMA commit + 256 epilogue threads)
-    uint64_t s16_ready;      // epilogue: S0 copy (and pre-scaled S) ready
-    uint64_t dt_ready;       // epilogue: Delta^T copies ready
-    uint64_t o_free;         // epilogue: output accumulators read
-    uint64_t d_done;         // MMA: Delta^T complete
-    uint64_t s_done;         // MMA: state update complete
-    uint64_t o_done;         // MMA: output accumulators complete
-    uint64_t fin;            // MMA: everything issued has completed
+    uint8_t ostage[2][C * D * 2];  // output tile [64 tokens][128 dv] bf16, for the TMA store
+    float egdec[2][2 * C];         // per stage: e^{gamma_t} then e^{gamma_L - gamma_t}
+    uint64_t full[2];              // stage loaded (TMA transaction count)
+    uint64_t empty[2];             // stage consumed (MMA commit + state and output threads)
+    uint64_t s16_ready;            // state threads: -S0 (bf16) and pre-scaled S in TMEM
+    uint64_t dt_ready;             // state threads: Delta^T copies in TMEM
+    uint64_t o_free;               // output threads: output accumulators read
+    uint64_t d_done;               // MMA: Delta^T complete
+    uint64_t s_done;               // MMA: state update complete
+    uint64_t o_done;               // MMA: output accumulators complete
+    uint64_t fin;                  // MMA: everything issued has completed
     uint32_t tmem;
     int abort;
     int issued;
 };
 
 constexpr uint32_t kStageBytes = 10 * kTile + 512;  // K, Q, V, W^T, T diag b, P, e^gamma/dec
-// TMEM columns of the chain kernel.
-constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColS = 256;
+// TMEM columns of the recurrence kernel.  D = U^T then Delta^T (fp32); O1 =
+// -S0 Q^T and O2 = Delta^T P^T (fp32); NS = -S0 as bf16 pairs (the A operand
+// of two MMAs); S = the fp32 state; DT and DTS = Delta^T and
+// Delta^T diag(e^{gamma_L - gamma}) as bf16 pairs (A operands).
+constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColNS = 192, kColS = 256,
+                   kColDT = 384, kColDTS = 416;
 
-// Bounded wait that also gives up as soon as another role of the CTA has.
-__device__ __forceinline__ bool chain_wait(ChainSmem &sm, uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    volatile int *ab = &sm.abort;
-    while (!mbar_try_wait(bar, parity)) {
-        if (*ab) return false;
-        if (clock64() - t0 > 4000000000ll) {
-            *ab = 1;
-            return false;
-        }
-    }
-    return true;
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+    tmem_ld32(taddr + 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[32 + i] = __uint_as_float(r[i]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Stores 64 state values of one row: -x as 32 bf16 pairs into NS and
+// scale * x as fp32 into S.
+__device__ __forceinline__ void store_state(uint32_t t_ns, uint32_t t_s, const float (&x)[64],
+                                            float scale) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = pack_bf16(-x[2 * i], -x[2 * i + 1]);
+    tmem_st32(t_ns, r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(scale * x[i]);
+    tmem_st32(t_s, r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(scale * x[32 + i]);
+    tmem_st32(t_s + 32, r);
+}
+
+__global__ void __launch_bounds__(kChainThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const int *__restrict__ chunk_off,
-                 const int *__restrict__ order, const int4 *__restrict__ table,
-                 const uint8_t *__restrict__ slots, const float *__restrict__ h0,
-                 __nv_bfloat16 *__restrict__ out, float *__restrict__ hT,
-                 int *__restrict__ err, int N, int Hk, int Hv) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const int *__restrict__ chunk_off, const int *__restrict__ order,
+                 const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
+                 const float *__restrict__ h0, __nv_bfloat16 *__restrict__ out,
+                 float *__restrict__ hT, int *__restrict__ err, int N, int Hk, int Hv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -578,15 +597,15 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int hk = h / (Hv / Hk);
     const int c_begin = chunk_off[n], nc = chunk_off[n + 1] - c_begin;
     const size_t state_off = ((size_t)n * Hv + h) * D * D;
-    // Epilogue warps 2-9: TMEM quadrant q, state row j, column half.
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    // Epilogue warps: TMEM quadrant q, state or output row j.
+    const int q = warp & 3;
     const int j = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 
     if (nc == 0) {
         // Empty sequence (or a rejected chunk table): final state = initial state.
         if (hT && !(chunk_off[N] == 0 && *err != kErrNone)) {
-            for (int i = tid; i < D * D / 4; i += kThreads) {
+            for (int i = tid; i < D * D / 4; i += kChainThreads) {
                 const float4 x = h0 ? reinterpret_cast<const float4 *>(h0 + state_off)[i]
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 reinterpret_cast<float4 *>(hT + state_off)[i] = x;
@@ -599,13 +618,14 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_o);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1 + kEpiThreads);
+            mbar_init(&sm.empty[s], 1 + kStateThreads + kOutThreads);
         }
-        mbar_init(&sm.s16_ready, kEpiThreads);
-        mbar_init(&sm.dt_ready, kEpiThreads);
-        mbar_init(&sm.o_free, kEpiThreads);
+        mbar_init(&sm.s16_ready, kStateThreads);
+        mbar_init(&sm.dt_ready, kStateThreads);
+        mbar_init(&sm.o_free, kOutThreads);
         mbar_init(&sm.d_done, 1);
         mbar_init(&sm.s_done, 1);
         mbar_init(&sm.o_done, 1);
@@ -628,7 +648,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
-                if (c >= 2 && !chain_wait(sm, &sm.empty[s], ((c >> 1) + 1) & 1)) break;
+                if (c >= 2 && !thread_wait(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
                 const int tok0 = table[ch].y;
                 ChainStage &st = sm.st[s];
@@ -651,176 +671,178 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            const uint32_t s16 = smem_u32(sm.s16), dt = smem_u32(sm.dt), dts = smem_u32(sm.dts);
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
                 ChainStage &st = sm.st[s];
-                const uint32_t kt = smem_u32(st.k), qt = smem_u32(st.q), vt = smem_u32(st.v),
-                               wt = smem_u32(st.wt), tb = smem_u32(st.tb), pt = smem_u32(st.p);
-                if (!chain_wait(sm, &sm.full[s], (c >> 1) & 1)) break;
+                if (!thread_wait(&sm.full[s], (c >> 1) & 1, &sm.abort)) break;
                 tc_fence_after();
-                // U^T = V^T (T diag b)^T                  [M=128 dv, N=64, K=64]
+                // Base descriptors; a k-step moves the start address only
+                // (the 14-bit address field cannot carry: smem < 256 KB).
+                const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
+                const uint64_t d_tb = smem_desc(smem_u32(st.tb), 16, 1024);
+                const uint64_t d_wt = smem_desc(smem_u32(st.wt), kTile, 1024);
+                const uint64_t d_q = smem_desc(smem_u32(st.q), 16, 1024);
+                const uint64_t d_k = smem_desc(smem_u32(st.k), kTile, 1024);
+                const uint64_t d_p = smem_desc(smem_u32(st.p), 16, 1024);
+                // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
                 constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kColD, smem_desc(vt + 2048 * k, kTile, 1024),
-                             smem_desc(tb + 32 * k, 16, 1024), id_u, k > 0);
-                if (!chain_wait(sm, &sm.s16_ready, c & 1)) break;
+                    mma_bf16(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
+                if (!thread_wait(&sm.s16_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
-                // Delta^T = U^T - S0 W^T                 [M=128 dv, N=64, K=128 dk]
-                constexpr uint32_t id_d = idesc_bf16(128, 64, false, true, true);
+                // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
+                constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem + kColD,
-                             smem_desc(s16 + (k / 4) * 2 * kTile + (k % 4) * 32, 16, 1024),
-                             smem_desc(wt + 2048 * k, kTile, 1024), id_d, 1);
+                    mma_bf16_ta(tmem + kColD, tmem + kColNS + 8 * k, d_wt + 128 * k, id_w, 1);
                 mma_commit(&sm.d_done);
-                if (c > 0 && !chain_wait(sm, &sm.o_free, (c - 1) & 1)) break;
+                if (c > 0 && !thread_wait(&sm.o_free, (c - 1) & 1, &sm.abort)) break;
                 tc_fence_after();
-                // O1^T = S0 Q^T                          [M=128 dv, N=64, K=128 dk]
-                constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);
+                // O1 = (-S0) Q^T                         [M=128 dv, N=64, K=128 dk]
+                constexpr uint32_t id_q = idesc_bf16(128, 64, false, false);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem + kColO1,
-                             smem_desc(s16 + (k / 4) * 2 * kTile + (k % 4) * 32, 16, 1024),
-                             smem_desc(qt + (k / 4) * kTile + (k % 4) * 32, 16, 1024), id_o,
-                             k > 0);
-                if (!chain_wait(sm, &sm.dt_ready, c & 1)) break;
+                    mma_bf16_ta(tmem + kColO1, tmem + kColNS + 8 * k,
+                                d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_q, k > 0);
+                if (!thread_wait(&sm.dt_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
-                // S += (diag(e^{gamma_L - gamma}) Delta)^T K   [M=128 dv, N=128 dk, K=64]
+                // S += (Delta^T diag(e^{gamma_L - gamma})) K   [M=128 dv, N=128 dk, K=64]
                 constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kColS, smem_desc(dts + 32 * k, 16, 1024),
-                             smem_desc(kt + 2048 * k, kTile, 1024), id_s, 1);
+                    mma_bf16_ta(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
                 mma_commit(&sm.s_done);
-                // O2^T = Delta^T P^T                     [M=128 dv, N=64, K=64]
+                // O2 = Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kColO2, smem_desc(dt + 32 * k, 16, 1024),
-                             smem_desc(pt + 32 * k, 16, 1024), id_o, k > 0);
+                    mma_bf16_ta(tmem + kColO2, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, k > 0);
                 mma_commit(&sm.o_done);
                 mma_commit(&sm.empty[s]);
             }
             mma_commit(&sm.fin);
         }
-    } else {
-        // ---------------- epilogue warps 2-9: row j of every 128-row tile,
-        // columns [32 half, 32 half + 32) of the 64-wide ones and
-        // [64 half, 64 half + 64) of the state.
-        const int c32 = 32 * half, c64 = 64 * half;
-        bool ok = chain_wait(sm, &sm.full[0], 0);
+    } else if (warp < 10) {
+        // ---------------- state warps 2-9: row j, half h2 of the state's
+        // columns (and of Delta's 64 tokens).  E3: Delta^T -> bf16 A operands;
+        // E6: the updated state -> -S0 (bf16) and the pre-scaled fp32 state.
+        const int h2 = (warp - 2) >> 2;
+        const uint32_t t_ns = tmem + lane_base + kColNS + 32 * h2;
+        const uint32_t t_s = tmem + lane_base + kColS + 64 * h2;
+        bool ok = warp_wait(&sm.full[0], 0, &sm.abort);
         if (ok) {
-            // Initial state: bf16 copy for S0, fp32 copy pre-scaled by the
-            // first chunk's total decay e^{gamma_L}.
-            const float scale = sm.egdec[0][C - 1];
             float x[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
                 const float4 v4 = h0 ? *reinterpret_cast<const float4 *>(
-                                           h0 + state_off + (size_t)j * D + c64 + c)
+                                           h0 + state_off + (size_t)j * D + 64 * h2 + c)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[c] = v4.x; x[c + 1] = v4.y; x[c + 2] = v4.z; x[c + 3] = v4.w;
             }
-            uint8_t *atom = sm.s16 + half * 2 * kTile;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4 *>(atom + swz(j, cc)) = pack8(x + 8 * cc);
-#pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-                uint32_t r[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(scale * x[32 * p2 + i]);
-                tmem_st32(tmem + lane_base + kColS + c64 + 32 * p2, r);
-            }
+            store_state(t_ns, t_s, x, sm.egdec[0][C - 1]);
             tmem_st_wait();
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.s16_ready);
         }
         for (int c = 0; ok && c < nc; ++c) {
             const int s = c & 1;
-            const int4 e = table[c_begin + c];
-            const int tok0 = e.y, L = e.z;
-            const float *eg = sm.egdec[s];
             const float *dec = sm.egdec[s] + C;
-            // E3: Delta^T row j -> bf16 copies (plain and decayed to the chunk end)
-            if (!(ok = chain_wait(sm, &sm.d_done, c & 1))) break;
+            if (!(ok = warp_wait(&sm.d_done, c & 1, &sm.abort))) break;
             tc_fence_after();
             {
-                float d[32];
-                tmem_ld32f(tmem + lane_base + kColD + c32, d);
-                float ds[32];
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + kColD + 32 * h2, r);
+                tmem_ld_wait();
+                uint32_t pd[16], ps[16];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) ds[t] = d[t] * dec[c32 + t];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    *reinterpret_cast<uint4 *>(sm.dt + swz(j, 4 * half + cc)) = pack8(d + 8 * cc);
-                    *reinterpret_cast<uint4 *>(sm.dts + swz(j, 4 * half + cc)) = pack8(ds + 8 * cc);
+                for (int i = 0; i < 16; ++i) {
+                    const float d0 = __uint_as_float(r[2 * i]), d1 = __uint_as_float(r[2 * i + 1]);
+                    const float2 dv = *reinterpret_cast<const float2 *>(dec + 32 * h2 + 2 * i);
+                    pd[i] = pack_bf16(d0, d1);
+                    ps[i] = pack_bf16(d0 * dv.x, d1 * dv.y);
                 }
+                tmem_st16(tmem + lane_base + kColDT + 16 * h2, pd);
+                tmem_st16(tmem + lane_base + kColDTS + 16 * h2, ps);
+                tmem_st_wait();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.dt_ready);
-            // E6: the updated state -> next chunk's S0 and pre-scaled fp32 state,
-            // or the final state after the last chunk.
-            if (!(ok = chain_wait(sm, &sm.s_done, c & 1))) break;
+            mbar_arrive(&sm.empty[s]);
+            if (!(ok = warp_wait(&sm.s_done, c & 1, &sm.abort))) break;
             tc_fence_after();
             {
                 float x[64];
-                {
-                    float a[32], b[32];
-                    tmem_ld32f(tmem + lane_base + kColS + c64, a);
-                    tmem_ld32f(tmem + lane_base + kColS + c64 + 32, b);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) { x[i] = a[i]; x[32 + i] = b[i]; }
-                }
+                tmem_ld64(t_s, x);
                 if (c == nc - 1) {
                     if (hT) {
-                        float *dst = hT + state_off + (size_t)j * D + c64;
+                        float *dst = hT + state_off + (size_t)j * D + 64 * h2;
 #pragma unroll
                         for (int i = 0; i < 64; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) =
                                 make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
                     }
                 } else {
-                    uint8_t *atom = sm.s16 + half * 2 * kTile;
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        *reinterpret_cast<uint4 *>(atom + swz(j, cc)) = pack8(x + 8 * cc);
-                    if (!(ok = chain_wait(sm, &sm.full[s ^ 1], ((c + 1) >> 1) & 1))) break;
-                    const float scale = sm.egdec[s ^ 1][C - 1];
-#pragma unroll
-                    for (int p2 = 0; p2 < 2; ++p2) {
-                        uint32_t r[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(scale * x[32 * p2 + i]);
-                        tmem_st32(tmem + lane_base + kColS + c64 + 32 * p2, r);
-                    }
+                    if (!(ok = warp_wait(&sm.full[s ^ 1], ((c + 1) >> 1) & 1, &sm.abort))) break;
+                    store_state(t_ns, t_s, x, sm.egdec[s ^ 1][C - 1]);
                     tmem_st_wait();
-                    fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(&sm.s16_ready);
                 }
             }
-            // E5: output o_t = e^{gamma_t} O1 + O2 for value dim j.
-            if (!(ok = chain_wait(sm, &sm.o_done, c & 1))) break;
-            tc_fence_after();
-            {
-                float o1[32], o2[32];
-                tmem_ld32f(tmem + lane_base + kColO1 + c32, o1);
-                tmem_ld32f(tmem + lane_base + kColO2 + c32, o2);
-                __nv_bfloat16 *op = out + ((size_t)(tok0 + c32) * Hv + h) * D + j;
-                const size_t tstride = (size_t)Hv * D;
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (c32 + t < L)
-                        op[t * tstride] = __float2bfloat16_rn(fmaf(eg[c32 + t], o1[t], o2[t]));
-            }
-            tc_fence_before();
-            mbar_arrive(&sm.o_free);
-            mbar_arrive(&sm.empty[s]);
         }
+    } else {
+        // ---------------- output warps 10-13: o_t = e^{gamma_t} S0 q_t +
+        // (Delta^T P^T)_t for value dim j, staged as a [64 tokens][128 dv]
+        // tile and written with one TMA store (plain stores for a short last
+        // chunk, whose tile would reach into the next sequence).
+        const bool leader = (warp == 10 && lane == 0);
+        for (int c = 0; c < nc; ++c) {
+            const int s = c & 1;
+            const int4 e = table[c_begin + c];
+            const int tok0 = e.y, L = e.z;
+            if (!warp_wait(&sm.o_done, c & 1, &sm.abort)) break;
+            tc_fence_after();
+            const bool full_tile = (L == C);
+            uint8_t *stg = sm.ostage[c & 1];
+            if (full_tile) {
+                if (leader) bulk_wait_group_read<1>();  // the store from chunk c - 2 has read it
+                named_barrier(1, kOutThreads);
+            }
+            const float *eg = sm.egdec[s];
+            __nv_bfloat16 *op = out + ((size_t)tok0 * Hv + h) * D + j;
+            const size_t tstride = (size_t)Hv * D;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t r1[32], r2[32];
+                tmem_ld32(tmem + lane_base + kColO1 + 32 * hh, r1);
+                tmem_ld32(tmem + lane_base + kColO2 + 32 * hh, r2);
+                tmem_ld_wait();
+                if (hh == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&sm.o_free);
+                }
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int tt = 32 * hh + t;
+                    const float o = fmaf(-eg[tt], __uint_as_float(r1[t]), __uint_as_float(r2[t]));
+                    if (full_tile)
+                        *reinterpret_cast<__nv_bfloat16 *>(stg + tt * (D * 2) + 2 * j) =
+                            __float2bfloat16_rn(o);
+                    else if (tt < L)
+                        op[tt * tstride] = __float2bfloat16_rn(o);
+                }
+            }
+            mbar_arrive(&sm.empty[s]);
+            if (full_tile) {
+                fence_proxy_async_smem();
+                named_barrier(1, kOutThreads);
+                if (leader) {
+                    tma_store_3d(&tm_o, 0, h, tok0, stg);
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (leader) bulk_wait_group<0>();
     }
     __syncthreads();
     if (sm.abort) {
@@ -854,15 +876,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [T, H, 128] bf16 tensor, boxes of 64 features x 1 head x 64 tokens, 128-byte swizzle.
-bool encode_thd(CUtensorMap *map, const void *base, int64_t T, int H) {
+bool encode_thd(CUtensorMap *map, const void *base, int64_t T, int H, bool out_tile = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+    // Loads: 64-feature boxes, 128-byte swizzle (MMA operand layout).  The
+    // output store: whole 128-feature rows, no swizzle.
+    const cuuint32_t box[3] = {out_tile ? (cuuint32_t)D : 64u, 1, (cuuint32_t)C};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               out_tile ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -887,16 +912,18 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     int4 *table = reinterpret_cast<int4 *>(ws + w.table);
     uint8_t *slots = ws + w.tiles;
 
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (p.total_tokens > 0) {
         if (!encode_thd(&tq, q, p.total_tokens, p.num_k_heads) ||
             !encode_thd(&tk, k, p.total_tokens, p.num_k_heads) ||
-            !encode_thd(&tv, v, p.total_tokens, p.num_v_heads))
+            !encode_thd(&tv, v, p.total_tokens, p.num_v_heads) ||
+            !encode_thd(&to, out, p.total_tokens, p.num_v_heads, true))
             return GDN_ERR_CUDA;
     } else {
         memset(&tq, 0, sizeof(tq));
         memset(&tk, 0, sizeof(tk));
         memset(&tv, 0, sizeof(tv));
+        memset(&to, 0, sizeof(to));
     }
 
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, p.num_seqs, p.total_tokens, w.max_chunks,
@@ -918,8 +945,8 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     if (cudaFuncSetAttribute(gdn_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
-    gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kThreads, smem, stream>>>(
-        tq, tk, tv, chunk_off, order, table, slots, h0, static_cast<__nv_bfloat16 *>(out), hT,
+    gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
+        tq, tk, tv, to, chunk_off, order, table, slots, h0, static_cast<__nv_bfloat16 *>(out), hT,
         err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -12,6 +12,11 @@
 //   4: A K-major [128 x K], B MN-major (B stored [K][N])      (K = 128, N = 64)
 //   5: M = 64: A K-major [64 x K], B MN-major [K][N]          (K = 64,  N = 64);
 //      all 128 TMEM lanes are dumped so the host can map rows to lanes
+//   6: A from TMEM [128 x K] (packed bf16 pairs per column), B K-major [N x K]
+//      (K = 128, N = 64)
+//   7: timing: 64 back-to-back MMAs of mode 0's shape (N = 64) and then of
+//      N = 128; d[0..3] = cycles to issue 64 (N=64), issue+complete (N=64),
+//      issue 64 (N=128), issue+complete (N=128)
 // Inputs (host-provided, row-major fp32, rounded to bf16 here):
 //   a: mode 0/2/3/4: [128][K];  mode 1: [K][128]  (i.e. A^T)
 //   b: mode 0/1/3:   [N][K];    mode 2/4: [K][N]
@@ -54,14 +59,16 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     } else {                    // A [M rows][K]: K-major, atoms over K
         for (int i = tid; i < M * K; i += 128) put(sa, M, i / K, i % K, a[i]);
     }
-    if (mode == 2 || mode == 4 || mode == 5) {  // B stored [K rows][N]: MN-major, atoms over N
+    if (mode == 7) {            // B [128 rows][K] so both N = 64 and N = 128 read valid data
+        for (int i = tid; i < 128 * K; i += 128) put(sb, 128, i / K, i % K, b[i % (64 * K)]);
+    } else if (mode == 2 || mode == 4 || mode == 5) {  // B stored [K rows][N]: MN-major, atoms over N
         for (int i = tid; i < K * N; i += 128) put(sb, K, i / N, i % N, b[i]);
     } else {                    // B [N rows][K]: K-major
         for (int i = tid; i < N * K; i += 128) put(sb, N, i / K, i % K, b[i]);
     }
     fence_proxy_async_smem();
     if (warp == 0) {
-        tmem_alloc(&tslot, 128);
+        tmem_alloc(&tslot, 256);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -73,11 +80,52 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     tc_fence_after();
     const uint32_t tmem = tslot;
     const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
+    if (mode == 6) {
+        // A row tid into TMEM columns 128.. as packed bf16 pairs.
+        for (int c0 = 0; c0 < K / 2; c0 += 32) {
+            uint32_t r[32];
+            for (int c = 0; c < 32; ++c)
+                r[c] = pack_bf16(a[tid * K + 2 * (c0 + c)], a[tid * K + 2 * (c0 + c) + 1]);
+            tmem_st32(tmem + ((uint32_t)(32 * warp) << 16) + 128 + c0, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (mode == 7) {
+        if (tid == 0) {
+            const uint64_t ad = smem_desc(a0, 16, 1024);
+            for (int pass = 0; pass < 2; ++pass) {
+                const int Nn = pass ? 128 : 64;
+                const uint64_t bd = smem_desc(b0, 16, 1024);
+                const long long t0 = clock64();
+                for (int r = 0; r < 64; ++r)
+                    mma_bf16(tmem, ad + 2 * (r % 4), bd + 2 * (r % 4), idesc_bf16(128, Nn, false, false), r > 0);
+                const long long t1 = clock64();
+                mma_commit(&bar);
+                mbar_wait(&bar, pass, 2000000000ll);
+                const long long t2 = clock64();
+                d[2 * pass] = (float)(t1 - t0);
+                d[2 * pass + 1] = (float)(t2 - t0);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, 256);
+        return;
+    }
     if (tid == 0) {
         const int reps = (mode == 3) ? 2 : 1;
         for (int rep = 0; rep < reps; ++rep) {
             for (int k = 0; k < K / 16; ++k) {
                 uint64_t ad, bd;
+                if (mode == 6) {
+                    mma_bf16_ta(tmem, tmem + 128 + 8 * k,
+                                smem_desc(b0 + (k / 4) * (N * 128) + (k % 4) * 32, 16, 1024),
+                                idesc_bf16(128, N, false, false), k > 0);
+                    continue;
+                }
                 if (mode == 1)
                     ad = smem_desc(a0 + k * 2048, K * 128, 1024);
                 else
@@ -104,7 +152,7 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 extern "C" int tc_probe_run(const float *a, const float *b, float *d, int mode, int *status) {

@@ -32,7 +32,7 @@ def bf(x):
     return torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 6])
 def test_layout(probe, mode):
     rng = np.random.default_rng(mode)
     K = 64 if mode in (1, 2) else 128
@@ -76,3 +76,20 @@ def test_m64_lane_layout(probe):
         lanes.append(lane)
     print("M=64 row->lane:", lanes)
     assert len(set(lanes)) == 64
+
+
+def test_mma_issue_and_latency(probe):
+    """Cycles to issue 64 tcgen05.mma (M=128, K=16) from one thread, and to
+    complete them, for N = 64 and N = 128 (printed; sanity-checked only)."""
+    rng = np.random.default_rng(7)
+    a = rng.standard_normal((128, 128)).astype(np.float32)
+    b = rng.standard_normal((64, 128)).astype(np.float32)
+    dd = torch.zeros((128, 64), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe_run(torch.from_numpy(a).cuda().data_ptr(),
+                            torch.from_numpy(b).cuda().data_ptr(), dd.data_ptr(), 7, st.data_ptr())
+    assert rc == 0
+    t = dd.flatten()[:4].cpu().numpy()
+    print(f"64 MMAs N=64: issue {t[0]:.0f} cyc, done {t[1]:.0f} cyc; "
+          f"N=128: issue {t[2]:.0f} cyc, done {t[3]:.0f} cyc")
+    assert t[1] > 0 and t[3] > 0
