@@ -72,7 +72,7 @@ constexpr int kSlotBytes = kSlotDEC + 256;    // 33280
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-    size_t hdr, chunk_off, order, table, tiles, total;
+    size_t hdr, chunk_off, order, table, gl, tiles, total;
     int64_t max_chunks;
 };
 
@@ -85,7 +85,8 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.chunk_off = 256;
     w.order = align_up(w.chunk_off + 4 * (size_t)(p.num_seqs + 1), 256);
     w.table = align_up(w.order + 4 * (size_t)p.num_seqs, 256);
-    w.tiles = align_up(w.table + 16 * (size_t)w.max_chunks, 1024);
+    w.gl = align_up(w.table + 16 * (size_t)w.max_chunks, 256);  // e^{gamma_L} per (chunk, value head)
+    w.tiles = align_up(w.gl + 4 * (size_t)w.max_chunks * p.num_v_heads, 1024);
     w.total = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
     return w;
 }
@@ -255,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float *__restrict__ g, const float *__restrict__ beta,
                 const int *__restrict__ chunk_off, const int4 *__restrict__ table,
-                uint8_t *__restrict__ slots, int *__restrict__ err, int N, int Hk, int Hv) {
+                uint8_t *__restrict__ slots, float *__restrict__ gl, int *__restrict__ err, int N,
+                int Hk, int Hv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -316,6 +318,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
             slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
             slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
+            if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[j][C - 1];
         }
         if (j0 == 0) {
             bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
@@ -331,18 +334,35 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (q < 2) {
                 const int t = row;
                 for (int j = 0; j < nh; ++j) {
+                    // Decay factors first (shared loads), then the stores.
                     const float gt = sm.gam[j][t], bt = sm.beta[j][t];
+                    float av[32];
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
+                        const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int i = c0 + u + w;
+                            av[u + w] = i < t ? bt * exp2f((gt - gi[w]) * kLog2e) * x[u + w] : 0.f;
+                        }
+                    }
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         float ev[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const int i = c0 + 8 * cc + u;
-                            const float a = i < t ? bt * exp2f((gt - sm.gam[j][i]) * kLog2e) * x[8 * cc + u] : 0.f;
-                            if ((t >> 5) == (i >> 5)) sm.ad[j][t >> 5][t & 31][i & 31] = a;
-                            ev[u] = (t >= 32 && i < 32) ? a : 0.f;
+                            ev[u] = (t >= 32 && i < 32) ? av[8 * cc + u] : 0.f;
                         }
                         *reinterpret_cast<uint4 *>(sm.e[j] + swz(t, (c0 >> 3) + cc)) = pack8(ev);
+                    }
+                    if ((t >> 5) == half) {  // diagonal block: this thread's columns are in it
+                        float *dst = sm.ad[j][half][t & 31];
+#pragma unroll
+                        for (int u = 0; u < 32; u += 4)
+                            *reinterpret_cast<float4 *>(dst + u) =
+                                make_float4(av[u], av[u + 1], av[u + 2], av[u + 3]);
                     }
                 }
             } else {
@@ -350,17 +370,21 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int j = 0; j < nh; ++j) {
                     const int h = hk * G + j0 + j;
                     const float gr = sm.gam[j][r];
+                    float pv[32];
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
+                        const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int i = c0 + u + w;
+                            pv[u + w] = i <= r ? exp2f((gr - gi[w]) * kLog2e) * x[u + w] : 0.f;
+                        }
+                    }
                     uint8_t *pdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotP;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float pv[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int i = c0 + 8 * cc + u;
-                            pv[u] = i <= r ? exp2f((gr - sm.gam[j][i]) * kLog2e) * x[8 * cc + u] : 0.f;
-                        }
-                        *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv);
-                    }
+                    for (int cc = 0; cc < 4; ++cc)
+                        *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv + 8 * cc);
                 }
             }
         }
@@ -547,6 +571,7 @@ struct ChainSmem {
 };
 
 constexpr uint32_t kStageBytes = 10 * kTile + 512;  // K, Q, V, W^T, T diag b, P, e^gamma/dec
+constexpr int kPrefetch = 3;  // chunks pulled into L2 ahead of the two staged ones
 // TMEM columns of the recurrence kernel.  D = U^T then Delta^T (fp32); O1 =
 // -S0 Q^T and O2 = Delta^T P^T (fp32); NS = -S0 as bf16 pairs (the A operand
 // of two MMAs); S = the fp32 state; DT and DTS = Delta^T and
@@ -587,7 +612,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const int *__restrict__ chunk_off, const int *__restrict__ order,
                  const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
-                 const float *__restrict__ h0, __nv_bfloat16 *__restrict__ out,
+                 const float *__restrict__ gl, const float *__restrict__ h0,
+                 __nv_bfloat16 *__restrict__ out,
                  float *__restrict__ hT, int *__restrict__ err, int N, int Hk, int Hv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
@@ -644,8 +670,22 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t tmem = sm.tmem;
 
     if (warp == 0) {
-        // ---------------- producer: TMA tiles and the prep kernel's slot
+        // ---------------- producer: TMA tiles and the prep kernel's slot;
+        // chunks kPrefetch ahead are pulled into L2 so that a stage's loads
+        // hit L2 when the stage frees up.
         if (lane == 0) {
+            auto prefetch = [&](int c) {
+                const int ch = c_begin + c;
+                const int tok0 = table[ch].y;
+                tma_prefetch_3d(&tm_k, 0, hk, tok0);
+                tma_prefetch_3d(&tm_k, 64, hk, tok0);
+                tma_prefetch_3d(&tm_q, 0, hk, tok0);
+                tma_prefetch_3d(&tm_q, 64, hk, tok0);
+                tma_prefetch_3d(&tm_v, 0, h, tok0);
+                tma_prefetch_3d(&tm_v, 64, h, tok0);
+                bulk_prefetch_l2(slots + ((size_t)ch * Hv + h) * kSlotBytes, kSlotBytes);
+            };
+            for (int c = 2; c < min(nc, 2 + kPrefetch); ++c) prefetch(c);
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !thread_wait(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
@@ -666,6 +706,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bulk_load(st.p, slot + kSlotP, kTile, bar);
                 bulk_load(sm.egdec[s], slot + kSlotEG, 512, bar);
                 sm.issued = c + 1;
+                if (c + 2 + kPrefetch - 1 < nc && c >= 1) prefetch(c + 2 + kPrefetch - 1);
             }
         }
     } else if (warp == 1) {
@@ -747,6 +788,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int c = 0; ok && c < nc; ++c) {
             const int s = c & 1;
             const float *dec = sm.egdec[s] + C;
+            // Total decay of the next chunk, for pre-scaling the state (read
+            // early, straight from the prep kernel's output).
+            const float next_decay = c + 1 < nc ? gl[(size_t)(c_begin + c + 1) * Hv + h] : 1.f;
             if (!(ok = warp_wait(&sm.d_done, c & 1, &sm.abort))) break;
             tc_fence_after();
             {
@@ -782,8 +826,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
                     }
                 } else {
-                    if (!(ok = warp_wait(&sm.full[s ^ 1], ((c + 1) >> 1) & 1, &sm.abort))) break;
-                    store_state(t_ns, t_s, x, sm.egdec[s ^ 1][C - 1]);
+                    store_state(t_ns, t_s, x, next_decay);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&sm.s16_ready);
@@ -821,15 +864,27 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_before();
                     mbar_arrive(&sm.o_free);
                 }
+                // All shared-memory reads before the first store: the compiler
+                // cannot tell the staging tile from e^gamma, and would order
+                // each load after the previous store.
+                float o[32];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int tt = 32 * hh + t;
-                    const float o = fmaf(-eg[tt], __uint_as_float(r1[t]), __uint_as_float(r2[t]));
-                    if (full_tile)
-                        *reinterpret_cast<__nv_bfloat16 *>(stg + tt * (D * 2) + 2 * j) =
-                            __float2bfloat16_rn(o);
-                    else if (tt < L)
-                        op[tt * tstride] = __float2bfloat16_rn(o);
+                for (int t = 0; t < 32; t += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4 *>(eg + 32 * hh + t);
+                    o[t] = fmaf(-e4.x, __uint_as_float(r1[t]), __uint_as_float(r2[t]));
+                    o[t + 1] = fmaf(-e4.y, __uint_as_float(r1[t + 1]), __uint_as_float(r2[t + 1]));
+                    o[t + 2] = fmaf(-e4.z, __uint_as_float(r1[t + 2]), __uint_as_float(r2[t + 2]));
+                    o[t + 3] = fmaf(-e4.w, __uint_as_float(r1[t + 3]), __uint_as_float(r2[t + 3]));
+                }
+                if (full_tile) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        *reinterpret_cast<__nv_bfloat16 *>(stg + (32 * hh + t) * (D * 2) + 2 * j) =
+                            __float2bfloat16_rn(o[t]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (32 * hh + t < L) op[(32 * hh + t) * tstride] = __float2bfloat16_rn(o[t]);
                 }
             }
             mbar_arrive(&sm.empty[s]);
@@ -910,6 +965,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     int *chunk_off = reinterpret_cast<int *>(ws + w.chunk_off);
     int *order = reinterpret_cast<int *>(ws + w.order);
     int4 *table = reinterpret_cast<int4 *>(ws + w.table);
+    float *gl = reinterpret_cast<float *>(ws + w.gl);
     uint8_t *slots = ws + w.tiles;
 
     CUtensorMap tq, tk, tv, to;
@@ -937,7 +993,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
             return GDN_ERR_CUDA;
         dim3 grid((unsigned)w.max_chunks, p.num_k_heads);
         gdn_prep_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, g, beta, chunk_off, table, slots,
-                                                          err, p.num_seqs, p.num_k_heads,
+                                                          gl, err, p.num_seqs, p.num_k_heads,
                                                           p.num_v_heads);
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
@@ -946,7 +1002,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
                              (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
     gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
-        tq, tk, tv, to, chunk_off, order, table, slots, h0, static_cast<__nv_bfloat16 *>(out), hT,
+        tq, tk, tv, to, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
         err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -60,6 +60,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep in hardware (not
+// taking issue slots) until the phase completes or about `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // about `limit` clock cycles and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
@@ -72,10 +86,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     return true;
 }
 
-// Warp-cooperative bounded wait: only lane 0 polls the barrier (polling from
-// every thread costs shared-memory bandwidth that the tensor core needs for
-// its operands), the time limit is checked every 256 polls, and the whole
-// warp leaves together.  Returns false on time-out or when *abort is set.
+// Warp-cooperative bounded wait: only lane 0 polls the barrier, sleeping in
+// hardware between polls (a spinning warp would take issue slots from the
+// working warps of its sub-partition); the time limit is checked every 16
+// polls, and the whole warp leaves together.  Returns false on time-out or when *abort is set.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           long long limit = 4000000000ll) {
     int ok = 1;
@@ -83,8 +97,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
         if (!mbar_try_wait(bar, parity)) {
             const long long t0 = clock64();
             for (uint32_t i = 1;; ++i) {
-                if (mbar_try_wait(bar, parity)) break;
-                if ((i & 255) == 0) {
+                if (mbar_try_wait_sleep(bar, parity, 100000)) break;
+                if ((i & 15) == 0) {
                     if (abort && *abort) { ok = 0; break; }
                     if (clock64() - t0 > limit) {
                         if (abort) *abort = 1;
@@ -106,8 +120,8 @@ __device__ __forceinline__ bool thread_wait(uint64_t *bar, uint32_t parity, vola
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 100000)) return true;
+        if ((i & 15) == 0) {
             if (abort && *abort) return false;
             if (clock64() - t0 > limit) {
                 if (abort) *abort = 1;
@@ -125,6 +139,22 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
+}
+
+// L2 prefetch of one TMA box (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// L2 prefetch of a global range (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
 }
 
 // Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
