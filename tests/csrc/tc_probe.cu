@@ -14,6 +14,10 @@
 //      all 128 TMEM lanes are dumped so the host can map rows to lanes
 //   6: A from TMEM [128 x K] (packed bf16 pairs per column), B K-major [N x K]
 //      (K = 128, N = 64)
+//   8: as 7, issued warp-uniformly by warp 0 (elect.sync inside the asm)
+//   9: timing of 64 MMAs (A smem, B K-major, warp-uniform issue) in one
+//      accumulator chain vs interleaved over several accumulators:
+//      v0 N=64 x1, v1 N=64 x4, v2 N=128 x1, v3 N=128 x2, v4 N=256 x1, v5 N=64 x2
 //   7: timing: 64 back-to-back MMAs of mode 0's shape (N = 64) and then of
 //      N = 128; d[0..3] = cycles to issue 64 (N=64), issue+complete (N=64),
 //      issue 64 (N=128), issue+complete (N=128)
@@ -35,6 +39,59 @@ __device__ void put(uint8_t *tile, int rows, int row, int col, float x) {
     const int atom = col / 64, c = col % 64;
     uint8_t *p = tile + atom * rows * 128 + swz(row, c / 8) + (c % 8) * 2;
     *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+template <int V>
+__device__ void time_chains(uint32_t a0, uint32_t b0, uint32_t tmem, uint64_t *bar, float *d) {
+    constexpr int Nn = (V <= 1 || V == 5) ? 64 : (V <= 3 ? 128 : 256);
+    constexpr int chains = V == 1 ? 4 : (V == 3 || V == 5 ? 2 : 1);
+    const uint64_t ad = smem_desc(a0, 16, 1024);
+    const uint64_t bd = smem_desc(b0, 16, 1024);
+    constexpr uint32_t id = idesc_bf16(128, Nn, false, false);
+    const long long t0 = clock64();
+#pragma unroll
+    for (int r = 0; r < 64; ++r)
+        mma_bf16_w(tmem + (r % chains) * Nn, ad + 2 * (r % 4), bd + 2 * (r % 4), id, r >= chains);
+    const long long t1 = clock64();
+    mma_commit_w(bar);
+    warp_wait(bar, V & 1, nullptr);
+    const long long t2 = clock64();
+    if ((threadIdx.x & 31) == 0) {
+        d[2 * V] = (float)(t1 - t0);
+        d[2 * V + 1] = (float)(t2 - t0);
+    }
+}
+
+template <int V>
+__device__ void time_variant(int mode, uint32_t a0, uint32_t b0, uint32_t tmem, uint64_t *bar,
+                             float *d) {
+    constexpr int Nn = (V == 1 || V == 5) ? 128 : 64;
+    constexpr bool a_tm = (V == 2 || V == 3 || V == 5);
+    constexpr bool b_mn = (V == 3 || V == 4 || V == 5);
+    const uint64_t ad = smem_desc(a0, 16, 1024);
+    const uint64_t bd = b_mn ? smem_desc(b0, 8192, 1024) : smem_desc(b0, 16, 1024);
+    constexpr uint32_t id = idesc_bf16(128, Nn, false, b_mn);
+    const bool warp_mode = (mode == 8);
+    const long long t0 = clock64();
+#pragma unroll
+    for (int r = 0; r < 64; ++r) {
+        const uint64_t b = b_mn ? bd + 128 * (r % 4) : bd + 2 * (r % 4);
+        if (warp_mode) {
+            if (a_tm) mma_bf16_ta_w(tmem, tmem + 128 + 8 * (r % 8), b, id, r > 0);
+            else mma_bf16_w(tmem, ad + 2 * (r % 4), b, id, r > 0);
+        } else {
+            if (a_tm) mma_bf16_ta(tmem, tmem + 128 + 8 * (r % 8), b, id, r > 0);
+            else mma_bf16(tmem, ad + 2 * (r % 4), b, id, r > 0);
+        }
+    }
+    const long long t1 = clock64();
+    if (warp_mode) mma_commit_w(bar); else mma_commit(bar);
+    if (warp_mode) warp_wait(bar, V & 1, nullptr); else mbar_wait(bar, V & 1, 2000000000ll);
+    const long long t2 = clock64();
+    if ((threadIdx.x & 31) == 0) {
+        d[2 * V] = (float)(t1 - t0);
+        d[2 * V + 1] = (float)(t2 - t0);
+    }
 }
 
 }  // namespace
@@ -59,7 +116,9 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     } else {                    // A [M rows][K]: K-major, atoms over K
         for (int i = tid; i < M * K; i += 128) put(sa, M, i / K, i % K, a[i]);
     }
-    if (mode == 7) {            // B [128 rows][K] so both N = 64 and N = 128 read valid data
+    if (mode == 9) {            // B [256 rows][64]: one atom of 32 KB
+        for (int i = tid; i < 256 * 64; i += 128) put(sb, 256, i / 64, i % 64, b[i % (64 * 128)]);
+    } else if (mode == 7) {     // B [128 rows][K] so both N = 64 and N = 128 read valid data
         for (int i = tid; i < 128 * K; i += 128) put(sb, 128, i / K, i % K, b[i % (64 * K)]);
     } else if (mode == 2 || mode == 4 || mode == 5) {  // B stored [K rows][N]: MN-major, atoms over N
         for (int i = tid; i < K * N; i += 128) put(sb, K, i / N, i % N, b[i]);
@@ -93,22 +152,33 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
         __syncthreads();
         tc_fence_after();
     }
-    if (mode == 7) {
-        if (tid == 0) {
-            const uint64_t ad = smem_desc(a0, 16, 1024);
-            for (int pass = 0; pass < 2; ++pass) {
-                const int Nn = pass ? 128 : 64;
-                const uint64_t bd = smem_desc(b0, 16, 1024);
-                const long long t0 = clock64();
-                for (int r = 0; r < 64; ++r)
-                    mma_bf16(tmem, ad + 2 * (r % 4), bd + 2 * (r % 4), idesc_bf16(128, Nn, false, false), r > 0);
-                const long long t1 = clock64();
-                mma_commit(&bar);
-                mbar_wait(&bar, pass, 2000000000ll);
-                const long long t2 = clock64();
-                d[2 * pass] = (float)(t1 - t0);
-                d[2 * pass + 1] = (float)(t2 - t0);
-            }
+    if (mode == 9) {
+        if (warp == 0) {
+            time_chains<0>(a0, b0, tmem, &bar, d);
+            time_chains<1>(a0, b0, tmem, &bar, d);
+            time_chains<2>(a0, b0, tmem, &bar, d);
+            time_chains<3>(a0, b0, tmem, &bar, d);
+            time_chains<4>(a0, b0, tmem, &bar, d);
+            time_chains<5>(a0, b0, tmem, &bar, d);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, 256);
+        return;
+    }
+    if (mode == 7 || mode == 8) {
+        // Timing of 64 back-to-back MMAs (M = 128, K = 16) per variant:
+        // 0: A smem K-major, B K-major, N=64     1: same, N=128
+        // 2: A TMEM,         B K-major, N=64     3: A TMEM, B MN-major, N=64
+        // 4: A smem K-major, B MN-major, N=64    5: A TMEM, B MN-major, N=128
+        // d[2v] = issue cycles, d[2v+1] = issue + completion cycles.
+        if (mode == 7 ? tid == 0 : warp == 0) {
+            time_variant<0>(mode, a0, b0, tmem, &bar, d);
+            time_variant<1>(mode, a0, b0, tmem, &bar, d);
+            time_variant<2>(mode, a0, b0, tmem, &bar, d);
+            time_variant<3>(mode, a0, b0, tmem, &bar, d);
+            time_variant<4>(mode, a0, b0, tmem, &bar, d);
+            time_variant<5>(mode, a0, b0, tmem, &bar, d);
         }
         tc_fence_before();
         __syncthreads();

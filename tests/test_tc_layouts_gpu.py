@@ -78,18 +78,39 @@ def test_m64_lane_layout(probe):
     assert len(set(lanes)) == 64
 
 
-def test_mma_issue_and_latency(probe):
+@pytest.mark.parametrize("mode", [7, 8])
+def test_mma_issue_and_latency(probe, mode):
     """Cycles to issue 64 tcgen05.mma (M=128, K=16) from one thread, and to
-    complete them, for N = 64 and N = 128 (printed; sanity-checked only)."""
+    complete them, for operand placements and majors the kernels use
+    (printed; sanity-checked only)."""
     rng = np.random.default_rng(7)
     a = rng.standard_normal((128, 128)).astype(np.float32)
     b = rng.standard_normal((64, 128)).astype(np.float32)
     dd = torch.zeros((128, 64), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = probe.tc_probe_run(torch.from_numpy(a).cuda().data_ptr(),
-                            torch.from_numpy(b).cuda().data_ptr(), dd.data_ptr(), 7, st.data_ptr())
+                            torch.from_numpy(b).cuda().data_ptr(), dd.data_ptr(), mode, st.data_ptr())
     assert rc == 0
-    t = dd.flatten()[:4].cpu().numpy()
-    print(f"64 MMAs N=64: issue {t[0]:.0f} cyc, done {t[1]:.0f} cyc; "
-          f"N=128: issue {t[2]:.0f} cyc, done {t[3]:.0f} cyc")
-    assert t[1] > 0 and t[3] > 0
+    t = dd.flatten()[:12].cpu().numpy()
+    names = ["A smem, B K-major, N=64", "A smem, B K-major, N=128", "A TMEM, B K-major, N=64",
+             "A TMEM, B MN-major, N=64", "A smem, B MN-major, N=64", "A TMEM, B MN-major, N=128"]
+    for v, nm in enumerate(names):
+        print(f"[{'warp' if mode == 8 else 'thread'} issue] 64 MMAs {nm}: issue {t[2 * v]:.0f} cyc, done {t[2 * v + 1]:.0f} cyc")
+    assert (t[1::2] > 0).all()
+
+
+def test_mma_accumulator_chains(probe):
+    """64 MMAs into one accumulator vs interleaved over several (printed)."""
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((128, 128)).astype(np.float32)
+    b = rng.standard_normal((64, 128)).astype(np.float32)
+    dd = torch.zeros((128, 64), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe_run(torch.from_numpy(a).cuda().data_ptr(),
+                            torch.from_numpy(b).cuda().data_ptr(), dd.data_ptr(), 9, st.data_ptr())
+    assert rc == 0
+    t = dd.flatten()[:12].cpu().numpy()
+    names = ["N=64 x1 chain", "N=64 x4 chains", "N=128 x1", "N=128 x2", "N=256 x1", "N=64 x2"]
+    for v, nm in enumerate(names):
+        print(f"[chains] 64 MMAs {nm}: issue {t[2 * v]:.0f} cyc, done {t[2 * v + 1]:.0f} cyc")
+    assert (t[1::2] > 0).all()
