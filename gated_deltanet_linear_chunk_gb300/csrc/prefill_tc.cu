@@ -211,8 +211,8 @@ struct PrepSmem {
     uint8_t kq[4 * kTile];                // atom 0: K rows 0-63 | Q rows 64-127; atom 1 likewise
     uint8_t e[kPrepHeads][kTile];         // E (lower-left block of A), then T diag(b)
     uint8_t dp[kPrepHeads][kTile];        // D' = blockdiag((I + A_bb)^-1)
-    uint8_t n[kPrepHeads][kTile];         // N = D' E, then T diag(b e^gamma)
-    float ad[kPrepHeads][2][32][36];      // the two diagonal 32 x 32 blocks of A, fp32
+    uint8_t n[kPrepHeads][kTile];         // diagonal blocks of A (fp32), then N = D' E,
+                                          // then T diag(b e^gamma)
     float gam[kPrepHeads][C];
     float beta[kPrepHeads][C];
     float eg[kPrepHeads][C];
@@ -225,7 +225,17 @@ struct PrepSmem {
 // TMEM columns of the prep kernel.
 constexpr uint32_t kPColKQ = 0;    // [K K^T; Q K^T], M = 128, 64 columns
 constexpr uint32_t kPColProd = 64; // + 64 j: N then Y = N D' of head j (M = 64 layout)
-constexpr uint32_t kPColW = 256;   // + 64 j: W^T of head j (M = 128)
+constexpr uint32_t kPColW = 64;    // + 64 j: W^T of head j (M = 128), after the products
+constexpr uint32_t kPrepTmemCols = 256;
+
+// The two fp32 diagonal 32 x 32 blocks of A live in a head's n buffer before
+// N is computed: row t of block b at float offset (32 b + t) * 32, its float4
+// group f stored at group f ^ (t % 8) (conflict-free row stores, broadcast
+// reads in the forward substitution).
+__device__ __forceinline__ float *ad_row(uint8_t *buf, int blk, int t) {
+    return reinterpret_cast<float *>(buf) + (32 * blk + t) * 32;
+}
+__device__ __forceinline__ int ad_f4(int f, int t) { return (f ^ (t & 7)) * 4; }
 
 // Writes 8 floats as one 16-byte bf16 chunk.
 __device__ __forceinline__ uint4 pack8(const float *x) {
@@ -252,7 +262,7 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
     for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float *__restrict__ g, const float *__restrict__ beta,
                 const int *__restrict__ chunk_off, const int4 *__restrict__ table,
@@ -280,7 +290,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&sm.tmem, 512);
+        tmem_alloc(&sm.tmem, kPrepTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -344,7 +354,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
                             const int i = c0 + u + w;
-                            av[u + w] = i < t ? bt * exp2f((gt - gi[w]) * kLog2e) * x[u + w] : 0.f;
+                            av[u + w] = i < t ? bt * ex2_approx((gt - gi[w]) * kLog2e) * x[u + w] : 0.f;
                         }
                     }
 #pragma unroll
@@ -358,10 +368,10 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         *reinterpret_cast<uint4 *>(sm.e[j] + swz(t, (c0 >> 3) + cc)) = pack8(ev);
                     }
                     if ((t >> 5) == half) {  // diagonal block: this thread's columns are in it
-                        float *dst = sm.ad[j][half][t & 31];
+                        float *dst = ad_row(sm.n[j], half, t & 31);
 #pragma unroll
                         for (int u = 0; u < 32; u += 4)
-                            *reinterpret_cast<float4 *>(dst + u) =
+                            *reinterpret_cast<float4 *>(dst + ad_f4(u >> 2, t)) =
                                 make_float4(av[u], av[u + 1], av[u + 2], av[u + 3]);
                     }
                 }
@@ -378,7 +388,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
                             const int i = c0 + u + w;
-                            pv[u + w] = i <= r ? exp2f((gr - gi[w]) * kLog2e) * x[u + w] : 0.f;
+                            pv[u + w] = i <= r ? ex2_approx((gr - gi[w]) * kLog2e) * x[u + w] : 0.f;
                         }
                     }
                     uint8_t *pdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotP;
@@ -397,17 +407,18 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
                 float a0 = (t == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                const float *Ar = sm.ad[j][blk][t];
+                const float *Ar = ad_row(sm.n[j], blk, t);
 #pragma unroll
                 for (int i = 0; i < (t & ~3); i += 4) {
-                    const float4 av = *reinterpret_cast<const float4 *>(Ar + i);
+                    const float4 av = *reinterpret_cast<const float4 *>(Ar + ad_f4(i >> 2, t));
                     a0 = fmaf(-av.x, xc[i], a0);
                     a1 = fmaf(-av.y, xc[i + 1], a1);
                     a2 = fmaf(-av.z, xc[i + 2], a2);
                     a3 = fmaf(-av.w, xc[i + 3], a3);
                 }
 #pragma unroll
-                for (int i = (t & ~3); i < t; ++i) a0 = fmaf(-Ar[i], xc[i], a0);
+                for (int i = (t & ~3); i < t; ++i)
+                    a0 = fmaf(-Ar[ad_f4(i >> 2, t) + (i & 3)], xc[i], a0);
                 xc[t] = (a0 + a1) + (a2 + a3);
             }
             const int ccol = 32 * blk + col;
@@ -535,7 +546,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (bad && tid == 0) atomicExch(err, kErrTimeout);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
 // ------------------------------------------------------------------ kernel 3
