@@ -566,9 +566,10 @@ struct ChainStage {
 struct ChainSmem {
     ChainStage st[2];
     uint8_t ostage[2][C * D * 2];  // output tile [64 tokens][128 dv] bf16, for the TMA store
-    float egdec[2][2 * C];         // per stage: e^{gamma_t} then e^{gamma_L - gamma_t}
+    float egdec[4][2 * C];         // ring by chunk: e^{gamma_t} then e^{gamma_L - gamma_t}
     uint64_t full[2];              // stage loaded (TMA transaction count)
-    uint64_t empty[2];             // stage consumed (MMA commit + state and output threads)
+    uint64_t empty[2];             // stage consumed (MMA commit + state threads)
+    uint64_t eg_free[4];           // output threads done with an egdec entry
     uint64_t s16_ready;            // state threads: -S0 (bf16) and pre-scaled S in TMEM
     uint64_t dt_ready;             // state threads: Delta^T copies in TMEM
     uint64_t o_free;               // output threads: output accumulators read
@@ -583,12 +584,17 @@ struct ChainSmem {
 
 constexpr uint32_t kStageBytes = 10 * kTile + 512;  // K, Q, V, W^T, T diag b, P, e^gamma/dec
 constexpr int kPrefetch = 3;  // chunks pulled into L2 ahead of the two staged ones
+// Below this the state's running scale factor is folded back into the
+// stored state (keeps 1 / sigma far from fp32 overflow).
+constexpr float kRenorm = 1.0e-12f;
 // TMEM columns of the recurrence kernel.  D = U^T then Delta^T (fp32); O1 =
 // -S0 Q^T and O2 = Delta^T P^T (fp32); NS = -S0 as bf16 pairs (the A operand
-// of two MMAs); S = the fp32 state; DT and DTS = Delta^T and
+// of two MMAs, two buffers); S = the fp32 state; DT and DTS = Delta^T and
 // Delta^T diag(e^{gamma_L - gamma}) as bf16 pairs (A operands).
-constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColNS = 192, kColS = 256,
-                   kColDT = 384, kColDTS = 416;
+// NS is double-buffered by chunk parity: chunk c's O1 may be issued after its
+// state update, i.e. after the state warps have written chunk c + 1's -S0.
+constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColNS = 192, kColS = 320,
+                   kColDT = 448, kColDTS = 480;
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
     uint32_t r[32];
@@ -658,8 +664,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_o);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1 + kStateThreads + kOutThreads);
+            mbar_init(&sm.empty[s], 1 + kStateThreads);
         }
+        for (int e = 0; e < 4; ++e) mbar_init(&sm.eg_free[e], kOutThreads);
         mbar_init(&sm.s16_ready, kStateThreads);
         mbar_init(&sm.dt_ready, kStateThreads);
         mbar_init(&sm.o_free, kOutThreads);
@@ -685,9 +692,11 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // chunks kPrefetch ahead are pulled into L2 so that a stage's loads
         // hit L2 when the stage frees up.
         if (lane == 0) {
+            // A sequence's chunks are consecutive 64-token windows.
+            const int seq_tok0 = table[c_begin].y;
             auto prefetch = [&](int c) {
                 const int ch = c_begin + c;
-                const int tok0 = table[ch].y;
+                const int tok0 = seq_tok0 + C * c;
                 tma_prefetch_3d(&tm_k, 0, hk, tok0);
                 tma_prefetch_3d(&tm_k, 64, hk, tok0);
                 tma_prefetch_3d(&tm_q, 0, hk, tok0);
@@ -700,8 +709,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !thread_wait(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
+                if (c >= 4 && !thread_wait(&sm.eg_free[c & 3], ((c >> 2) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
-                const int tok0 = table[ch].y;
+                const int tok0 = seq_tok0 + C * c;
                 ChainStage &st = sm.st[s];
                 uint64_t *bar = &sm.full[s];
                 const uint8_t *slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
@@ -715,74 +725,109 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bulk_load(st.wt, slot + kSlotWT, 2 * kTile, bar);
                 bulk_load(st.tb, slot + kSlotTB, kTile, bar);
                 bulk_load(st.p, slot + kSlotP, kTile, bar);
-                bulk_load(sm.egdec[s], slot + kSlotEG, 512, bar);
+                bulk_load(sm.egdec[c & 3], slot + kSlotEG, 512, bar);
                 sm.issued = c + 1;
                 if (c + 2 + kPrefetch - 1 < nc && c >= 1) prefetch(c + 2 + kPrefetch - 1);
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            for (int c = 0; c < nc; ++c) {
+        // ---------------- MMA issuer: the whole warp runs this loop with
+        // identical values (descriptors stay warp-uniform) and one elected
+        // lane issues each tcgen05 instruction.  U^T for chunk c + 1 is issued
+        // right after chunk c's last MMAs, so it runs while the state warps
+        // prepare chunk c + 1's S0.
+        {
+            constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
+            constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t id_q = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t id_s = idesc_bf16(128, 64, false, true);
+            // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
+            auto issue_u = [&](int c) -> bool {
                 const int s = c & 1;
-                ChainStage &st = sm.st[s];
-                if (!thread_wait(&sm.full[s], (c >> 1) & 1, &sm.abort)) break;
+                if (!warp_wait_spin(&sm.full[s], (c >> 1) & 1, &sm.abort)) return false;
                 tc_fence_after();
-                // Base descriptors; a k-step moves the start address only
-                // (the 14-bit address field cannot carry: smem < 256 KB).
+                ChainStage &st = sm.st[s];
                 const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
                 const uint64_t d_tb = smem_desc(smem_u32(st.tb), 16, 1024);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_w(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
+                return true;
+            };
+            bool ok = issue_u(0);
+            for (int c = 0; ok && c < nc; ++c) {
+                const int s = c & 1;
+                ChainStage &st = sm.st[s];
+                // Base descriptors; a k-step moves the start address only
+                // (the 14-bit address field cannot carry: smem < 256 KB).
                 const uint64_t d_wt = smem_desc(smem_u32(st.wt), kTile, 1024);
                 const uint64_t d_q = smem_desc(smem_u32(st.q), 16, 1024);
                 const uint64_t d_k = smem_desc(smem_u32(st.k), kTile, 1024);
                 const uint64_t d_p = smem_desc(smem_u32(st.p), 16, 1024);
-                // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
-                constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
-                if (!thread_wait(&sm.s16_ready, c & 1, &sm.abort)) break;
+                const uint32_t ns = kColNS + 64 * (c & 1);
+                if (!warp_wait_spin(&sm.s16_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
-                constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16_ta(tmem + kColD, tmem + kColNS + 8 * k, d_wt + 128 * k, id_w, 1);
-                mma_commit(&sm.d_done);
-                if (c > 0 && !thread_wait(&sm.o_free, (c - 1) & 1, &sm.abort)) break;
-                tc_fence_after();
+                    mma_bf16_ta_w(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
+                mma_commit_w(&sm.d_done);
                 // O1 = (-S0) Q^T                         [M=128 dv, N=64, K=128 dk]
-                constexpr uint32_t id_q = idesc_bf16(128, 64, false, false);
+                // Needs the output warps to have read chunk c - 1's O1; issue it
+                // now if they have, else after the state update so that the
+                // state chain never waits for the output path.
+                auto issue_o1 = [&]() {
+                    tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16_ta(tmem + kColO1, tmem + kColNS + 8 * k,
-                                d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_q, k > 0);
-                if (!thread_wait(&sm.dt_ready, c & 1, &sm.abort)) break;
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ta_w(tmem + kColO1, tmem + ns + 8 * k,
+                                      d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_q, k > 0);
+                };
+                int o1_now = 1;
+                if (c > 0) {
+                    if (lane == 0) o1_now = mbar_try_wait(&sm.o_free, (c - 1) & 1) ? 1 : 0;
+                    o1_now = __shfl_sync(0xffffffffu, o1_now, 0);
+                }
+                if (o1_now) issue_o1();
+                if (!warp_wait_spin(&sm.dt_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
-                // S += (Delta^T diag(e^{gamma_L - gamma})) K   [M=128 dv, N=128 dk, K=64]
-                constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);
+                // S^ += (Delta^T diag(e^{gamma_L - gamma}) / sigma) K   [M=128, N=128, K=64]
+                // as two N = 64 halves (an N = 128 MMA with A in TMEM runs
+                // several times slower than two N = 64 ones).
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ta(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
-                mma_commit(&sm.s_done);
+                for (int k = 0; k < 4; ++k) {
+                    mma_bf16_ta_w(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
+                    mma_bf16_ta_w(tmem + kColS + 64, tmem + kColDTS + 8 * k,
+                                  d_k + (kTile >> 4) + 128 * k, id_s, 1);
+                }
+                mma_commit_w(&sm.s_done);
+                if (!o1_now) {
+                    if (!warp_wait_spin(&sm.o_free, (c - 1) & 1, &sm.abort)) break;
+                    issue_o1();
+                }
                 // O2 = Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16_ta(tmem + kColO2, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, k > 0);
-                mma_commit(&sm.o_done);
-                mma_commit(&sm.empty[s]);
+                    mma_bf16_ta_w(tmem + kColO2, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, k > 0);
+                mma_commit_w(&sm.o_done);
+                mma_commit_w(&sm.empty[s]);
+                if (c + 1 < nc) ok = issue_u(c + 1);
             }
-            mma_commit(&sm.fin);
+            mma_commit_w(&sm.fin);
         }
     } else if (warp < 10) {
         // ---------------- state warps 2-9: row j, half h2 of the state's
-        // columns (and of Delta's 64 tokens).  E3: Delta^T -> bf16 A operands;
-        // E6: the updated state -> -S0 (bf16) and the pre-scaled fp32 state.
+        // columns (and of Delta's 64 tokens).  The state is kept in TMEM as
+        // S^ with S = sigma S^: the chunk decay e^{gamma_L} folds into sigma,
+        // and 1 / sigma into the Delta operand of the update, so the fp32
+        // state is only rewritten when sigma gets small (renormalisation).
+        // E3: Delta^T -> bf16 A operands; E6: S -> -S0 (bf16).
         const int h2 = (warp - 2) >> 2;
-        const uint32_t t_ns = tmem + lane_base + kColNS + 32 * h2;
+        const uint32_t t_ns = tmem + lane_base + kColNS + 32 * h2;  // + 64 * (chunk & 1)
         const uint32_t t_s = tmem + lane_base + kColS + 64 * h2;
-        bool ok = warp_wait(&sm.full[0], 0, &sm.abort);
-        if (ok) {
+        float sigma = 1.f;
+        bool ok = true;
+        {
             float x[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
@@ -791,19 +836,33 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[c] = v4.x; x[c + 1] = v4.y; x[c + 2] = v4.z; x[c + 3] = v4.w;
             }
-            store_state(t_ns, t_s, x, sm.egdec[0][C - 1]);
+            store_state(t_ns, t_s, x, 1.f);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.s16_ready);
         }
         for (int c = 0; ok && c < nc; ++c) {
-            const int s = c & 1;
-            const float *dec = sm.egdec[s] + C;
-            // Total decay of the next chunk, for pre-scaling the state (read
-            // early, straight from the prep kernel's output).
-            const float next_decay = c + 1 < nc ? gl[(size_t)(c_begin + c + 1) * Hv + h] : 1.f;
+            const float *dec = sm.egdec[c & 3] + C;
+            const float decay = gl[(size_t)(c_begin + c) * Hv + h];  // e^{gamma_L} of chunk c
             if (!(ok = warp_wait(&sm.d_done, c & 1, &sm.abort))) break;
             tc_fence_after();
+            float sigma_next = sigma * decay;
+            if (!(sigma_next >= kRenorm)) {
+                // Fold sigma_next into S^ (sigma becomes 1).  G6 of the previous
+                // chunk has completed (its s_done was observed) and this
+                // chunk's G6 waits for dt_ready, so S^ is ours to rewrite.
+                float x[64];
+                tmem_ld64(t_s, x);
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sigma_next * x[i]);
+                tmem_st32(t_s, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sigma_next * x[32 + i]);
+                tmem_st32(t_s + 32, r);
+                sigma_next = 1.f;
+            }
+            const float inv = 1.f / sigma_next;
             {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + kColD + 32 * h2, r);
@@ -814,15 +873,16 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const float d0 = __uint_as_float(r[2 * i]), d1 = __uint_as_float(r[2 * i + 1]);
                     const float2 dv = *reinterpret_cast<const float2 *>(dec + 32 * h2 + 2 * i);
                     pd[i] = pack_bf16(d0, d1);
-                    ps[i] = pack_bf16(d0 * dv.x, d1 * dv.y);
+                    ps[i] = pack_bf16(d0 * dv.x * inv, d1 * dv.y * inv);
                 }
                 tmem_st16(tmem + lane_base + kColDT + 16 * h2, pd);
                 tmem_st16(tmem + lane_base + kColDTS + 16 * h2, ps);
                 tmem_st_wait();
             }
+            sigma = sigma_next;
             tc_fence_before();
             mbar_arrive(&sm.dt_ready);
-            mbar_arrive(&sm.empty[s]);
+            mbar_arrive(&sm.empty[c & 1]);
             if (!(ok = warp_wait(&sm.s_done, c & 1, &sm.abort))) break;
             tc_fence_after();
             {
@@ -834,10 +894,15 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 64; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) =
-                                make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                                make_float4(sigma * x[i], sigma * x[i + 1], sigma * x[i + 2],
+                                            sigma * x[i + 3]);
                     }
                 } else {
-                    store_state(t_ns, t_s, x, next_decay);
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = pack_bf16(-sigma * x[2 * i], -sigma * x[2 * i + 1]);
+                    tmem_st32(t_ns + 64 * ((c + 1) & 1), r);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&sm.s16_ready);
@@ -862,7 +927,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (leader) bulk_wait_group_read<1>();  // the store from chunk c - 2 has read it
                 named_barrier(1, kOutThreads);
             }
-            const float *eg = sm.egdec[s];
+            const float *eg = sm.egdec[c & 3];
             __nv_bfloat16 *op = out + ((size_t)tok0 * Hv + h) * D + j;
             const size_t tstride = (size_t)Hv * D;
 #pragma unroll
@@ -898,7 +963,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         if (32 * hh + t < L) op[(32 * hh + t) * tstride] = __float2bfloat16_rn(o[t]);
                 }
             }
-            mbar_arrive(&sm.empty[s]);
+            mbar_arrive(&sm.eg_free[c & 3]);
             if (full_tile) {
                 fence_proxy_async_smem();
                 named_barrier(1, kOutThreads);
@@ -919,7 +984,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mbar_wait(&sm.full[c & 1], (c >> 1) & 1, 200000000ll);
         }
     }
-    if (tid == 32) mbar_wait(&sm.fin, 0, 200000000ll);
+    if (tid == 32) mbar_wait(&sm.fin, 0, 200000000ll);  // MMA warp's final commit
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

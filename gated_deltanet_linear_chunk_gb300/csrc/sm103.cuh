@@ -114,14 +114,43 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-// Single-thread bounded wait with the same polling discipline.
+// Warp-cooperative bounded wait without the suspend hint (for the warp that
+// issues MMAs, where wake-up latency matters): lane 0 polls, the warp leaves
+// together.
+__device__ __forceinline__ bool warp_wait_spin(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               long long limit = 4000000000ll) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        if (!mbar_try_wait(bar, parity)) {
+            const long long t0 = clock64();
+            for (uint32_t i = 1;; ++i) {
+                if (mbar_try_wait(bar, parity)) break;
+                if ((i & 255) == 0) {
+                    if (abort && *abort) { ok = 0; break; }
+                    if (clock64() - t0 > limit) {
+                        if (abort) *abort = 1;
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// Single-thread bounded wait for the latency-critical roles (TMA producer,
+// MMA issuer): plain polling, no suspend hint, time limit checked every 256
+// polls.
 __device__ __forceinline__ bool thread_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                             long long limit = 4000000000ll) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_sleep(bar, parity, 100000)) return true;
-        if ((i & 15) == 0) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 0) {
             if (abort && *abort) return false;
             if (clock64() - t0 > limit) {
                 if (abort) *abort = 1;

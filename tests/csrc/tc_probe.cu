@@ -15,6 +15,10 @@
 //   6: A from TMEM [128 x K] (packed bf16 pairs per column), B K-major [N x K]
 //      (K = 128, N = 64)
 //   8: as 7, issued warp-uniformly by warp 0 (elect.sync inside the asm)
+//  10: group latency (issue -> commit -> wait, best of 10) of MMA groups:
+//      v0 1 MMA N=64; v1 8 MMAs N=64 one accumulator; v2 8 as 2 interleaved
+//      accumulators; v3 8 independent accumulators; v4 4 MMAs N=128 one
+//      accumulator; v5 4 MMAs N=128 as 2 accumulators (A in TMEM throughout)
 //   9: timing of 64 MMAs (A smem, B K-major, warp-uniform issue) in one
 //      accumulator chain vs interleaved over several accumulators:
 //      v0 N=64 x1, v1 N=64 x4, v2 N=128 x1, v3 N=128 x2, v4 N=256 x1, v5 N=64 x2
@@ -39,6 +43,41 @@ __device__ void put(uint8_t *tile, int rows, int row, int col, float x) {
     const int atom = col / 64, c = col % 64;
     uint8_t *p = tile + atom * rows * 128 + swz(row, c / 8) + (c % 8) * 2;
     *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+template <int V>
+__device__ void time_groups(uint32_t a0, uint32_t b0, uint32_t tmem, uint64_t *bar, float *d,
+                            int &phase) {
+    // v0: 8 x N=64, A TMEM, B K-major      v1: 8 x N=64, A TMEM, B MN-major
+    // v2: 8 x N=64, A smem K-major, B K-major
+    // v3: 8 x N=64, A smem MN-major, B K-major
+    // v4: 4 x N=128, A TMEM, B K-major     v5: 4 x N=128, A TMEM, B MN-major
+    constexpr int count = V >= 4 ? 4 : 8;
+    constexpr int Nn = V >= 4 ? 128 : 64;
+    constexpr bool a_tm = (V == 0 || V == 1 || V == 4 || V == 5);
+    constexpr bool a_mn = (V == 3);
+    constexpr bool b_mn = (V == 1 || V == 5);
+    const uint64_t ad = a_mn ? smem_desc(a0, 8192, 1024) : smem_desc(a0, 16, 1024);
+    const uint64_t bd = b_mn ? smem_desc(b0, 8192, 1024) : smem_desc(b0, 16, 1024);
+    constexpr uint32_t id = idesc_bf16(128, Nn, a_mn, b_mn);
+    long long best = 1ll << 40;
+    for (int rep = 0; rep < 10; ++rep) {
+        const long long t0 = clock64();
+#pragma unroll
+        for (int r = 0; r < count; ++r) {
+            const uint64_t b = b_mn ? bd + 128 * (r % 4) : bd + 2 * (r % 4);
+            if (a_tm)
+                mma_bf16_ta_w(tmem, tmem + 384 + 8 * (r % 8), b, id, r > 0);
+            else
+                mma_bf16_w(tmem, a_mn ? ad + 128 * (r % 4) : ad + 2 * (r % 4), b, id, r > 0);
+        }
+        mma_commit_w(bar);
+        warp_wait(bar, phase & 1, nullptr);
+        ++phase;
+        const long long t1 = clock64();
+        best = min(best, t1 - t0);
+    }
+    if ((threadIdx.x & 31) == 0) d[V] = (float)best;
 }
 
 template <int V>
@@ -116,7 +155,7 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     } else {                    // A [M rows][K]: K-major, atoms over K
         for (int i = tid; i < M * K; i += 128) put(sa, M, i / K, i % K, a[i]);
     }
-    if (mode == 9) {            // B [256 rows][64]: one atom of 32 KB
+    if (mode == 9 || mode == 10) {  // B [256 rows][64]: one atom of 32 KB
         for (int i = tid; i < 256 * 64; i += 128) put(sb, 256, i / 64, i % 64, b[i % (64 * 128)]);
     } else if (mode == 7) {     // B [128 rows][K] so both N = 64 and N = 128 read valid data
         for (int i = tid; i < 128 * K; i += 128) put(sb, 128, i / K, i % K, b[i % (64 * K)]);
@@ -127,7 +166,7 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
     }
     fence_proxy_async_smem();
     if (warp == 0) {
-        tmem_alloc(&tslot, 256);
+        tmem_alloc(&tslot, mode == 10 ? 512 : 256);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -151,6 +190,21 @@ extern "C" __global__ void __launch_bounds__(128) tc_probe_kernel(const float *a
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+    }
+    if (mode == 10) {
+        if (warp == 0) {
+            int phase = 0;
+            time_groups<0>(a0, b0, tmem, &bar, d, phase);
+            time_groups<1>(a0, b0, tmem, &bar, d, phase);
+            time_groups<2>(a0, b0, tmem, &bar, d, phase);
+            time_groups<3>(a0, b0, tmem, &bar, d, phase);
+            time_groups<4>(a0, b0, tmem, &bar, d, phase);
+            time_groups<5>(a0, b0, tmem, &bar, d, phase);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, 512);
+        return;
     }
     if (mode == 9) {
         if (warp == 0) {

@@ -114,3 +114,22 @@ def test_mma_accumulator_chains(probe):
     for v, nm in enumerate(names):
         print(f"[chains] 64 MMAs {nm}: issue {t[2 * v]:.0f} cyc, done {t[2 * v + 1]:.0f} cyc")
     assert (t[1::2] > 0).all()
+
+
+def test_mma_group_latency(probe):
+    """Issue -> commit -> wait latency of small MMA groups (printed)."""
+    rng = np.random.default_rng(10)
+    a = rng.standard_normal((128, 128)).astype(np.float32)
+    b = rng.standard_normal((64, 128)).astype(np.float32)
+    dd = torch.zeros((128, 64), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe_run(torch.from_numpy(a).cuda().data_ptr(),
+                            torch.from_numpy(b).cuda().data_ptr(), dd.data_ptr(), 10, st.data_ptr())
+    assert rc == 0
+    t = dd.flatten()[:6].cpu().numpy()
+    names = ["8 x N=64, A TMEM, B K-major", "8 x N=64, A TMEM, B MN-major",
+             "8 x N=64, A smem K-major, B K-major", "8 x N=64, A smem MN-major, B K-major",
+             "4 x N=128, A TMEM, B K-major", "4 x N=128, A TMEM, B MN-major"]
+    for v, nm in enumerate(names):
+        print(f"[group] {nm}: {t[v]:.0f} cyc")
+    assert (t > 0).all()
