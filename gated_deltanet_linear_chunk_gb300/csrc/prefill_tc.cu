@@ -550,7 +550,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ kernel 3
-constexpr int kChainThreads = 480;  // 15 warps: 0 loads, 1-2 MMAs, 3-10 state, 11-14 output
+constexpr int kChainThreads = 448;  // 14 warps: 0 loads, 1 MMAs, 2-9 state, 10-13 output
 constexpr int kStateThreads = 256;
 constexpr int kOutThreads = 128;
 
@@ -565,7 +565,7 @@ struct ChainStage {
 
 struct ChainSmem {
     ChainStage st[2];
-    uint8_t ostage[2][C * D * 2];  // output tile [64 tokens][128 dv] bf16, for the TMA store
+    uint8_t ostage[3][C * D * 2];  // output tiles [64 tokens][128 dv] bf16, for TMA stores
     float egdec[4][2 * C];         // ring by chunk: e^{gamma_t} then e^{gamma_L - gamma_t}
     uint64_t full[2];              // stage loaded (TMA transaction count)
     uint64_t empty[2];             // stage consumed (MMA commit + state threads)
@@ -576,9 +576,7 @@ struct ChainSmem {
     uint64_t d_done;               // MMA: Delta^T complete
     uint64_t s_done;               // MMA: state update complete
     uint64_t o_done;               // MMA: output accumulators complete
-    uint64_t o1_done[2];           // output MMA warp: O1 complete, per -S0 buffer (a
-                                   // single barrier could run two phases ahead of a waiter)
-    uint64_t fin;                  // MMA warps: everything issued has completed
+    uint64_t fin;                  // MMA: everything issued has completed
     uint32_t tmem;
     int abort;
     int issued;
@@ -666,7 +664,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_o);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 2 + kStateThreads);
+            mbar_init(&sm.empty[s], 1 + kStateThreads);
         }
         for (int e = 0; e < 4; ++e) mbar_init(&sm.eg_free[e], kOutThreads);
         mbar_init(&sm.s16_ready, kStateThreads);
@@ -675,9 +673,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(&sm.d_done, 1);
         mbar_init(&sm.s_done, 1);
         mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.o1_done[0], 1);
-        mbar_init(&sm.o1_done[1], 1);
-        mbar_init(&sm.fin, 2);
+        mbar_init(&sm.fin, 1);
         sm.abort = 0;
         sm.issued = 0;
         fence_mbar_init();
@@ -735,96 +731,98 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         }
     } else if (warp == 1) {
-        // ---------------- state-chain MMA warp: U^T, Delta^T and the state
-        // update only.  The whole warp runs the loop with identical values
-        // (descriptors stay warp-uniform) and one elected lane issues each
-        // tcgen05 instruction; it never waits for the output path.
-        constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
-        constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
-        constexpr uint32_t id_s = idesc_bf16(128, 64, false, true);
-        // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
-        auto issue_u = [&](int c) -> bool {
-            const int s = c & 1;
-            if (!warp_wait_spin(&sm.full[s], (c >> 1) & 1, &sm.abort)) return false;
-            tc_fence_after();
-            ChainStage &st = sm.st[s];
-            const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
-            const uint64_t d_tb = smem_desc(smem_u32(st.tb), 16, 1024);
+        // ---------------- MMA issuer: the whole warp runs this loop with
+        // identical values (descriptors stay warp-uniform) and one elected
+        // lane issues each tcgen05 instruction.  U^T for chunk c + 1 is issued
+        // right after chunk c's last MMAs, so it runs while the state warps
+        // prepare chunk c + 1's S0.
+        {
+            constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
+            constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t id_q = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t id_s = idesc_bf16(128, 64, false, true);
+            // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
+            auto issue_u = [&](int c) -> bool {
+                const int s = c & 1;
+                if (!warp_wait_spin(&sm.full[s], (c >> 1) & 1, &sm.abort)) return false;
+                tc_fence_after();
+                ChainStage &st = sm.st[s];
+                const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
+                const uint64_t d_tb = smem_desc(smem_u32(st.tb), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16_w(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
-            return true;
-        };
-        bool ok = issue_u(0);
-        for (int c = 0; ok && c < nc; ++c) {
-            const int s = c & 1;
-            ChainStage &st = sm.st[s];
-            // Base descriptors; a k-step moves the start address only (the
-            // 14-bit address field cannot carry: smem < 256 KB).
-            const uint64_t d_wt = smem_desc(smem_u32(st.wt), kTile, 1024);
-            const uint64_t d_k = smem_desc(smem_u32(st.k), kTile, 1024);
-            const uint32_t ns = kColNS + 64 * (c & 1);
-            if (!warp_wait_spin(&sm.s16_ready, c & 1, &sm.abort)) break;
-            tc_fence_after();
-            // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_w(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
+                return true;
+            };
+            bool ok = issue_u(0);
+            for (int c = 0; ok && c < nc; ++c) {
+                const int s = c & 1;
+                ChainStage &st = sm.st[s];
+                // Base descriptors; a k-step moves the start address only
+                // (the 14-bit address field cannot carry: smem < 256 KB).
+                const uint64_t d_wt = smem_desc(smem_u32(st.wt), kTile, 1024);
+                const uint64_t d_q = smem_desc(smem_u32(st.q), 16, 1024);
+                const uint64_t d_k = smem_desc(smem_u32(st.k), kTile, 1024);
+                const uint64_t d_p = smem_desc(smem_u32(st.p), 16, 1024);
+                const uint32_t ns = kColNS + 64 * (c & 1);
+                if (!warp_wait_spin(&sm.s16_ready, c & 1, &sm.abort)) break;
+                tc_fence_after();
+                // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_bf16_ta_w(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
-            mma_commit_w(&sm.d_done);
-            if (!warp_wait_spin(&sm.dt_ready, c & 1, &sm.abort)) break;
-            tc_fence_after();
-            // S^ += (Delta^T diag(e^{gamma_L - gamma}) / sigma) K   [M=128, N=128, K=64]
-            // as two N = 64 halves (an N = 128 MMA with A in TMEM runs several
-            // times slower than two N = 64 ones).
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ta_w(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
+                mma_commit_w(&sm.d_done);
+                // O1 = (-S0) Q^T                         [M=128 dv, N=64, K=128 dk]
+                // Needs the output warps to have read chunk c - 1's O1; issue it
+                // now if they have, else after the state update so that the
+                // state chain never waits for the output path.
+                auto issue_o1 = [&]() {
+                    tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                mma_bf16_ta_w(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
-                mma_bf16_ta_w(tmem + kColS + 64, tmem + kColDTS + 8 * k,
-                              d_k + (kTile >> 4) + 128 * k, id_s, 1);
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ta_w(tmem + kColO1, tmem + ns + 8 * k,
+                                      d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_q, k > 0);
+                };
+                int o1_now = 1;
+                if (c > 0) {
+                    if (lane == 0) o1_now = mbar_try_wait(&sm.o_free, (c - 1) & 1) ? 1 : 0;
+                    o1_now = __shfl_sync(0xffffffffu, o1_now, 0);
+                }
+                if (o1_now) issue_o1();
+                if (!warp_wait_spin(&sm.dt_ready, c & 1, &sm.abort)) break;
+                tc_fence_after();
+                // S^ += (Delta^T diag(e^{gamma_L - gamma}) / sigma) K   [M=128, N=128, K=64]
+                // as two N = 64 halves (an N = 128 MMA with A in TMEM runs
+                // several times slower than two N = 64 ones).
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    mma_bf16_ta_w(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
+                    mma_bf16_ta_w(tmem + kColS + 64, tmem + kColDTS + 8 * k,
+                                  d_k + (kTile >> 4) + 128 * k, id_s, 1);
+                }
+                mma_commit_w(&sm.s_done);
+                if (!o1_now) {
+                    if (!warp_wait_spin(&sm.o_free, (c - 1) & 1, &sm.abort)) break;
+                    issue_o1();
+                }
+                // O2 = Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_ta_w(tmem + kColO2, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, k > 0);
+                mma_commit_w(&sm.o_done);
+                mma_commit_w(&sm.empty[s]);
+                if (c + 1 < nc) ok = issue_u(c + 1);
             }
-            mma_commit_w(&sm.s_done);
-            mma_commit_w(&sm.empty[s]);
-            if (c + 1 < nc) ok = issue_u(c + 1);
+            mma_commit_w(&sm.fin);
         }
-        mma_commit_w(&sm.fin);
-    } else if (warp == 2) {
-        // ---------------- output MMA warp: O1 = (-S0) Q^T and O2 = Delta^T P^T,
-        // lagging the state chain as the output warps allow.
-        constexpr uint32_t id_q = idesc_bf16(128, 64, false, false);
-        for (int c = 0; c < nc; ++c) {
-            const int s = c & 1;
-            ChainStage &st = sm.st[s];
-            const uint64_t d_q = smem_desc(smem_u32(st.q), 16, 1024);
-            const uint64_t d_p = smem_desc(smem_u32(st.p), 16, 1024);
-            const uint32_t ns = kColNS + 64 * (c & 1);
-            if (!warp_wait(&sm.full[s], (c >> 1) & 1, &sm.abort)) break;
-            if (!warp_wait(&sm.s16_ready, c & 1, &sm.abort)) break;
-            if (c > 0 && !warp_wait(&sm.o_free, (c - 1) & 1, &sm.abort)) break;
-            tc_fence_after();
-            // O1 = (-S0) Q^T                         [M=128 dv, N=64, K=128 dk]
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_bf16_ta_w(tmem + kColO1, tmem + ns + 8 * k,
-                              d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_q, k > 0);
-            mma_commit_w(&sm.o1_done[c & 1]);
-            if (!warp_wait(&sm.dt_ready, c & 1, &sm.abort)) break;
-            tc_fence_after();
-            // O2 = Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16_ta_w(tmem + kColO2, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, k > 0);
-            mma_commit_w(&sm.o_done);
-            mma_commit_w(&sm.empty[s]);
-        }
-        mma_commit_w(&sm.fin);
-    } else if (warp < 11) {
-        // ---------------- state warps 3-10: row j, half h2 of the state's
+    } else if (warp < 10) {
+        // ---------------- state warps 2-9: row j, half h2 of the state's
         // columns (and of Delta's 64 tokens).  The state is kept in TMEM as
         // S^ with S = sigma S^: the chunk decay e^{gamma_L} folds into sigma,
         // and 1 / sigma into the Delta operand of the update, so the fp32
         // state is only rewritten when sigma gets small (renormalisation).
         // E3: Delta^T -> bf16 A operands; E6: S -> -S0 (bf16).
-        const int h2 = (warp - 3) >> 2;
+        const int h2 = (warp - 2) >> 2;
         const uint32_t t_ns = tmem + lane_base + kColNS + 32 * h2;  // + 64 * (chunk & 1)
         const uint32_t t_s = tmem + lane_base + kColS + 64 * h2;
         float sigma = 1.f;
@@ -865,9 +863,6 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 sigma_next = 1.f;
             }
             const float inv = 1.f / sigma_next;
-            // DT is still read by chunk c - 1's O2 MMA until o_done(c - 1).
-            if (c > 0 && !(ok = warp_wait(&sm.o_done, (c - 1) & 1, &sm.abort))) break;
-            tc_fence_after();
             {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + kColD + 32 * h2, r);
@@ -903,12 +898,6 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                             sigma * x[i + 3]);
                     }
                 } else {
-                    // The -S0 buffer for chunk c + 1 was chunk c - 1's: wait
-                    // until that chunk's O1 MMA has read it.
-                    if (c > 0 && !(ok = warp_wait(&sm.o1_done[(c - 1) & 1], ((c - 1) >> 1) & 1,
-                                                  &sm.abort)))
-                        break;
-                    tc_fence_after();
                     uint32_t r[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -921,11 +910,11 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         }
     } else {
-        // ---------------- output warps 11-14: o_t = e^{gamma_t} S0 q_t +
+        // ---------------- output warps 10-13: o_t = e^{gamma_t} S0 q_t +
         // (Delta^T P^T)_t for value dim j, staged as a [64 tokens][128 dv]
         // tile and written with one TMA store (plain stores for a short last
         // chunk, whose tile would reach into the next sequence).
-        const bool leader = (warp == 11 && lane == 0);
+        const bool leader = (warp == 10 && lane == 0);
         for (int c = 0; c < nc; ++c) {
             const int s = c & 1;
             const int4 e = table[c_begin + c];
@@ -933,9 +922,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!warp_wait(&sm.o_done, c & 1, &sm.abort)) break;
             tc_fence_after();
             const bool full_tile = (L == C);
-            uint8_t *stg = sm.ostage[c & 1];
+            uint8_t *stg = sm.ostage[c % 3];
             if (full_tile) {
-                if (leader) bulk_wait_group_read<1>();  // the store from chunk c - 2 has read it
+                if (leader) bulk_wait_group_read<2>();  // the store from chunk c - 3 has read it
                 named_barrier(1, kOutThreads);
             }
             const float *eg = sm.egdec[c & 3];
