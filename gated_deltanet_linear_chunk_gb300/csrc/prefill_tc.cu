@@ -66,9 +66,10 @@ enum DeviceError : int { kErrNone = 0, kErrCuSeqlens = 1, kErrTimeout = 2 };
 constexpr int kSlotWT = 0;                    // W^T  [128 dk][64 tokens], MN-major B image
 constexpr int kSlotTB = kSlotWT + 2 * kTile;  // T diag(b) [64 out][64 in], K-major B image
 constexpr int kSlotP = kSlotTB + kTile;       // P [64 out][64 in], K-major B image
-constexpr int kSlotEG = kSlotP + kTile;       // e^{gamma_t}, fp32 [64]
+constexpr int kSlotQ = kSlotP + kTile;        // diag(e^gamma) Q [64 tokens][128 dk], K-major B image
+constexpr int kSlotEG = kSlotQ + 2 * kTile;   // e^{gamma_t}, fp32 [64]
 constexpr int kSlotDEC = kSlotEG + 256;       // e^{gamma_L - gamma_t}, fp32 [64]
-constexpr int kSlotBytes = kSlotDEC + 256;    // 33280
+constexpr int kSlotBytes = kSlotDEC + 256;    // 49664
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
@@ -429,6 +430,24 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 *reinterpret_cast<__nv_bfloat16 *>(dp + swz(t, ccol >> 3) + 2 * (ccol & 7)) =
                     __float2bfloat16_rn(val);
             }
+        } else if (tid < 64 || tid >= 256) {
+            // Meanwhile the other four warps write diag(e^gamma) Q of every
+            // value head of the round: the same swizzled image as Q's tiles,
+            // scaled row by row.
+            const int w = tid < 64 ? tid : tid - 192;  // 0 .. 127
+            for (int idx = w; idx < nh * 2 * C * 8; idx += 128) {
+                const int j = idx / (2 * C * 8), a = (idx / (C * 8)) & 1;
+                const int r = (idx >> 3) & (C - 1), cc = idx & 7;
+                const uint32_t off = swz(r, cc);
+                float x[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sm.kq + (2 * a + 1) * kTile + off), x);
+                const float sc = sm.eg[j][r];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] *= sc;
+                const int h = hk * G + j0 + j;
+                *reinterpret_cast<uint4 *>(slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotQ +
+                                           a * kTile + off) = pack8(x);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -554,47 +573,48 @@ constexpr int kChainThreads = 448;  // 14 warps: 0 loads, 1 MMAs, 2-9 state, 10-
 constexpr int kStateThreads = 256;
 constexpr int kOutThreads = 128;
 
-struct ChainStage {
+struct alignas(1024) ChainStage {  // 1024-aligned: the tiles are 128-byte-swizzle atoms
     uint8_t k[2 * kTile];   // K [64 tokens][128 dk] as two 64-column atoms
-    uint8_t q[2 * kTile];   // Q, likewise
+    uint8_t q[2 * kTile];   // diag(e^gamma) Q, likewise
     uint8_t v[2 * kTile];   // V [64 tokens][128 dv]
     uint8_t wt[2 * kTile];  // W^T [128 dk][64 tokens], MN-major B image
     uint8_t tb[kTile];      // T diag(b)
     uint8_t p[kTile];       // P = M o Q K^T
+    float egdec[2 * C];     // e^{gamma_t}, then e^{gamma_L - gamma_t}
 };
 
 struct ChainSmem {
     ChainStage st[2];
     uint8_t ostage[3][C * D * 2];  // output tiles [64 tokens][128 dv] bf16, for TMA stores
-    float egdec[4][2 * C];         // ring by chunk: e^{gamma_t} then e^{gamma_L - gamma_t}
     uint64_t full[2];              // stage loaded (TMA transaction count)
     uint64_t empty[2];             // stage consumed (MMA commit + state threads)
-    uint64_t eg_free[4];           // output threads done with an egdec entry
     uint64_t s16_ready;            // state threads: -S0 (bf16) and pre-scaled S in TMEM
     uint64_t dt_ready;             // state threads: Delta^T copies in TMEM
-    uint64_t o_free;               // output threads: output accumulators read
+    uint64_t o_free[2];            // output threads: output accumulator (by chunk parity) read
     uint64_t d_done;               // MMA: Delta^T complete
     uint64_t s_done;               // MMA: state update complete
-    uint64_t o_done;               // MMA: output accumulators complete
+    uint64_t o_done[2];            // MMA: output accumulator (by chunk parity) complete
     uint64_t fin;                  // MMA: everything issued has completed
     uint32_t tmem;
     int abort;
     int issued;
 };
 
-constexpr uint32_t kStageBytes = 10 * kTile + 512;  // K, Q, V, W^T, T diag b, P, e^gamma/dec
+constexpr uint32_t kStageBytes = 10 * kTile + 512;  // K, Q~, V, W^T, T diag b, P, e^gamma/dec
 constexpr int kPrefetch = 3;  // chunks pulled into L2 ahead of the two staged ones
 // Below this the state's running scale factor is folded back into the
 // stored state (keeps 1 / sigma far from fp32 overflow).
 constexpr float kRenorm = 1.0e-12f;
-// TMEM columns of the recurrence kernel.  D = U^T then Delta^T (fp32); O1 =
-// -S0 Q^T and O2 = Delta^T P^T (fp32); NS = -S0 as bf16 pairs (the A operand
-// of two MMAs, two buffers); S = the fp32 state; DT and DTS = Delta^T and
-// Delta^T diag(e^{gamma_L - gamma}) as bf16 pairs (A operands).
-// NS is double-buffered by chunk parity: chunk c's O1 may be issued after its
-// state update, i.e. after the state warps have written chunk c + 1's -S0.
-constexpr uint32_t kColD = 0, kColO1 = 64, kColO2 = 128, kColNS = 192, kColS = 320,
-                   kColDT = 448, kColDTS = 480;
+// TMEM columns of the recurrence kernel.  D = U^T then Delta^T (fp32); O =
+// S0 Q~^T + Delta^T P^T (fp32, two buffers by chunk parity, so that the
+// output warps read one while the next chunk's output accumulates); NS = -S0
+// as bf16 pairs (the A operand of two MMAs, two buffers); S = the fp32 state;
+// DT and DTS = Delta^T and Delta^T diag(e^{gamma_L - gamma}) as bf16 pairs
+// (A operands).  NS is double-buffered by chunk parity: chunk c's S0 Q~^T may
+// be issued after its state update, i.e. after the state warps have written
+// chunk c + 1's -S0.
+constexpr uint32_t kColD = 0, kColO = 64, kColNS = 192, kColS = 320, kColDT = 448,
+                   kColDTS = 480;
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
     uint32_t r[32];
@@ -625,8 +645,8 @@ __device__ __forceinline__ void store_state(uint32_t t_ns, uint32_t t_s, const f
 }
 
 __global__ void __launch_bounds__(kChainThreads, 1)
-gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_o,
                  const int *__restrict__ chunk_off, const int *__restrict__ order,
                  const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
                  const float *__restrict__ gl, const float *__restrict__ h0,
@@ -658,7 +678,6 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 
     if (tid == 0) {
-        prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_o);
@@ -666,13 +685,14 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1 + kStateThreads);
         }
-        for (int e = 0; e < 4; ++e) mbar_init(&sm.eg_free[e], kOutThreads);
         mbar_init(&sm.s16_ready, kStateThreads);
         mbar_init(&sm.dt_ready, kStateThreads);
-        mbar_init(&sm.o_free, kOutThreads);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.o_free[b], kOutThreads);
+            mbar_init(&sm.o_done[b], 1);
+        }
         mbar_init(&sm.d_done, 1);
         mbar_init(&sm.s_done, 1);
-        mbar_init(&sm.o_done, 1);
         mbar_init(&sm.fin, 1);
         sm.abort = 0;
         sm.issued = 0;
@@ -690,44 +710,46 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 0) {
         // ---------------- producer: TMA tiles and the prep kernel's slot;
         // chunks kPrefetch ahead are pulled into L2 so that a stage's loads
-        // hit L2 when the stage frees up.
-        if (lane == 0) {
+        // hit L2 when the stage frees up.  The whole warp runs the loop and one
+        // elected lane issues each copy.
+        {
             // A sequence's chunks are consecutive 64-token windows.
             const int seq_tok0 = table[c_begin].y;
             auto prefetch = [&](int c) {
+                if (lane != 0) return;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
                 tma_prefetch_3d(&tm_k, 0, hk, tok0);
                 tma_prefetch_3d(&tm_k, 64, hk, tok0);
-                tma_prefetch_3d(&tm_q, 0, hk, tok0);
-                tma_prefetch_3d(&tm_q, 64, hk, tok0);
                 tma_prefetch_3d(&tm_v, 0, h, tok0);
                 tma_prefetch_3d(&tm_v, 64, h, tok0);
                 bulk_prefetch_l2(slots + ((size_t)ch * Hv + h) * kSlotBytes, kSlotBytes);
             };
+            #pragma unroll 1
             for (int c = 2; c < min(nc, 2 + kPrefetch); ++c) prefetch(c);
+            __syncwarp();
+            #pragma unroll 1
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
-                if (c >= 2 && !thread_wait(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
-                if (c >= 4 && !thread_wait(&sm.eg_free[c & 3], ((c >> 2) + 1) & 1, &sm.abort)) break;
+                if (c >= 2 && !warp_wait_spin(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
                 ChainStage &st = sm.st[s];
                 uint64_t *bar = &sm.full[s];
                 const uint8_t *slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
-                mbar_arrive_expect_tx(bar, kStageBytes);
-                tma_load_3d(st.k, &tm_k, 0, hk, tok0, bar);
-                tma_load_3d(st.k + kTile, &tm_k, 64, hk, tok0, bar);
-                tma_load_3d(st.q, &tm_q, 0, hk, tok0, bar);
-                tma_load_3d(st.q + kTile, &tm_q, 64, hk, tok0, bar);
-                tma_load_3d(st.v, &tm_v, 0, h, tok0, bar);
-                tma_load_3d(st.v + kTile, &tm_v, 64, h, tok0, bar);
-                bulk_load(st.wt, slot + kSlotWT, 2 * kTile, bar);
-                bulk_load(st.tb, slot + kSlotTB, kTile, bar);
-                bulk_load(st.p, slot + kSlotP, kTile, bar);
-                bulk_load(sm.egdec[c & 3], slot + kSlotEG, 512, bar);
-                sm.issued = c + 1;
+                mbar_arrive_expect_tx_w(bar, kStageBytes);
+                tma_load_3d_w(st.k, &tm_k, 0, hk, tok0, bar);
+                tma_load_3d_w(st.k + kTile, &tm_k, 64, hk, tok0, bar);
+                tma_load_3d_w(st.v, &tm_v, 0, h, tok0, bar);
+                tma_load_3d_w(st.v + kTile, &tm_v, 64, h, tok0, bar);
+                bulk_load_w(st.wt, slot + kSlotWT, 2 * kTile, bar);
+                bulk_load_w(st.tb, slot + kSlotTB, kTile, bar);
+                bulk_load_w(st.p, slot + kSlotP, kTile, bar);
+                bulk_load_w(st.q, slot + kSlotQ, 2 * kTile, bar);
+                bulk_load_w(st.egdec, slot + kSlotEG, 512, bar);
+                if (lane == 0) sm.issued = c + 1;
                 if (c + 2 + kPrefetch - 1 < nc && c >= 1) prefetch(c + 2 + kPrefetch - 1);
+                __syncwarp();
             }
         }
     } else if (warp == 1) {
@@ -740,6 +762,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
             constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
             constexpr uint32_t id_q = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t id_qn = idesc_bf16(128, 64, false, false, true);  // A negated
             constexpr uint32_t id_s = idesc_bf16(128, 64, false, true);
             // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
             auto issue_u = [&](int c) -> bool {
@@ -755,6 +778,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 return true;
             };
             bool ok = issue_u(0);
+            #pragma unroll 1
             for (int c = 0; ok && c < nc; ++c) {
                 const int s = c & 1;
                 ChainStage &st = sm.st[s];
@@ -765,6 +789,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint64_t d_k = smem_desc(smem_u32(st.k), kTile, 1024);
                 const uint64_t d_p = smem_desc(smem_u32(st.p), 16, 1024);
                 const uint32_t ns = kColNS + 64 * (c & 1);
+                const uint32_t ob = kColO + 64 * (c & 1);
                 if (!warp_wait_spin(&sm.s16_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
@@ -772,20 +797,22 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int k = 0; k < 8; ++k)
                     mma_bf16_ta_w(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
                 mma_commit_w(&sm.d_done);
-                // O1 = (-S0) Q^T                         [M=128 dv, N=64, K=128 dk]
-                // Needs the output warps to have read chunk c - 1's O1; issue it
-                // now if they have, else after the state update so that the
-                // state chain never waits for the output path.
+                // O = S0 Q~^T (A = -S0, negated)         [M=128 dv, N=64, K=128 dk]
+                // into this chunk's output buffer, free once the output warps
+                // have read chunk c - 2's; issue it now if they have (the usual
+                // case), else after the state update so that the state chain
+                // never waits for the output path.
                 auto issue_o1 = [&]() {
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_bf16_ta_w(tmem + kColO1, tmem + ns + 8 * k,
-                                      d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_q, k > 0);
+                        mma_bf16_ta_w(tmem + ob, tmem + ns + 8 * k,
+                                      d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_qn, k > 0);
                 };
                 int o1_now = 1;
-                if (c > 0) {
-                    if (lane == 0) o1_now = mbar_try_wait(&sm.o_free, (c - 1) & 1) ? 1 : 0;
+                if (c >= 2) {
+                    if (lane == 0)
+                        o1_now = mbar_try_wait(&sm.o_free[c & 1], ((c >> 1) - 1) & 1) ? 1 : 0;
                     o1_now = __shfl_sync(0xffffffffu, o1_now, 0);
                 }
                 if (o1_now) issue_o1();
@@ -802,14 +829,14 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 mma_commit_w(&sm.s_done);
                 if (!o1_now) {
-                    if (!warp_wait_spin(&sm.o_free, (c - 1) & 1, &sm.abort)) break;
+                    if (!warp_wait_spin(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
                     issue_o1();
                 }
-                // O2 = Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
+                // O += Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16_ta_w(tmem + kColO2, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, k > 0);
-                mma_commit_w(&sm.o_done);
+                    mma_bf16_ta_w(tmem + ob, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, 1);
+                mma_commit_w(&sm.o_done[c & 1]);
                 mma_commit_w(&sm.empty[s]);
                 if (c + 1 < nc) ok = issue_u(c + 1);
             }
@@ -841,8 +868,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc_fence_before();
             mbar_arrive(&sm.s16_ready);
         }
+        #pragma unroll 1
         for (int c = 0; ok && c < nc; ++c) {
-            const float *dec = sm.egdec[c & 3] + C;
+            const float *dec = sm.st[c & 1].egdec + C;
             const float decay = gl[(size_t)(c_begin + c) * Hv + h];  // e^{gamma_L} of chunk c
             if (!(ok = warp_wait(&sm.d_done, c & 1, &sm.abort))) break;
             tc_fence_after();
@@ -910,66 +938,60 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         }
     } else {
-        // ---------------- output warps 10-13: o_t = e^{gamma_t} S0 q_t +
-        // (Delta^T P^T)_t for value dim j, staged as a [64 tokens][128 dv]
-        // tile and written with one TMA store (plain stores for a short last
-        // chunk, whose tile would reach into the next sequence).
+        // ---------------- output warps 10-13: o_t = S0 (e^{gamma_t} q_t) +
+        // (Delta^T P^T)_t for this warp's 32 value dims, read from this
+        // chunk's output accumulator with the 16x256b TMEM shape (the m8n8
+        // fragment layout) and written transposed with stmatrix into a
+        // [64 tokens][128 dv] tile held as two 128-byte-swizzled halves, then
+        // stored by TMA (a short last chunk, whose tile would reach into the
+        // next sequence, is copied out row by row instead).
         const bool leader = (warp == 10 && lane == 0);
+        const int hh = q >> 1;                  // dv half of this warp's rows
+        const int k8 = lane & 7, d8 = lane >> 3; // stmatrix row and matrix of this lane
+#pragma unroll 1
         for (int c = 0; c < nc; ++c) {
-            const int s = c & 1;
             const int4 e = table[c_begin + c];
             const int tok0 = e.y, L = e.z;
-            if (!warp_wait(&sm.o_done, c & 1, &sm.abort)) break;
+            if (!warp_wait(&sm.o_done[c & 1], (c >> 1) & 1, &sm.abort)) break;
             tc_fence_after();
-            const bool full_tile = (L == C);
+            uint32_t r[2][32];
+            tmem_ld16x256b_x8(tmem + lane_base + kColO + 64 * (c & 1), r[0]);
+            tmem_ld16x256b_x8(tmem + lane_base + (16u << 16) + kColO + 64 * (c & 1), r[1]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&sm.o_free[c & 1]);
             uint8_t *stg = sm.ostage[c % 3];
-            if (full_tile) {
-                if (leader) bulk_wait_group_read<2>();  // the store from chunk c - 3 has read it
-                named_barrier(1, kOutThreads);
-            }
-            const float *eg = sm.egdec[c & 3];
-            __nv_bfloat16 *op = out + ((size_t)tok0 * Hv + h) * D + j;
-            const size_t tstride = (size_t)Hv * D;
+            if (leader) bulk_wait_group_read<2>();  // the stores from chunk c - 3 have read it
+            named_barrier(1, kOutThreads);
+            // Matrix d8 of a group: value dims 32 (q & 1) + 8 d8 .. + 7 of half
+            // hh (16-byte chunk 4 (q & 1) + d8 of a 128-byte row); row k8 is
+            // token 8 g + k8.
+            uint8_t *tile = stg + hh * kTile;
+            const uint32_t chunk = 4 * (q & 1) + d8;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t r1[32], r2[32];
-                tmem_ld32(tmem + lane_base + kColO1 + 32 * hh, r1);
-                tmem_ld32(tmem + lane_base + kColO2 + 32 * hh, r2);
-                tmem_ld_wait();
-                if (hh == 1) {
-                    tc_fence_before();
-                    mbar_arrive(&sm.o_free);
-                }
-                // All shared-memory reads before the first store: the compiler
-                // cannot tell the staging tile from e^gamma, and would order
-                // each load after the previous store.
-                float o[32];
-#pragma unroll
-                for (int t = 0; t < 32; t += 4) {
-                    const float4 e4 = *reinterpret_cast<const float4 *>(eg + 32 * hh + t);
-                    o[t] = fmaf(-e4.x, __uint_as_float(r1[t]), __uint_as_float(r2[t]));
-                    o[t + 1] = fmaf(-e4.y, __uint_as_float(r1[t + 1]), __uint_as_float(r2[t + 1]));
-                    o[t + 2] = fmaf(-e4.z, __uint_as_float(r1[t + 2]), __uint_as_float(r2[t + 2]));
-                    o[t + 3] = fmaf(-e4.w, __uint_as_float(r1[t + 3]), __uint_as_float(r2[t + 3]));
-                }
-                if (full_tile) {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        *reinterpret_cast<__nv_bfloat16 *>(stg + (32 * hh + t) * (D * 2) + 2 * j) =
-                            __float2bfloat16_rn(o[t]);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        if (32 * hh + t < L) op[(32 * hh + t) * tstride] = __float2bfloat16_rn(o[t]);
-                }
-            }
-            mbar_arrive(&sm.eg_free[c & 3]);
-            if (full_tile) {
+            for (int g = 0; g < C / 8; ++g)
+                stmatrix_x4_trans(tile + swz(8 * g + k8, chunk),
+                                  pack_bf16(__uint_as_float(r[0][4 * g]), __uint_as_float(r[0][4 * g + 1])),
+                                  pack_bf16(__uint_as_float(r[0][4 * g + 2]), __uint_as_float(r[0][4 * g + 3])),
+                                  pack_bf16(__uint_as_float(r[1][4 * g]), __uint_as_float(r[1][4 * g + 1])),
+                                  pack_bf16(__uint_as_float(r[1][4 * g + 2]), __uint_as_float(r[1][4 * g + 3])));
+            if (L == C) {
                 fence_proxy_async_smem();
                 named_barrier(1, kOutThreads);
                 if (leader) {
                     tma_store_3d(&tm_o, 0, h, tok0, stg);
+                    tma_store_3d(&tm_o, 64, h, tok0, stg + kTile);
                     bulk_commit_group();
+                }
+            } else {
+                named_barrier(1, kOutThreads);
+                // Rows t < L: 16 chunks of 16 bytes each, un-swizzled.
+                const int tid_o = tid - 10 * 32;
+                for (int idx = tid_o; idx < L * 16; idx += kOutThreads) {
+                    const int t = idx >> 4, cc = idx & 15;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + (cc >> 3) * kTile +
+                                                                     swz(t, cc & 7));
+                    *reinterpret_cast<uint4 *>(out + ((size_t)(tok0 + t) * Hv + h) * D + 8 * cc) = v;
                 }
             }
         }
@@ -1007,18 +1029,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [T, H, 128] bf16 tensor, boxes of 64 features x 1 head x 64 tokens, 128-byte swizzle.
-bool encode_thd(CUtensorMap *map, const void *base, int64_t T, int H, bool out_tile = false) {
+bool encode_thd(CUtensorMap *map, const void *base, int64_t T, int H) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    // Loads: 64-feature boxes, 128-byte swizzle (MMA operand layout).  The
-    // output store: whole 128-feature rows, no swizzle.
-    const cuuint32_t box[3] = {out_tile ? (cuuint32_t)D : 64u, 1, (cuuint32_t)C};
+    // 64-feature boxes, 128-byte swizzle: the MMA operand layout for loads,
+    // and the bank-conflict-free staging layout of the output stores.
+    const cuuint32_t box[3] = {64u, 1, (cuuint32_t)C};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               out_tile ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1049,7 +1071,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         if (!encode_thd(&tq, q, p.total_tokens, p.num_k_heads) ||
             !encode_thd(&tk, k, p.total_tokens, p.num_k_heads) ||
             !encode_thd(&tv, v, p.total_tokens, p.num_v_heads) ||
-            !encode_thd(&to, out, p.total_tokens, p.num_v_heads, true))
+            !encode_thd(&to, out, p.total_tokens, p.num_v_heads))
             return GDN_ERR_CUDA;
     } else {
         memset(&tq, 0, sizeof(tq));
@@ -1078,7 +1100,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
                              (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
     gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
-        tq, tk, tv, to, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
+        tk, tv, to, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
         err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -68,7 +68,7 @@ def test_noalloc_matches_prefill_twice(lib, dtype, d, tol):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(lib):
-    # bf16, d=128, 48 value heads needs ~16 KiB of workspace per chunk and
+    # bf16, d=128, 48 value heads needs ~48 KiB of workspace per chunk and
     # value head: 200k tokens need far more than 64 MiB.
     T = 200_000
     prob = gdn.Problem(1, T, 16, 48, 128, 128, gdn.GDN_BF16, None, 0)
