@@ -799,23 +799,17 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 mma_commit_w(&sm.d_done);
                 // O = S0 Q~^T (A = -S0, negated)         [M=128 dv, N=64, K=128 dk]
                 // into this chunk's output buffer, free once the output warps
-                // have read chunk c - 2's; issue it now if they have (the usual
-                // case), else after the state update so that the state chain
-                // never waits for the output path.
-                auto issue_o1 = [&]() {
-                    tc_fence_after();
+                // have read chunk c - 2's (they have two chunk steps for it, so
+                // the wait normally returns at once).  Each MMA group has one
+                // copy of its code: the issuing warp's loop has to stay small
+                // enough for the instruction cache, or its MMAs issue at
+                // instruction-fetch speed.
+                if (c >= 2 && !warp_wait_spin(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
+                tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mma_bf16_ta_w(tmem + ob, tmem + ns + 8 * k,
-                                      d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_qn, k > 0);
-                };
-                int o1_now = 1;
-                if (c >= 2) {
-                    if (lane == 0)
-                        o1_now = mbar_try_wait(&sm.o_free[c & 1], ((c >> 1) - 1) & 1) ? 1 : 0;
-                    o1_now = __shfl_sync(0xffffffffu, o1_now, 0);
-                }
-                if (o1_now) issue_o1();
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ta_w(tmem + ob, tmem + ns + 8 * k,
+                                  d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_qn, k > 0);
                 if (!warp_wait_spin(&sm.dt_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // S^ += (Delta^T diag(e^{gamma_L - gamma}) / sigma) K   [M=128, N=128, K=64]
@@ -828,10 +822,6 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                                   d_k + (kTile >> 4) + 128 * k, id_s, 1);
                 }
                 mma_commit_w(&sm.s_done);
-                if (!o1_now) {
-                    if (!warp_wait_spin(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
-                    issue_o1();
-                }
                 // O += Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
