@@ -754,10 +754,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: the whole warp runs this loop with
-        // identical values (descriptors stay warp-uniform) and one elected
-        // lane issues each tcgen05 instruction.  U^T for chunk c + 1 is issued
-        // right after chunk c's last MMAs, so it runs while the state warps
-        // prepare chunk c + 1's S0.
+        // identical values (descriptors stay warp-uniform) and one lane,
+        // elected once per group, issues the group's tcgen05 instructions.
+        // U^T for chunk c + 1 is issued right after chunk c's last MMAs, so it
+        // runs while the state warps prepare chunk c + 1's S0.
         {
             constexpr uint32_t id_u = idesc_bf16(128, 64, true, false);
             constexpr uint32_t id_w = idesc_bf16(128, 64, false, true);
@@ -772,9 +772,12 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 ChainStage &st = sm.st[s];
                 const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
                 const uint64_t d_tb = smem_desc(smem_u32(st.tb), 16, 1024);
+if (elect_one_sync()) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_w(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
+                }
+                __syncwarp();
                 return true;
             };
             bool ok = issue_u(0);
@@ -793,10 +796,13 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 if (!warp_wait_spin(&sm.s16_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
+if (elect_one_sync()) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16_ta_w(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
-                mma_commit_w(&sm.d_done);
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ta(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
+                    mma_commit(&sm.d_done);
+                }
+                __syncwarp();
                 // O = S0 Q~^T (A = -S0, negated)         [M=128 dv, N=64, K=128 dk]
                 // into this chunk's output buffer, free once the output warps
                 // have read chunk c - 2's (they have two chunk steps for it, so
@@ -806,28 +812,37 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 // instruction-fetch speed.
                 if (c >= 2 && !warp_wait_spin(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
                 tc_fence_after();
+if (elect_one_sync()) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16_ta_w(tmem + ob, tmem + ns + 8 * k,
-                                  d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_qn, k > 0);
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ta(tmem + ob, tmem + ns + 8 * k,
+                                    d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_qn, k > 0);
+                }
+                __syncwarp();
                 if (!warp_wait_spin(&sm.dt_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // S^ += (Delta^T diag(e^{gamma_L - gamma}) / sigma) K   [M=128, N=128, K=64]
                 // as two N = 64 halves (an N = 128 MMA with A in TMEM runs
                 // several times slower than two N = 64 ones).
+if (elect_one_sync()) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    mma_bf16_ta_w(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
-                    mma_bf16_ta_w(tmem + kColS + 64, tmem + kColDTS + 8 * k,
-                                  d_k + (kTile >> 4) + 128 * k, id_s, 1);
+                    for (int k = 0; k < 4; ++k) {
+                        mma_bf16_ta(tmem + kColS, tmem + kColDTS + 8 * k, d_k + 128 * k, id_s, 1);
+                        mma_bf16_ta(tmem + kColS + 64, tmem + kColDTS + 8 * k,
+                                    d_k + (kTile >> 4) + 128 * k, id_s, 1);
+                    }
+                    mma_commit(&sm.s_done);
                 }
-                mma_commit_w(&sm.s_done);
+                __syncwarp();
                 // O += Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
+if (elect_one_sync()) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ta_w(tmem + ob, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, 1);
-                mma_commit_w(&sm.o_done[c & 1]);
-                mma_commit_w(&sm.empty[s]);
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16_ta(tmem + ob, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, 1);
+                    mma_commit(&sm.o_done[c & 1]);
+                    mma_commit(&sm.empty[s]);
+                }
+                __syncwarp();
                 if (c + 1 < nc) ok = issue_u(c + 1);
             }
             mma_commit_w(&sm.fin);

@@ -88,57 +88,47 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
 
 // Warp-cooperative bounded wait: only lane 0 polls the barrier, sleeping in
 // hardware between polls (a spinning warp would take issue slots from the
-// working warps of its sub-partition); the time limit is checked every 16
-// polls, and the whole warp leaves together.  Returns false on time-out or when *abort is set.
+// working warps of its sub-partition); the time limit and the abort flag are
+// checked after every poll (a short loop keeps the callers' code small), and
+// the whole warp leaves together.  Returns false on time-out or when *abort
+// is set.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           long long limit = 4000000000ll) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        if (!mbar_try_wait(bar, parity)) {
-            const long long t0 = clock64();
-            for (uint32_t i = 1;; ++i) {
-                if (mbar_try_wait_sleep(bar, parity, 100000)) break;
-                if ((i & 15) == 0) {
-                    if (abort && *abort) { ok = 0; break; }
-                    if (clock64() - t0 > limit) {
-                        if (abort) *abort = 1;
-                        ok = 0;
-                        break;
-                    }
-                }
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+        const long long t0 = clock64();
+#pragma unroll 1
+        while (!mbar_try_wait_sleep(bar, parity, 100000)) {
+            if (clock64() - t0 > limit || (abort && *abort)) {
+                if (abort) *abort = 1;
+                ok = 0;
+                break;
             }
         }
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Warp-cooperative bounded wait without the suspend hint (for the warp that
-// issues MMAs, where wake-up latency matters): lane 0 polls, the warp leaves
-// together.
+// Warp-cooperative bounded wait without the suspend hint (for the warps that
+// issue copies and MMAs, where wake-up latency matters): lane 0 polls, checking
+// the clock limit and the abort flag on every poll (a short loop keeps the
+// callers' code small), and the warp leaves together.  Returns false on
+// time-out or when *abort is set.
 __device__ __forceinline__ bool warp_wait_spin(uint64_t *bar, uint32_t parity, volatile int *abort,
                                                long long limit = 4000000000ll) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        if (!mbar_try_wait(bar, parity)) {
-            const long long t0 = clock64();
-            for (uint32_t i = 1;; ++i) {
-                if (mbar_try_wait(bar, parity)) break;
-                if ((i & 255) == 0) {
-                    if (abort && *abort) { ok = 0; break; }
-                    if (clock64() - t0 > limit) {
-                        if (abort) *abort = 1;
-                        ok = 0;
-                        break;
-                    }
-                }
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+        const long long t0 = clock64();
+#pragma unroll 1
+        while (!mbar_try_wait(bar, parity)) {
+            if (clock64() - t0 > limit || (abort && *abort)) {
+                if (abort) *abort = 1;
+                ok = 0;
+                break;
             }
         }
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Single-thread bounded wait for the latency-critical roles (TMA producer,
@@ -339,6 +329,17 @@ __device__ __forceinline__ void mma_bf16_ta_w(uint32_t d_tmem, uint32_t a_tmem, 
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// True in exactly one lane of a converged warp (elect.sync).
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
 }
 
 __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
