@@ -25,12 +25,21 @@ from . import build as _build
 __all__ = [
     "GDNError", "library", "gdn_chunk_prefill", "gdn_decode_step",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
-    "gdn_version", "Problem",
+    "gdn_version", "gdn_chunk_prefill_device_status", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
 GDN_BF16 = 0
 GDN_F32 = 1
+
+# gdn_status codes (include/gdn.h).
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = 1
+GDN_ERR_UNSUPPORTED = 2
+GDN_ERR_MISALIGNED = 3
+GDN_ERR_WORKSPACE = 4
+GDN_ERR_CUDA = 5
+GDN_ERR_TIMEOUT = 6
 _DTYPES = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
 
 
@@ -84,6 +93,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_version.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
+    lib.gdn_chunk_prefill_device_status.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_device_status.argtypes = [P, P]
     _lib = lib
     return lib
 
@@ -193,6 +204,26 @@ def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if rc != 0:
         raise GDNError(rc, "gdn_chunk_prefill")
     return out, final_state
+
+
+def gdn_chunk_prefill_device_status(workspace: Optional[torch.Tensor] = None,
+                                    stream=None, noalloc: bool = False) -> int:
+    """Device-side status of the last bf16 (d = 128) prefill (see
+    ``gdn_chunk_prefill_device_status`` in include/gdn.h): waits for the
+    stream and returns GDN_OK, GDN_ERR_INVALID_ARG (malformed cu_seqlens),
+    GDN_ERR_TIMEOUT (a bounded device wait ran out) or GDN_ERR_CUDA.
+    ``workspace``: the one the call used; by default the workspace this
+    module keeps for the current device, or with ``noalloc`` the built-in
+    scratch of ``gdn_chunk_prefill_noalloc``."""
+    if noalloc:
+        ptr = None
+    else:
+        if workspace is None:
+            workspace = _workspaces.get(torch.cuda.current_device())
+            if workspace is None:
+                raise ValueError("no workspace: no prefill has run through this module")
+        ptr = workspace.data_ptr()
+    return int(library().gdn_chunk_prefill_device_status(ptr, _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

@@ -88,6 +88,24 @@ GDN_API gdn_status gdn_decode_step(const gdn_problem *problem, const void *q, co
     return launch_decode(p, q, k, v, g, beta, state, out, reinterpret_cast<cudaStream_t>(stream));
 }
 
+GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace,
+                                                   gdn_stream_t stream) {
+    const void *ws = workspace ? workspace : gdn::noalloc_scratch();
+    if (!ws) return GDN_ERR_CUDA;
+    if (!gdn::aligned16(ws)) return GDN_ERR_MISALIGNED;
+    int word = 0;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    switch (word) {
+        case gdn::kErrNone: return GDN_OK;
+        case gdn::kErrCuSeqlens: return GDN_ERR_INVALID_ARG;
+        case gdn::kErrTimeout: return GDN_ERR_TIMEOUT;
+    }
+    return GDN_ERR_CUDA;
+}
+
 GDN_API const char *gdn_status_string(gdn_status status) {
     switch (status) {
         case GDN_OK: return "GDN_OK";
@@ -96,6 +114,7 @@ GDN_API const char *gdn_status_string(gdn_status status) {
         case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED: pointer not 16-byte aligned";
         case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA launch or runtime error";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
     }
     return "GDN_ERR_UNKNOWN";
 }

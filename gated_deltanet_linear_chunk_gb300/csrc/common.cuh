@@ -28,6 +28,10 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Error word at offset 0 of the tensor-core prefill's workspace, written by
+// its kernels (reset by the first kernel of every call).
+enum DeviceError : int { kErrNone = 0, kErrCuSeqlens = 1, kErrTimeout = 2 };
+
 // Launch helpers return a gdn_status for the last launch on this thread.
 inline gdn_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -41,6 +45,10 @@ gdn_status launch_prefill_simt(const gdn_problem &p, const void *q, const void *
                                const void *v, const float *g, const float *beta,
                                const int32_t *cu_seqlens, const float *h0, void *out,
                                float *hT, cudaStream_t stream);
+
+// Device address of the no-alloc entry point's built-in scratch on the
+// current device (nullptr if it cannot be looked up).
+void *noalloc_scratch();
 
 size_t prefill_tc_workspace_size(const gdn_problem &p);
 bool prefill_tc_supported(const gdn_problem &p);

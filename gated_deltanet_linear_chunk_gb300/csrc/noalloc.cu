@@ -52,6 +52,10 @@ void *scratch_for_current_device() {
 
 }  // namespace
 
+namespace gdn {
+void *noalloc_scratch() { return scratch_for_current_device(); }
+}  // namespace gdn
+
 extern "C" {
 
 GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_problem *problem, const void *q,

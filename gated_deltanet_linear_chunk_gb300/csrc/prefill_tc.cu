@@ -60,7 +60,6 @@ constexpr int kThreads = 320;   // 10 warps: 0 loads, 1 MMAs, 2-9 epilogue
 constexpr int kMaxSortSeqs = 4096;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum DeviceError : int { kErrNone = 0, kErrCuSeqlens = 1, kErrTimeout = 2 };
 
 // Per (chunk, value head) slot written by the prep kernel.
 constexpr int kSlotWT = 0;                    // W^T  [128 dk][64 tokens], MN-major B image

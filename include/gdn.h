@@ -59,7 +59,9 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 2,  /* head dims, head grouping or dtype not built   */
     GDN_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned       */
     GDN_ERR_WORKSPACE = 4,    /* workspace missing, too small or misaligned    */
-    GDN_ERR_CUDA = 5          /* a CUDA runtime call or launch failed          */
+    GDN_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed          */
+    GDN_ERR_TIMEOUT = 6       /* a bounded wait inside a kernel ran out
+                                 (reported by gdn_chunk_prefill_device_status) */
 } gdn_status;
 
 typedef enum {
@@ -158,6 +160,25 @@ GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_problem *problem,
                                              const float *initial_state,
                                              void *out, float *final_state,
                                              gdn_stream_t stream);
+
+/*
+ * Device-side status of the last bf16 (d = 128) prefill that ran with a given
+ * workspace.  Those kernels keep an error word at the start of their
+ * workspace: they cannot return a status themselves, and they do not fault
+ * on the two conditions they detect.  This call waits for `stream` (it is the
+ * one entry point that synchronises) and reads that word:
+ *   GDN_OK             no condition recorded
+ *   GDN_ERR_INVALID_ARG cu_seqlens was malformed (cu[0] != 0, decreasing, or
+ *                      cu[N] != T); the prefill then wrote no output and no
+ *                      final state
+ *   GDN_ERR_TIMEOUT    a bounded wait inside a kernel ran out (each wait
+ *                      gives up after about two seconds); outputs incomplete
+ *   GDN_ERR_CUDA       the stream reports an error, or the read failed
+ * workspace: problem->workspace of that gdn_chunk_prefill call, or NULL for
+ * the built-in scratch of gdn_chunk_prefill_noalloc on the current device.
+ * Meaningless after calls that need no workspace (fp32 inputs, d = 64).
+ */
+GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace, gdn_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = gdn.gdn_status_string(code)
         assert s.startswith("GDN_")
     assert "UNKNOWN" in gdn.gdn_status_string(99)
