@@ -54,10 +54,11 @@ def prefill_bytes(T, Hk, Hv, d):
     return T * (2 * Hk * d * 2 + Hv * d * 2 + Hv * d * 2 + 2 * Hv * 4)
 
 
-def decode_bytes(N, Hk, Hv, d):
-    """Compulsory HBM bytes of one decode step: the fp32 state read and
-    written, q/k/v read and out written (bf16), g and beta read (fp32)."""
-    return N * (2 * Hv * d * d * 4 + 2 * Hk * d * 2 + 2 * Hv * d * 2 + 2 * Hv * 4)
+def decode_bytes(N, Hk, Hv, d, state_bytes=4):
+    """Compulsory HBM bytes of one decode step: the state read and written
+    (fp32, or 2 bytes per element when stored in 16 bits), q/k/v read and out
+    written (bf16), g and beta read (fp32)."""
+    return N * (2 * Hv * d * d * state_bytes + 2 * Hk * d * 2 + 2 * Hv * d * 2 + 2 * Hv * 4)
 
 
 class ClockSampler:
@@ -304,6 +305,21 @@ def run_ours(args, rank, world, local):
     dec_us = 1e3 * d0.elapsed_time(d1) / args.decode_steps
     dbytes = decode_bytes(D["N"], D["Hk"], D["Hv"], D["d"])
     dec_gbs = dbytes / (dec_us / 1e6) / 1e9
+    # The same steps with the state stored in fp16 (the pages' fork).
+    state16 = inputs.decode_state(D["N"], D["Hv"], D["d"], D["d"]).to(torch.float16).to(dev)
+    del state
+    for s in range(3):
+        gdn.gdn_decode_step_half_state(*dsteps[s % len(dsteps)], state16, out=dout)
+    torch.cuda.synchronize()
+    barrier()
+    d0.record(stream)
+    for s in range(args.decode_steps):
+        gdn.gdn_decode_step_half_state(*dsteps[s], state16, out=dout)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec16_us = 1e3 * d0.elapsed_time(d1) / args.decode_steps
+    dbytes16 = decode_bytes(D["N"], D["Hk"], D["Hv"], D["d"], state_bytes=2)
+    dec16_gbs = dbytes16 / (dec16_us / 1e6) / 1e9
 
     clk = clocks.summary()
     line = {
@@ -328,6 +344,11 @@ def run_ours(args, rank, world, local):
                    "bytes_per_step": dbytes, "achieved_gbs": dec_gbs,
                    "peak_gbs": peaks["hbm_gbs"], "frac": dec_gbs / peaks["hbm_gbs"],
                    "frac_of_8tbs": dec_gbs / 8000.0, "peak_kind": peak_kind},
+        "decode_f16_state": {"workload": "as decode, state stored in fp16 (fp32 math)",
+                             "us_per_step": dec16_us, "steps": args.decode_steps,
+                             "bytes_per_step": dbytes16, "achieved_gbs": dec16_gbs,
+                             "peak_gbs": peaks["hbm_gbs"], "frac": dec16_gbs / peaks["hbm_gbs"],
+                             "speedup_vs_fp32_state": dec_us / dec16_us},
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and not args.no_cpu_baseline:

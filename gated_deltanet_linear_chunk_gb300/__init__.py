@@ -25,12 +25,13 @@ from . import build as _build
 __all__ = [
     "GDNError", "library", "gdn_chunk_prefill", "gdn_decode_step",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
-    "gdn_version", "gdn_chunk_prefill_device_status", "Problem",
+    "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
 GDN_BF16 = 0
 GDN_F32 = 1
+GDN_F16 = 2  # state storage of gdn_decode_step_half_state only
 
 # gdn_status codes (include/gdn.h).
 GDN_OK = 0
@@ -93,6 +94,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_version.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
+    lib.gdn_decode_step_half_state.restype = ctypes.c_int
+    lib.gdn_decode_step_half_state.argtypes = [PP, P, P, P, P, P, P, ctypes.c_int32, P, P]
     lib.gdn_chunk_prefill_device_status.restype = ctypes.c_int
     lib.gdn_chunk_prefill_device_status.argtypes = [P, P]
     _lib = lib
@@ -292,6 +295,39 @@ def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                    _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
     if rc != 0:
         raise GDNError(rc, "gdn_decode_step")
+    return out
+
+
+_STATE_DTYPES = {torch.float16: GDN_F16, torch.bfloat16: GDN_BF16}
+
+
+def gdn_decode_step_half_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               g: torch.Tensor, beta: torch.Tensor, state: torch.Tensor,
+                               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """``gdn_decode_step`` with a 16-bit state (fp16 or bf16, updated in place;
+    see ``gdn_decode_step_half_state`` in include/gdn.h).  Returns out."""
+    N, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported q/k/v dtype {dt}")
+    if state.dtype not in _STATE_DTYPES:
+        raise TypeError(f"state must be float16 or bfloat16, got {state.dtype}")
+    _check(q, "q", dt, (N, Hk, dk))
+    _check(k, "k", dt, (N, Hk, dk))
+    _check(v, "v", dt, (N, Hv, dv))
+    _check(g, "g", torch.float32, (N, Hv))
+    _check(beta, "beta", torch.float32, (N, Hv))
+    _check(state, "state", state.dtype, (N, Hv, dv, dk))
+    if out is None:
+        out = torch.empty((N, Hv, dv), dtype=dt, device=q.device)
+    _check(out, "out", dt, (N, Hv, dv))
+    p = make_problem(N, N, Hk, Hv, dk, dv, dt)
+    rc = library().gdn_decode_step_half_state(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+        _STATE_DTYPES[state.dtype], _ptr(out), _stream(stream))
+    if rc != 0:
+        raise GDNError(rc, "gdn_decode_step_half_state")
     return out
 
 

@@ -85,7 +85,26 @@ GDN_API gdn_status gdn_decode_step(const gdn_problem *problem, const void *q, co
     if (!q || !k || !v || !g || !beta || !state || !out) return GDN_ERR_INVALID_ARG;
     if (any_misaligned({q, k, v, g, beta, state, out})) return GDN_ERR_MISALIGNED;
     if (out == q || out == k || out == v) return GDN_ERR_INVALID_ARG;
-    return launch_decode(p, q, k, v, g, beta, state, out, reinterpret_cast<cudaStream_t>(stream));
+    return launch_decode(p, q, k, v, g, beta, state, GDN_F32, out,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+GDN_API gdn_status gdn_decode_step_half_state(const gdn_problem *problem, const void *q,
+                                              const void *k, const void *v, const float *g,
+                                              const float *beta, void *state,
+                                              int32_t state_dtype, void *out,
+                                              gdn_stream_t stream) {
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    const gdn_problem &p = *problem;
+    if (p.total_tokens != p.num_seqs) return GDN_ERR_INVALID_ARG;
+    if (state_dtype != GDN_F16 && state_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (p.num_seqs == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out) return GDN_ERR_INVALID_ARG;
+    if (any_misaligned({q, k, v, g, beta, state, out})) return GDN_ERR_MISALIGNED;
+    if (out == q || out == k || out == v) return GDN_ERR_INVALID_ARG;
+    return launch_decode(p, q, k, v, g, beta, state, state_dtype, out,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace,

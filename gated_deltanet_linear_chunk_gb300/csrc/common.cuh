@@ -38,9 +38,10 @@ inline gdn_status launch_status() {
 }
 
 // Kernel launchers implemented in the .cu files.
+// state_dtype: GDN_F32, GDN_F16 or GDN_BF16 (storage of the state).
 gdn_status launch_decode(const gdn_problem &p, const void *q, const void *k, const void *v,
-                         const float *g, const float *beta, float *state, void *out,
-                         cudaStream_t stream);
+                         const float *g, const float *beta, void *state, int state_dtype,
+                         void *out, cudaStream_t stream);
 gdn_status launch_prefill_simt(const gdn_problem &p, const void *q, const void *k,
                                const void *v, const float *g, const float *beta,
                                const int32_t *cu_seqlens, const float *h0, void *out,

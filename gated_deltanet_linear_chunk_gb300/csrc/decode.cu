@@ -11,47 +11,99 @@
 //   S <- a S + delta k^T                    (in place)
 //   o = S_new q = a y + (k . q) delta
 //
-// The step is a read-modify-write of the fp32 state, so it is bound by HBM
-// bandwidth: 2 * dv * dk * 4 bytes per (n, h) against ~6 dv dk flops.  Each
-// warp owns whole state rows: lane l holds dk/32 consecutive elements of a
-// row (16-byte loads for dk = 128), the two dot products are warp-shuffle
-// reductions, and ROWS rows are loaded before any is reduced so that every
-// lane keeps ROWS x 16 bytes in flight.  Loads and stores carry the
-// streaming (evict-first) hint: the state is touched once per step.
+// The state may also be stored in 16 bits (fp16 or bf16; the same page
+// reports the fork keeping it in fp16 at unchanged perplexity): it is then
+// read, updated in fp32 and stored rounded to nearest even.
+//
+// The step is a read-modify-write of the state, so it is bound by HBM
+// bandwidth: 2 * dv * dk * sizeof(state) bytes per (n, h) against ~6 dv dk
+// flops.  Each warp owns whole state rows: lane l holds dk/32 consecutive
+// elements of a row (16-byte loads for an fp32 state with dk = 128, 8-byte
+// loads for a 16-bit one), the two dot products are warp-shuffle reductions,
+// and kDecodeRows rows are loaded before any is reduced so that every lane
+// keeps several loads in flight.  Loads and stores carry the streaming
+// (evict-first) hint: the state is touched once per step.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeRows = 8;  // rows per warp per iteration
+constexpr int kDecodeRows = 8;  // rows per warp per iteration (also best for 16-bit states)
 
-template <int EPT> struct Vec;
-template <> struct Vec<4> {
-    using T = float4;
-    __device__ static void load(const float *p, float (&r)[4]) {
-        float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
+// EPT consecutive state elements of one lane: loaded as raw words
+// (streaming loads; a 16-bit state stays packed in registers until used),
+// unpacked to fp32 where needed, and stored from fp32 (streaming stores,
+// round to nearest even for 16 bits).
+template <typename TS, int EPT> struct StateIO;
+template <> struct StateIO<float, 4> {
+    using Raw = float4;
+    __device__ static Raw load(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
+    __device__ static void unpack(const Raw &t, float (&r)[4]) {
         r[0] = t.x; r[1] = t.y; r[2] = t.z; r[3] = t.w;
     }
     __device__ static void store(float *p, const float (&r)[4]) {
         __stcs(reinterpret_cast<float4 *>(p), make_float4(r[0], r[1], r[2], r[3]));
     }
 };
-template <> struct Vec<2> {
-    __device__ static void load(const float *p, float (&r)[2]) {
-        float2 t = __ldcs(reinterpret_cast<const float2 *>(p));
-        r[0] = t.x; r[1] = t.y;
-    }
+template <> struct StateIO<float, 2> {
+    using Raw = float2;
+    __device__ static Raw load(const float *p) { return __ldcs(reinterpret_cast<const float2 *>(p)); }
+    __device__ static void unpack(const Raw &t, float (&r)[2]) { r[0] = t.x; r[1] = t.y; }
     __device__ static void store(float *p, const float (&r)[2]) {
         __stcs(reinterpret_cast<float2 *>(p), make_float2(r[0], r[1]));
     }
 };
 
-template <typename TIn, int DK>
+// Two 16-bit values in one word, to and from fp32 (round to nearest even).
+__device__ __forceinline__ float2 unpack2(uint32_t w, __half) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+__device__ __forceinline__ float2 unpack2(uint32_t w, __nv_bfloat16) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <typename TS> struct StateIO<TS, 4> {
+    using Raw = uint2;
+    __device__ static Raw load(const TS *p) { return __ldcs(reinterpret_cast<const uint2 *>(p)); }
+    __device__ static void unpack(const Raw &t, float (&r)[4]) {
+        const float2 a = unpack2(t.x, TS()), b = unpack2(t.y, TS());
+        r[0] = a.x; r[1] = a.y; r[2] = b.x; r[3] = b.y;
+    }
+    __device__ static void store(TS *p, const float (&r)[4]) {
+        __stcs(reinterpret_cast<uint2 *>(p),
+               make_uint2(pack2(r[0], r[1], TS()), pack2(r[2], r[3], TS())));
+    }
+};
+template <typename TS> struct StateIO<TS, 2> {
+    using Raw = unsigned int;
+    __device__ static Raw load(const TS *p) {
+        return __ldcs(reinterpret_cast<const unsigned int *>(p));
+    }
+    __device__ static void unpack(const Raw &t, float (&r)[2]) {
+        const float2 a = unpack2(t, TS());
+        r[0] = a.x; r[1] = a.y;
+    }
+    __device__ static void store(TS *p, const float (&r)[2]) {
+        __stcs(reinterpret_cast<unsigned int *>(p), pack2(r[0], r[1], TS()));
+    }
+};
+
+template <typename TIn, typename TS, int DK>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 gdn_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                   const TIn *__restrict__ v, const float *__restrict__ g,
-                  const float *__restrict__ beta, float *__restrict__ state,
+                  const float *__restrict__ beta, TS *__restrict__ state,
                   TIn *__restrict__ out, int Hk, int Hv, int DV) {
     constexpr int EPT = DK / 32;
     const int nh = blockIdx.x;            // n * Hv + h
@@ -73,23 +125,26 @@ gdn_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
 
     const float a = expf(g[nh]);
     const float b = beta[nh];
-    float *S = state + (size_t)nh * DV * DK;
+    TS *S = state + (size_t)nh * DV * DK;
     const TIn *vrow = v + (size_t)nh * DV;
     TIn *orow = out + (size_t)nh * DV;
 
     for (int r0 = warp * kDecodeRows; r0 < DV; r0 += kDecodeWarps * kDecodeRows) {
-        float s[kDecodeRows][EPT];
+        using IO = StateIO<TS, EPT>;
+        typename IO::Raw raw[kDecodeRows];
 #pragma unroll
-        for (int r = 0; r < kDecodeRows; ++r) Vec<EPT>::load(S + (size_t)(r0 + r) * DK + lane * EPT, s[r]);
+        for (int r = 0; r < kDecodeRows; ++r) raw[r] = IO::load(S + (size_t)(r0 + r) * DK + lane * EPT);
         float vr = lane < kDecodeRows ? to_f32(vrow[r0 + lane]) : 0.f;
         float x[kDecodeRows], y[kDecodeRows];
 #pragma unroll
         for (int r = 0; r < kDecodeRows; ++r) {
+            float sv[EPT];
+            IO::unpack(raw[r], sv);
             float xs = 0.f, ys = 0.f;
 #pragma unroll
             for (int e = 0; e < EPT; ++e) {
-                xs = fmaf(s[r][e], kr[e], xs);
-                ys = fmaf(s[r][e], qr[e], ys);
+                xs = fmaf(sv[e], kr[e], xs);
+                ys = fmaf(sv[e], qr[e], ys);
             }
             x[r] = xs;
             y[r] = ys;
@@ -107,9 +162,11 @@ gdn_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
         for (int r = 0; r < kDecodeRows; ++r) {
             const float vv = __shfl_sync(0xffffffffu, vr, r);
             const float delta = b * (vv - a * x[r]);
+            float sv[EPT];
+            IO::unpack(raw[r], sv);
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) s[r][e] = fmaf(a, s[r][e], delta * kr[e]);
-            Vec<EPT>::store(S + (size_t)(r0 + r) * DK + lane * EPT, s[r]);
+            for (int e = 0; e < EPT; ++e) sv[e] = fmaf(a, sv[e], delta * kr[e]);
+            IO::store(S + (size_t)(r0 + r) * DK + lane * EPT, sv);
             const float o = fmaf(a, y[r], kq * delta);
             if (lane == r) o_mine = o;
         }
@@ -117,29 +174,43 @@ gdn_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     }
 }
 
-template <typename TIn, int DK>
+template <typename TIn, typename TS, int DK>
 gdn_status launch_typed(const gdn_problem &p, const void *q, const void *k, const void *v,
-                        const float *g, const float *beta, float *state, void *out,
+                        const float *g, const float *beta, void *state, void *out,
                         cudaStream_t stream) {
     const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_v_heads;
-    gdn_decode_kernel<TIn, DK><<<blocks, kDecodeWarps * 32, 0, stream>>>(
+    gdn_decode_kernel<TIn, TS, DK><<<blocks, kDecodeWarps * 32, 0, stream>>>(
         static_cast<const TIn *>(q), static_cast<const TIn *>(k), static_cast<const TIn *>(v), g,
-        beta, state, static_cast<TIn *>(out), p.num_k_heads, p.num_v_heads, p.head_dim_v);
+        beta, static_cast<TS *>(state), static_cast<TIn *>(out), p.num_k_heads, p.num_v_heads,
+        p.head_dim_v);
     return launch_status();
+}
+
+template <typename TS>
+gdn_status launch_state(const gdn_problem &p, const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, void *state, void *out,
+                        cudaStream_t stream) {
+    const bool bf = p.qkv_dtype == GDN_BF16;
+    if (p.head_dim_k == 128)
+        return bf ? launch_typed<__nv_bfloat16, TS, 128>(p, q, k, v, g, beta, state, out, stream)
+                  : launch_typed<float, TS, 128>(p, q, k, v, g, beta, state, out, stream);
+    return bf ? launch_typed<__nv_bfloat16, TS, 64>(p, q, k, v, g, beta, state, out, stream)
+              : launch_typed<float, TS, 64>(p, q, k, v, g, beta, state, out, stream);
 }
 
 }  // namespace
 
 gdn_status launch_decode(const gdn_problem &p, const void *q, const void *k, const void *v,
-                         const float *g, const float *beta, float *state, void *out,
-                         cudaStream_t stream) {
+                         const float *g, const float *beta, void *state, int state_dtype,
+                         void *out, cudaStream_t stream) {
     if (p.num_seqs == 0) return GDN_OK;
-    const bool bf = p.qkv_dtype == GDN_BF16;
-    if (p.head_dim_k == 128)
-        return bf ? launch_typed<__nv_bfloat16, 128>(p, q, k, v, g, beta, state, out, stream)
-                  : launch_typed<float, 128>(p, q, k, v, g, beta, state, out, stream);
-    return bf ? launch_typed<__nv_bfloat16, 64>(p, q, k, v, g, beta, state, out, stream)
-              : launch_typed<float, 64>(p, q, k, v, g, beta, state, out, stream);
+    switch (state_dtype) {
+        case GDN_F32: return launch_state<float>(p, q, k, v, g, beta, state, out, stream);
+        case GDN_F16: return launch_state<__half>(p, q, k, v, g, beta, state, out, stream);
+        case GDN_BF16:
+            return launch_state<__nv_bfloat16>(p, q, k, v, g, beta, state, out, stream);
+    }
+    return GDN_ERR_UNSUPPORTED;
 }
 
 }  // namespace gdn

@@ -304,6 +304,21 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_3d(sm.kq + 2 * kTile, &tm_k, 64, hk, tok0, &sm.tma_bar);
         tma_load_3d(sm.kq + 3 * kTile, &tm_q, 64, hk, tok0, &sm.tma_bar);
     }
+    // gamma, b and the decay factors of the first round of value heads,
+    // while the K and Q tiles are in flight.
+    auto head_gamma = [&](int j0, int nh) {
+        if (warp >= 1 && warp <= nh) {
+            const int j = warp - 1, h = hk * G + j0 + j;
+            chunk_gamma(g, tok0, L, Hv, h, sm.gam[j], sm.beta[j], beta, sm.eg[j], sm.dec[j]);
+            float *slot_f = reinterpret_cast<float *>(slots + ((size_t)ch * Hv + h) * kSlotBytes);
+            slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[j][2 * lane];
+            slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
+            slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
+            slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
+            if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[j][C - 1];
+        }
+    };
+    head_gamma(0, min(kPrepHeads, G));
     bool bad = !warp_wait(&sm.tma_bar, 0, nullptr);
     uint32_t mph = 0;
     if (tid == 0 && !bad) {
@@ -320,16 +335,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int j0 = 0; j0 < G; j0 += kPrepHeads) {
         const int nh = min(kPrepHeads, G - j0);
-        if (warp >= 1 && warp <= nh) {
-            const int j = warp - 1, h = hk * G + j0 + j;
-            chunk_gamma(g, tok0, L, Hv, h, sm.gam[j], sm.beta[j], beta, sm.eg[j], sm.dec[j]);
-            float *slot_f = reinterpret_cast<float *>(slots + ((size_t)ch * Hv + h) * kSlotBytes);
-            slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[j][2 * lane];
-            slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
-            slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
-            slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
-            if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[j][C - 1];
-        }
+        if (j0 > 0) head_gamma(j0, nh);
         if (j0 == 0) {
             bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
             mph ^= 1;
@@ -434,6 +440,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // value head of the round: the same swizzled image as Q's tiles,
             // scaled row by row.
             const int w = tid < 64 ? tid : tid - 192;  // 0 .. 127
+#pragma unroll 8
             for (int idx = w; idx < nh * 2 * C * 8; idx += 128) {
                 const int j = idx / (2 * C * 8), a = (idx / (C * 8)) & 1;
                 const int r = (idx >> 3) & (C - 1), cc = idx & 7;

@@ -66,7 +66,9 @@ typedef enum {
 
 typedef enum {
     GDN_BF16 = 0,  /* q, k, v and out are bf16 (tensor-core path)   */
-    GDN_F32 = 1    /* q, k, v and out are fp32 (FFMA check path)    */
+    GDN_F32 = 1,   /* q, k, v and out are fp32 (FFMA check path)    */
+    GDN_F16 = 2    /* only as the state storage of
+                      gdn_decode_step_half_state                    */
 } gdn_dtype;
 
 /*
@@ -133,6 +135,24 @@ GDN_API gdn_status gdn_decode_step(const gdn_problem *problem,
                                    const float *g, const float *beta,
                                    float *state, void *out,
                                    gdn_stream_t stream);
+
+/*
+ * gdn_decode_step with the state stored in 16 bits: each step reads the
+ * stored state, computes in fp32 exactly as gdn_decode_step does and stores
+ * the updated state rounded to nearest even, halving the state traffic that
+ * bounds the step.  (Page "reactapp.top", section "Exploiter l'architecture
+ * hybride": the forked server keeps this state in fp16 instead of fp32, at
+ * perplexity unchanged to three decimals.)
+ *   state        [N, Hv, dv, dk] in state_dtype, read and written in place
+ *   state_dtype  GDN_F16 (the pages' choice) or GDN_BF16; other values give
+ *                GDN_ERR_UNSUPPORTED
+ * Everything else as gdn_decode_step.
+ */
+GDN_API gdn_status gdn_decode_step_half_state(const gdn_problem *problem,
+                                              const void *q, const void *k, const void *v,
+                                              const float *g, const float *beta,
+                                              void *state, int32_t state_dtype, void *out,
+                                              gdn_stream_t stream);
 
 /*
  * gdn_chunk_prefill without caller-provided scratch.  (The paper has no

@@ -116,6 +116,22 @@ def test_decode_argument_errors(lib):
     assert decode(lib, prob(N=0, T=0)) == OK
 
 
+def half_decode(lib, p, sdt, s=A + 20480, out=A + 24576):
+    return lib.gdn_decode_step_half_state(ctypes.byref(p) if p is not None else None, A,
+                                          A + 4096, A + 8192, A + 12288, A + 16384, s, sdt,
+                                          out, None)
+
+
+def test_half_state_decode_argument_errors(lib):
+    assert half_decode(lib, None, gdn.GDN_F16) == INVALID
+    assert half_decode(lib, prob(N=4, T=4), gdn.GDN_F32) == UNSUPPORTED
+    assert half_decode(lib, prob(N=4, T=4), 7) == UNSUPPORTED
+    assert half_decode(lib, prob(N=4, T=5), gdn.GDN_F16) == INVALID
+    assert half_decode(lib, prob(N=4, T=4), gdn.GDN_BF16, s=A + 2) == MISALIGNED
+    assert half_decode(lib, prob(N=4, T=4, dtype=gdn.GDN_F16), gdn.GDN_F16) == UNSUPPORTED
+    assert half_decode(lib, prob(N=0, T=0), gdn.GDN_F16) == OK
+
+
 def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
