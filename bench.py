@@ -54,6 +54,22 @@ def prefill_bytes(T, Hk, Hv, d):
     return T * (2 * Hk * d * 2 + Hv * d * 2 + Hv * d * 2 + 2 * Hv * 4)
 
 
+def verify_bytes(N, K, Hk, Hv, d, state_bytes):
+    """Compulsory HBM bytes of one verify call: the state read once, K state
+    slots written, K tokens of q/k/v read and out written (bf16), g and beta."""
+    return N * (Hv * d * d * state_bytes * (1 + K) +
+                K * (2 * Hk * d * 2 + 2 * Hv * d * 2 + 2 * Hv * 4))
+
+
+def verify_inputs(N, K, Hk, Hv, d):
+    """K consecutive decode-step inputs per sequence, stacked [N, K, ...]."""
+    import torch
+    from gated_deltanet_linear_chunk_gb300 import inputs
+    xs = [inputs.decode_step_inputs(j, N, Hk, Hv, d, d) for j in range(K)]
+    return [torch.stack([getattr(x, f) for x in xs], dim=1).contiguous()
+            for f in ("q", "k", "v", "g", "beta")]
+
+
 def decode_bytes(N, Hk, Hv, d, state_bytes=4):
     """Compulsory HBM bytes of one decode step: the state read and written
     (fp32, or 2 bytes per element when stored in 16 bits), q/k/v read and out
@@ -320,6 +336,32 @@ def run_ours(args, rank, world, local):
     dec16_us = 1e3 * d0.elapsed_time(d1) / args.decode_steps
     dbytes16 = decode_bytes(D["N"], D["Hk"], D["Hv"], D["d"], state_bytes=2)
     dec16_gbs = dbytes16 / (dec16_us / 1e6) / 1e9
+    del state16
+
+    # ---------------- verify step (8 tokens per sequence, a slot per token) --------
+    K = 8
+    vx = [t.to(dev) for t in verify_inputs(D["N"], K, D["Hk"], D["Hv"], D["d"])]
+    vout = torch.empty((D["N"], K, D["Hv"], D["d"]), dtype=torch.bfloat16, device=dev)
+    verify = {}
+    for name, sdt, sb in (("fp32_state", torch.float32, 4), ("fp16_state", torch.float16, 2)):
+        vstate = inputs.decode_state(D["N"], D["Hv"], D["d"], D["d"]).to(sdt).to(dev)
+        vslots = torch.empty((D["N"], K, D["Hv"], D["d"], D["d"]), dtype=sdt, device=dev)
+        for _ in range(3):
+            gdn.gdn_verify_step(*vx, vstate, slots=vslots, out=vout)
+        torch.cuda.synchronize()
+        barrier()
+        reps = 20
+        d0.record(stream)
+        for _ in range(reps):
+            gdn.gdn_verify_step(*vx, vstate, slots=vslots, out=vout)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        v_us = 1e3 * d0.elapsed_time(d1) / reps
+        vbytes = verify_bytes(D["N"], K, D["Hk"], D["Hv"], D["d"], sb)
+        verify[name] = {"us_per_call": v_us, "tokens_per_s": D["N"] * K / (v_us / 1e6),
+                        "bytes_per_call": vbytes, "achieved_gbs": vbytes / (v_us / 1e6) / 1e9,
+                        "frac": vbytes / (v_us / 1e6) / 1e9 / peaks["hbm_gbs"]}
+        del vstate, vslots
 
     clk = clocks.summary()
     line = {
@@ -349,6 +391,8 @@ def run_ours(args, rank, world, local):
                              "bytes_per_step": dbytes16, "achieved_gbs": dec16_gbs,
                              "peak_gbs": peaks["hbm_gbs"], "frac": dec16_gbs / peaks["hbm_gbs"],
                              "speedup_vs_fp32_state": dec_us / dec16_us},
+        "verify": {"workload": "64 sequences x 8 tokens from one state, a state slot per "
+                               "token, 16/48 heads, d=128, bf16 q/k/v", **verify},
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -25,7 +25,8 @@ from . import build as _build
 __all__ = [
     "GDNError", "library", "gdn_chunk_prefill", "gdn_decode_step",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
-    "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state", "Problem",
+    "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
+    "gdn_verify_step", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
@@ -96,6 +97,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_version.argtypes = []
     lib.gdn_decode_step_half_state.restype = ctypes.c_int
     lib.gdn_decode_step_half_state.argtypes = [PP, P, P, P, P, P, P, ctypes.c_int32, P, P]
+    lib.gdn_verify_step.restype = ctypes.c_int
+    lib.gdn_verify_step.argtypes = [PP, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int32, P, P, P]
     lib.gdn_chunk_prefill_device_status.restype = ctypes.c_int
     lib.gdn_chunk_prefill_device_status.argtypes = [P, P]
     _lib = lib
@@ -329,6 +332,46 @@ def gdn_decode_step_half_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     if rc != 0:
         raise GDNError(rc, "gdn_decode_step_half_state")
     return out
+
+
+_ALL_STATE_DTYPES = {torch.float32: GDN_F32, torch.float16: GDN_F16, torch.bfloat16: GDN_BF16}
+
+
+def gdn_verify_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                    beta: torch.Tensor, state: torch.Tensor,
+                    slots: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Verify step of speculative decoding (see ``gdn_verify_step`` in
+    include/gdn.h).  q, k: [N, K, Hk, dk]; v: [N, K, Hv, dv]; g, beta:
+    [N, K, Hv] fp32 (K = 1 .. 8 tokens per sequence); state [N, Hv, dv, dk]
+    in fp32, fp16 or bf16 (read only).  Returns (out [N, K, Hv, dv], slots
+    [N, K, Hv, dv, dk] in the state's dtype: the state after each token)."""
+    N, K, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported q/k/v dtype {dt}")
+    if state.dtype not in _ALL_STATE_DTYPES:
+        raise TypeError(f"unsupported state dtype {state.dtype}")
+    _check(q, "q", dt, (N, K, Hk, dk))
+    _check(k, "k", dt, (N, K, Hk, dk))
+    _check(v, "v", dt, (N, K, Hv, dv))
+    _check(g, "g", torch.float32, (N, K, Hv))
+    _check(beta, "beta", torch.float32, (N, K, Hv))
+    _check(state, "state", state.dtype, (N, Hv, dv, dk))
+    if slots is None:
+        slots = torch.empty((N, K, Hv, dv, dk), dtype=state.dtype, device=q.device)
+    _check(slots, "slots", state.dtype, (N, K, Hv, dv, dk))
+    if out is None:
+        out = torch.empty((N, K, Hv, dv), dtype=dt, device=q.device)
+    _check(out, "out", dt, (N, K, Hv, dv))
+    p = make_problem(N, N * K, Hk, Hv, dk, dv, dt)
+    rc = library().gdn_verify_step(ctypes.byref(p), K, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(state), _ALL_STATE_DTYPES[state.dtype],
+                                   _ptr(slots), _ptr(out), _stream(stream))
+    if rc != 0:
+        raise GDNError(rc, "gdn_verify_step")
+    return out, slots
 
 
 def prefill_launches(Hv: int, d: int, dtype, total_tokens: int = 1) -> int:

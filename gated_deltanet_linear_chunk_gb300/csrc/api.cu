@@ -107,6 +107,25 @@ GDN_API gdn_status gdn_decode_step_half_state(const gdn_problem *problem, const 
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+GDN_API gdn_status gdn_verify_step(const gdn_problem *problem, int32_t num_tokens,
+                                   const void *q, const void *k, const void *v, const float *g,
+                                   const float *beta, const void *state, int32_t state_dtype,
+                                   void *slots, void *out, gdn_stream_t stream) {
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    const gdn_problem &p = *problem;
+    if (num_tokens < 1 || num_tokens > 8) return GDN_ERR_INVALID_ARG;
+    if (p.total_tokens != (int64_t)p.num_seqs * num_tokens) return GDN_ERR_INVALID_ARG;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_F16 && state_dtype != GDN_BF16)
+        return GDN_ERR_UNSUPPORTED;
+    if (p.num_seqs == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state || !slots || !out) return GDN_ERR_INVALID_ARG;
+    if (any_misaligned({q, k, v, g, beta, state, slots, out})) return GDN_ERR_MISALIGNED;
+    if (out == q || out == k || out == v || slots == state) return GDN_ERR_INVALID_ARG;
+    return launch_verify(p, num_tokens, q, k, v, g, beta, state, state_dtype, slots, out,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace,
                                                    gdn_stream_t stream) {
     const void *ws = workspace ? workspace : gdn::noalloc_scratch();

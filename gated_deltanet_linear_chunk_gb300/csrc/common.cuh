@@ -38,6 +38,11 @@ inline gdn_status launch_status() {
 }
 
 // Kernel launchers implemented in the .cu files.
+// Verify step: num_tokens (1..8) tokens per sequence from `state`, the state
+// after token t in slot t (storage state_dtype for both).
+gdn_status launch_verify(const gdn_problem &p, int num_tokens, const void *q, const void *k,
+                         const void *v, const float *g, const float *beta, const void *state,
+                         int state_dtype, void *slots, void *out, cudaStream_t stream);
 // state_dtype: GDN_F32, GDN_F16 or GDN_BF16 (storage of the state).
 gdn_status launch_decode(const gdn_problem &p, const void *q, const void *k, const void *v,
                          const float *g, const float *beta, void *state, int state_dtype,

@@ -174,6 +174,139 @@ gdn_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     }
 }
 
+// Verify step of speculative decoding: K <= kMaxVerify consecutive tokens of
+// each sequence from one stored state, every position's output, and the
+// state after every position in its own slot (the caller keeps the slot of
+// the last accepted token).  Page "reactapp.top": the target model checks a
+// block of draft tokens in one pass and keeps the correct prefix (section
+// "DFlash2 : rediger sept tokens en une seule passe"), with eight
+// speculative state slots per request (section "Pourquoi la limite est de
+// 131 072 et non de 136 429").  A warp's rows stay in fp32 registers across
+// the K tokens; each slot is written in the storage type.
+constexpr int kMaxVerify = 8;
+
+template <typename TIn, typename TS, int DK>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+gdn_verify_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
+                  const TIn *__restrict__ v, const float *__restrict__ g,
+                  const float *__restrict__ beta, const TS *__restrict__ state,
+                  TS *__restrict__ slots, TIn *__restrict__ out, int Hk, int Hv, int DV, int K) {
+    constexpr int EPT = DK / 32;
+    __shared__ float sk[kMaxVerify][DK], sq[kMaxVerify][DK];
+    __shared__ float sa[kMaxVerify], sb[kMaxVerify], skq[kMaxVerify];
+    const int nh = blockIdx.x;  // n * Hv + h
+    const int n = nh / Hv, h = nh - n * Hv;
+    const int hk = h / (Hv / Hk);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t t0 = (size_t)n * K;  // first token of the sequence
+
+    for (int i = threadIdx.x; i < K * DK; i += kDecodeWarps * 32) {
+        const int j = i / DK, e = i - j * DK;
+        const size_t off = ((t0 + j) * Hk + hk) * DK + e;
+        sk[j][e] = to_f32(k[off]);
+        sq[j][e] = to_f32(q[off]);
+    }
+    __syncthreads();
+    for (int j = warp; j < K; j += kDecodeWarps) {
+        float kq = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) kq = fmaf(sk[j][lane * EPT + e], sq[j][lane * EPT + e], kq);
+        kq = warp_sum(kq);
+        if (lane == 0) {
+            skq[j] = kq;
+            sa[j] = expf(g[(t0 + j) * Hv + h]);
+            sb[j] = beta[(t0 + j) * Hv + h];
+        }
+    }
+    __syncthreads();
+
+    using IO = StateIO<TS, EPT>;
+    const TS *S = state + (size_t)nh * DV * DK;
+    for (int r0 = warp * kDecodeRows; r0 < DV; r0 += kDecodeWarps * kDecodeRows) {
+        float s[kDecodeRows][EPT];
+        {
+            typename IO::Raw raw[kDecodeRows];
+#pragma unroll
+            for (int r = 0; r < kDecodeRows; ++r)
+                raw[r] = IO::load(S + (size_t)(r0 + r) * DK + lane * EPT);
+#pragma unroll
+            for (int r = 0; r < kDecodeRows; ++r) IO::unpack(raw[r], s[r]);
+        }
+        for (int j = 0; j < K; ++j) {
+            float kr[EPT], qr[EPT];
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                kr[e] = sk[j][lane * EPT + e];
+                qr[e] = sq[j][lane * EPT + e];
+            }
+            const size_t tok = t0 + j;
+            const float vr = lane < kDecodeRows ? to_f32(v[(tok * Hv + h) * DV + r0 + lane]) : 0.f;
+            float x[kDecodeRows], y[kDecodeRows];
+#pragma unroll
+            for (int r = 0; r < kDecodeRows; ++r) {
+                float xs = 0.f, ys = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    xs = fmaf(s[r][e], kr[e], xs);
+                    ys = fmaf(s[r][e], qr[e], ys);
+                }
+                x[r] = xs;
+                y[r] = ys;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                for (int r = 0; r < kDecodeRows; ++r) {
+                    x[r] += __shfl_xor_sync(0xffffffffu, x[r], o);
+                    y[r] += __shfl_xor_sync(0xffffffffu, y[r], o);
+                }
+            }
+            const float a = sa[j], b = sb[j], kq = skq[j];
+            TS *slot = slots + (tok * Hv + h) * (size_t)DV * DK;
+            float o_mine = 0.f;
+#pragma unroll
+            for (int r = 0; r < kDecodeRows; ++r) {
+                const float vv = __shfl_sync(0xffffffffu, vr, r);
+                const float delta = b * (vv - a * x[r]);
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) s[r][e] = fmaf(a, s[r][e], delta * kr[e]);
+                IO::store(slot + (size_t)(r0 + r) * DK + lane * EPT, s[r]);
+                const float o = fmaf(a, y[r], kq * delta);
+                if (lane == r) o_mine = o;
+            }
+            if (lane < kDecodeRows) out[(tok * Hv + h) * DV + r0 + lane] = from_f32<TIn>(o_mine);
+        }
+    }
+}
+
+template <typename TIn, typename TS, int DK>
+gdn_status launch_verify_typed(const gdn_problem &p, int K, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const void *state, void *slots, void *out, cudaStream_t stream) {
+    const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_v_heads;
+    gdn_verify_kernel<TIn, TS, DK><<<blocks, kDecodeWarps * 32, 0, stream>>>(
+        static_cast<const TIn *>(q), static_cast<const TIn *>(k), static_cast<const TIn *>(v), g,
+        beta, static_cast<const TS *>(state), static_cast<TS *>(slots), static_cast<TIn *>(out),
+        p.num_k_heads, p.num_v_heads, p.head_dim_v, K);
+    return launch_status();
+}
+
+template <typename TS>
+gdn_status launch_verify_state(const gdn_problem &p, int K, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const void *state, void *slots, void *out, cudaStream_t stream) {
+    const bool bf = p.qkv_dtype == GDN_BF16;
+    if (p.head_dim_k == 128)
+        return bf ? launch_verify_typed<__nv_bfloat16, TS, 128>(p, K, q, k, v, g, beta, state,
+                                                                slots, out, stream)
+                  : launch_verify_typed<float, TS, 128>(p, K, q, k, v, g, beta, state, slots,
+                                                        out, stream);
+    return bf ? launch_verify_typed<__nv_bfloat16, TS, 64>(p, K, q, k, v, g, beta, state, slots,
+                                                           out, stream)
+              : launch_verify_typed<float, TS, 64>(p, K, q, k, v, g, beta, state, slots, out,
+                                                   stream);
+}
+
 template <typename TIn, typename TS, int DK>
 gdn_status launch_typed(const gdn_problem &p, const void *q, const void *k, const void *v,
                         const float *g, const float *beta, void *state, void *out,
@@ -199,6 +332,25 @@ gdn_status launch_state(const gdn_problem &p, const void *q, const void *k, cons
 }
 
 }  // namespace
+
+gdn_status launch_verify(const gdn_problem &p, int num_tokens, const void *q, const void *k,
+                         const void *v, const float *g, const float *beta, const void *state,
+                         int state_dtype, void *slots, void *out, cudaStream_t stream) {
+    if (p.num_seqs == 0) return GDN_OK;
+    if (num_tokens < 1 || num_tokens > kMaxVerify) return GDN_ERR_INVALID_ARG;
+    switch (state_dtype) {
+        case GDN_F32:
+            return launch_verify_state<float>(p, num_tokens, q, k, v, g, beta, state, slots, out,
+                                              stream);
+        case GDN_F16:
+            return launch_verify_state<__half>(p, num_tokens, q, k, v, g, beta, state, slots,
+                                               out, stream);
+        case GDN_BF16:
+            return launch_verify_state<__nv_bfloat16>(p, num_tokens, q, k, v, g, beta, state,
+                                                      slots, out, stream);
+    }
+    return GDN_ERR_UNSUPPORTED;
+}
 
 gdn_status launch_decode(const gdn_problem &p, const void *q, const void *k, const void *v,
                          const float *g, const float *beta, void *state, int state_dtype,

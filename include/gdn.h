@@ -155,6 +155,35 @@ GDN_API gdn_status gdn_decode_step_half_state(const gdn_problem *problem,
                                               gdn_stream_t stream);
 
 /*
+ * Verify step of speculative decoding: num_tokens (1 to 8) consecutive
+ * tokens of every sequence, run from the stored state, with the output of
+ * every position and the state after every position in its own slot, so
+ * that the caller can keep the slot of the last accepted token.  (Page
+ * "reactapp.top": the target model checks a block of draft tokens in one
+ * pass and keeps the correct prefix -- section "DFlash2 : rediger sept
+ * tokens en une seule passe" -- with eight speculative state slots per
+ * request -- section "Pourquoi la limite est de 131 072 et non de 136 429".)
+ *   problem->total_tokens == problem->num_seqs * num_tokens; token t of
+ *   sequence n is row n * num_tokens + t of the token-major tensors:
+ *   q, k      [N * num_tokens, Hk, dk];  v, out [N * num_tokens, Hv, dv]
+ *   g, beta   [N * num_tokens, Hv] fp32
+ *   state     [N, Hv, dv, dk] in state_dtype, read only
+ *   slots     [N * num_tokens, Hv, dv, dk] in state_dtype: slot n *
+ *             num_tokens + t = the state after token t of sequence n; must
+ *             not alias state
+ *   state_dtype GDN_F32, GDN_F16 or GDN_BF16; the tokens are chained in fp32
+ *             registers, each slot is stored rounded (16-bit types: to
+ *             nearest even)
+ * Slot t equals what t + 1 successive gdn_decode_step (or
+ * gdn_decode_step_half_state) calls would leave.
+ */
+GDN_API gdn_status gdn_verify_step(const gdn_problem *problem, int32_t num_tokens,
+                                   const void *q, const void *k, const void *v,
+                                   const float *g, const float *beta,
+                                   const void *state, int32_t state_dtype,
+                                   void *slots, void *out, gdn_stream_t stream);
+
+/*
  * gdn_chunk_prefill without caller-provided scratch.  (The paper has no
  * counterpart: this exists for callers that cannot allocate device memory
  * when they call the layer -- engines that reserve nearly all device memory

@@ -132,6 +132,23 @@ def test_half_state_decode_argument_errors(lib):
     assert half_decode(lib, prob(N=0, T=0), gdn.GDN_F16) == OK
 
 
+def verify(lib, p, K, sdt=gdn.GDN_F32, state=A + 20480, slots=A + 28672, out=A + 24576):
+    return lib.gdn_verify_step(ctypes.byref(p) if p is not None else None, K, A, A + 4096,
+                               A + 8192, A + 12288, A + 16384, state, sdt, slots, out, None)
+
+
+def test_verify_argument_errors(lib):
+    assert verify(lib, None, 4) == INVALID
+    assert verify(lib, prob(N=4, T=16), 0) == INVALID
+    assert verify(lib, prob(N=4, T=36), 9) == INVALID
+    assert verify(lib, prob(N=4, T=15), 4) == INVALID          # T != N * K
+    assert verify(lib, prob(N=4, T=16), 4, sdt=9) == UNSUPPORTED
+    assert verify(lib, prob(N=4, T=16), 4, slots=A + 20480) == INVALID   # slots alias state
+    assert verify(lib, prob(N=4, T=16), 4, slots=A + 8) == MISALIGNED
+    assert verify(lib, prob(N=4, T=16), 4, out=A) == INVALID   # out aliases q
+    assert verify(lib, prob(N=0, T=0), 4) == OK
+
+
 def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
