@@ -273,6 +273,31 @@ def run_ours(args, rank, world, local):
     achieved_tf = flops / (ms_local / 1e3) / 1e12
     pbytes = prefill_bytes(T, P["Hk"], P["Hv"], P["d"])
 
+    # ---------------- the same call writing chunk-boundary snapshots ---------
+    snap_res = {}
+    for stride in (8, 1):
+        snaps = torch.empty((gdn.gdn_chunk_prefill_snapshot_slots(1, T, P["Hk"], P["Hv"], P["d"],
+                                                                  P["d"], stride),
+                             P["Hv"], P["d"], P["d"]), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            gdn.gdn_chunk_prefill_snapshots(dq, dk_, dv, dg, db, dcu, None, out=out,
+                                            snapshots=snaps, snapshot_chunks=stride)
+        snap_ms = []
+        for _ in range(5):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gdn.gdn_chunk_prefill_snapshots(dq, dk_, dv, dg, db, dcu, None, out=out,
+                                            snapshots=snaps, snapshot_chunks=stride)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            snap_ms.append(e0.elapsed_time(e1))
+        nsnap = -(-((T + 63) // 64) // stride)
+        snap_res[f"every_{stride}_chunks"] = {
+            "us_per_call": 1e3 * statistics.median(snap_ms), "snapshots": nsnap,
+            "snapshot_bytes": nsnap * P["Hv"] * P["d"] * P["d"] * 4}
+        del snaps
+
     # ---------------- end to end through host buffers ----------------
     hq, hk, hv = (x.pin_memory() for x in (p.q, p.k, p.v))
     hg, hb, hcu = (x.pin_memory() for x in (p.g, p.beta, p.cu_seqlens))
@@ -391,6 +416,7 @@ def run_ours(args, rank, world, local):
                              "bytes_per_step": dbytes16, "achieved_gbs": dec16_gbs,
                              "peak_gbs": peaks["hbm_gbs"], "frac": dec16_gbs / peaks["hbm_gbs"],
                              "speedup_vs_fp32_state": dec_us / dec16_us},
+        "prefill_with_snapshots": snap_res,
         "verify": {"workload": "64 sequences x 8 tokens from one state, a state slot per "
                                "token, 16/48 heads, d=128, bf16 q/k/v", **verify},
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},

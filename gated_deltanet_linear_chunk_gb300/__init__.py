@@ -26,7 +26,8 @@ __all__ = [
     "GDNError", "library", "gdn_chunk_prefill", "gdn_decode_step",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
-    "gdn_verify_step", "Problem",
+    "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
+    "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
@@ -97,6 +98,11 @@ def library() -> ctypes.CDLL:
     lib.gdn_version.argtypes = []
     lib.gdn_decode_step_half_state.restype = ctypes.c_int
     lib.gdn_decode_step_half_state.argtypes = [PP, P, P, P, P, P, P, ctypes.c_int32, P, P]
+    lib.gdn_chunk_prefill_snapshot_slots.restype = ctypes.c_int64
+    lib.gdn_chunk_prefill_snapshot_slots.argtypes = [PP, ctypes.c_int32]
+    lib.gdn_chunk_prefill_snapshots.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_snapshots.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_int32,
+                                                P]
     lib.gdn_verify_step.restype = ctypes.c_int
     lib.gdn_verify_step.argtypes = [PP, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int32, P, P, P]
     lib.gdn_chunk_prefill_device_status.restype = ctypes.c_int
@@ -151,6 +157,7 @@ def _check(t: torch.Tensor, name: str, dtype, shape) -> None:
 
 
 _workspaces = {}
+_NO_SNAPSHOTS = object()
 
 
 def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
@@ -162,6 +169,13 @@ def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
+
+
+def gdn_chunk_prefill_snapshot_slots(N: int, T: int, Hk: int, Hv: int, dk: int, dv: int,
+                                     snapshot_chunks: int = 1, dtype=torch.bfloat16) -> int:
+    """Slots gdn_chunk_prefill_snapshots needs (0 if unsupported)."""
+    p = make_problem(N, T, Hk, Hv, dk, dv, dtype)
+    return int(library().gdn_chunk_prefill_snapshot_slots(ctypes.byref(p), snapshot_chunks))
 
 
 def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -177,6 +191,14 @@ def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     cu_seqlens: [N+1] int32 on the device.  Returns (out, final_state); the
     final state is returned when ``final_state`` is given or
     ``output_final_state`` is set."""
+    return _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                    output_final_state, workspace, stream, _NO_SNAPSHOTS, 0)
+
+
+def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, output_final_state,
+             workspace, stream, snapshots, snapshot_chunks):
+    """Checks, workspace and dispatch of both prefill entry points
+    (``snapshots``: _NO_SNAPSHOTS, None to allocate, or a tensor)."""
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     N = cu_seqlens.shape[0] - 1
@@ -204,12 +226,44 @@ def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if workspace is None:
         workspace = _workspace(q.device, need)
     p = make_problem(N, T, Hk, Hv, dk, dv, dt, workspace)
-    rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                               _ptr(cu_seqlens), _ptr(initial_state), _ptr(out),
-                               _ptr(final_state), _stream(stream))
+    if snapshots is _NO_SNAPSHOTS:
+        rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state), _ptr(out),
+                                   _ptr(final_state), _stream(stream))
+        if rc != 0:
+            raise GDNError(rc, "gdn_chunk_prefill")
+        return out, final_state
+    slots = int(lib.gdn_chunk_prefill_snapshot_slots(ctypes.byref(p), snapshot_chunks))
+    if slots == 0:
+        raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_prefill_snapshots")
+    if snapshots is None:
+        snapshots = torch.empty((slots, Hv, dv, dk), dtype=torch.float32, device=q.device)
+    _check(snapshots, "snapshots", torch.float32, (slots, Hv, dv, dk))
+    rc = lib.gdn_chunk_prefill_snapshots(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                         _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state),
+                                         _ptr(out), _ptr(final_state), _ptr(snapshots),
+                                         snapshot_chunks, _stream(stream))
     if rc != 0:
-        raise GDNError(rc, "gdn_chunk_prefill")
-    return out, final_state
+        raise GDNError(rc, "gdn_chunk_prefill_snapshots")
+    return out, final_state, snapshots
+
+
+def gdn_chunk_prefill_snapshots(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                g: torch.Tensor, beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                                initial_state: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None,
+                                final_state: Optional[torch.Tensor] = None,
+                                output_final_state: bool = False,
+                                snapshots: Optional[torch.Tensor] = None,
+                                snapshot_chunks: int = 1,
+                                workspace: Optional[torch.Tensor] = None, stream=None):
+    """``gdn_chunk_prefill`` that also returns states at chunk boundaries (see
+    ``gdn_chunk_prefill_snapshots`` in include/gdn.h): one after every
+    ``snapshot_chunks`` chunks (64 tokens each) and after the last chunk of
+    each sequence.  Returns (out, final_state, snapshots [slots, Hv, dv, dk]
+    fp32); sequence n's snapshot i is slot sum_{m<n} ceil(chunks_m / s) + i."""
+    return _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                    output_final_state, workspace, stream, snapshots, snapshot_chunks)
 
 
 def gdn_chunk_prefill_device_status(workspace: Optional[torch.Tensor] = None,

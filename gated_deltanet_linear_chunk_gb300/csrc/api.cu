@@ -47,20 +47,29 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem) {
     return prefill_tc_supported(*problem) ? prefill_tc_workspace_size(*problem) : 0;
 }
 
-GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem, const void *q, const void *k,
-                                     const void *v, const float *g, const float *beta,
-                                     const int32_t *cu_seqlens, const float *initial_state,
-                                     void *out, float *final_state, gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The prefill entry points share their checks and dispatch; `snaps` (state
+// after every chunk) is only supported on the tensor-core path.
+gdn_status prefill_impl(const gdn_problem *problem, const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, const int32_t *cu_seqlens,
+                        const float *initial_state, void *out, float *final_state, float *snaps,
+                        int snap_stride, bool want_snaps, gdn_stream_t stream) {
     const gdn_status st = check_problem(problem);
     if (st != GDN_OK) return st;
     const gdn_problem &p = *problem;
+    if (want_snaps && !prefill_tc_supported(p)) return GDN_ERR_UNSUPPORTED;
     if (p.num_seqs == 0) return p.total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
     if (p.total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
-    if (any_misaligned({q, k, v, g, beta, initial_state, out, final_state}))
+    if (want_snaps && (!snaps || snap_stride < 1)) return GDN_ERR_INVALID_ARG;
+    if (any_misaligned({q, k, v, g, beta, initial_state, out, final_state, snaps}))
         return GDN_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return GDN_ERR_MISALIGNED;
     if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
+    if (snaps && (snaps == initial_state || snaps == final_state)) return GDN_ERR_INVALID_ARG;
     const size_t need = gdn_chunk_prefill_workspace_size(problem);
     if (need > 0) {
         if (!p.workspace || p.workspace_bytes < need) return GDN_ERR_WORKSPACE;
@@ -69,9 +78,39 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem, const void *q, 
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     if (prefill_tc_supported(p))
         return launch_prefill_tc(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
-                                 st_);
+                                 snaps, snap_stride, st_);
     return launch_prefill_simt(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
                                st_);
+}
+
+}  // namespace
+
+extern "C" {
+
+GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem, const void *q, const void *k,
+                                     const void *v, const float *g, const float *beta,
+                                     const int32_t *cu_seqlens, const float *initial_state,
+                                     void *out, float *final_state, gdn_stream_t stream) {
+    return prefill_impl(problem, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                        nullptr, 1, false, stream);
+}
+
+GDN_API int64_t gdn_chunk_prefill_snapshot_slots(const gdn_problem *problem,
+                                                 int32_t snapshot_chunks) {
+    if (check_problem(problem) != GDN_OK || !prefill_tc_supported(*problem) ||
+        snapshot_chunks < 1)
+        return 0;
+    return prefill_tc_snapshot_slots(*problem, snapshot_chunks);
+}
+
+GDN_API gdn_status gdn_chunk_prefill_snapshots(const gdn_problem *problem, const void *q,
+                                               const void *k, const void *v, const float *g,
+                                               const float *beta, const int32_t *cu_seqlens,
+                                               const float *initial_state, void *out,
+                                               float *final_state, float *snapshots,
+                                               int32_t snapshot_chunks, gdn_stream_t stream) {
+    return prefill_impl(problem, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                        snapshots, snapshot_chunks, true, stream);
 }
 
 GDN_API gdn_status gdn_decode_step(const gdn_problem *problem, const void *q, const void *k,

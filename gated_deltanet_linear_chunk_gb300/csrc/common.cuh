@@ -58,8 +58,14 @@ void *noalloc_scratch();
 
 size_t prefill_tc_workspace_size(const gdn_problem &p);
 bool prefill_tc_supported(const gdn_problem &p);
+// snaps: fp32 [slots, Hv, dv, dk] or nullptr: the state after every
+// snap_stride-th chunk and after the last chunk of every sequence.
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, const int32_t *cu_seqlens,
-                             const float *h0, void *out, float *hT, cudaStream_t stream);
+                             const float *h0, void *out, float *hT, float *snaps,
+                             int snap_stride, cudaStream_t stream);
+// Snapshot slots of a problem with one snapshot per snap_stride chunks (a
+// bound on the batch's count).
+int64_t prefill_tc_snapshot_slots(const gdn_problem &p, int snap_stride);
 
 }  // namespace gdn

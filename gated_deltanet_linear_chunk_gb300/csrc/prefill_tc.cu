@@ -72,7 +72,7 @@ constexpr int kSlotBytes = kSlotDEC + 256;    // 49664
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-    size_t hdr, chunk_off, order, table, gl, tiles, total;
+    size_t hdr, chunk_off, snap_off, order, table, gl, tiles, total;
     int64_t max_chunks;
 };
 
@@ -83,7 +83,8 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.max_chunks = (p.total_tokens + C - 1) / C + p.num_seqs;
     w.hdr = 0;
     w.chunk_off = 256;
-    w.order = align_up(w.chunk_off + 4 * (size_t)(p.num_seqs + 1), 256);
+    w.snap_off = align_up(w.chunk_off + 4 * (size_t)(p.num_seqs + 1), 256);
+    w.order = align_up(w.snap_off + 4 * (size_t)(p.num_seqs + 1), 256);
     w.table = align_up(w.order + 4 * (size_t)p.num_seqs, 256);
     w.gl = align_up(w.table + 16 * (size_t)w.max_chunks, 256);  // e^{gamma_L} per (chunk, value head)
     w.tiles = align_up(w.gl + 4 * (size_t)w.max_chunks * p.num_v_heads, 1024);
@@ -100,14 +101,16 @@ WsLayout ws_layout(const gdn_problem &p) {
 // make the whole call a no-op.
 __global__ void __launch_bounds__(1024)
 gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t max_chunks,
-                       int *__restrict__ err, int *__restrict__ chunk_off,
-                       int *__restrict__ order, int4 *__restrict__ table) {
-    __shared__ int s_scan[1024];
-    __shared__ int s_carry;
+                       int snap_stride, int *__restrict__ err, int *__restrict__ chunk_off,
+                       int *__restrict__ snap_off, int *__restrict__ order,
+                       int4 *__restrict__ table) {
+    __shared__ int s_scan[1024], s_scan2[1024];
+    __shared__ int s_carry, s_carry2;
     __shared__ int s_bad;
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_carry = 0;
+        s_carry2 = 0;
         s_bad = (cu[0] != 0 || (int64_t)cu[N] != T) ? 1 : 0;
         *err = kErrNone;
     }
@@ -120,22 +123,35 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
             if (len < 0) s_bad = 1;
             nch = len > 0 ? (len + C - 1) / C : 0;
         }
+        // Snapshot slots of the sequence: one per snap_stride chunks, the
+        // last chunk always included.
+        const int nsn = (n < N && snap_stride > 0) ? (nch + snap_stride - 1) / snap_stride : 0;
         s_scan[tid] = nch;
+        s_scan2[tid] = nsn;
         __syncthreads();
         for (int off = 1; off < 1024; off <<= 1) {
             const int x = tid >= off ? s_scan[tid - off] : 0;
+            const int x2 = tid >= off ? s_scan2[tid - off] : 0;
             __syncthreads();
             s_scan[tid] += x;
+            s_scan2[tid] += x2;
             __syncthreads();
         }
-        if (n < N) chunk_off[n] = s_carry + s_scan[tid] - nch;
+        if (n < N) {
+            chunk_off[n] = s_carry + s_scan[tid] - nch;
+            snap_off[n] = s_carry2 + s_scan2[tid] - nsn;
+        }
         __syncthreads();
-        if (tid == 1023) s_carry += s_scan[1023];
+        if (tid == 1023) {
+            s_carry += s_scan[1023];
+            s_carry2 += s_scan2[1023];
+        }
         __syncthreads();
     }
     if (tid == 0) {
         if ((int64_t)s_carry > max_chunks) s_bad = 1;
         if (s_bad) *err = kErrCuSeqlens;
+        snap_off[N] = s_carry2;
         chunk_off[N] = s_bad ? 0 : s_carry;
     }
     __syncthreads();
@@ -657,7 +673,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                  const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
                  const float *__restrict__ gl, const float *__restrict__ h0,
                  __nv_bfloat16 *__restrict__ out,
-                 float *__restrict__ hT, int *__restrict__ err, int N, int Hk, int Hv) {
+                 float *__restrict__ hT, float *__restrict__ snaps, int snap_stride,
+                 const int *__restrict__ snap_off, int *__restrict__ err, int N, int Hk, int Hv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -946,6 +963,17 @@ if (elect_one_sync()) {
                     tc_fence_before();
                     mbar_arrive(&sm.s16_ready);
                 }
+                if (snaps && ((c + 1) % snap_stride == 0 || c == nc - 1)) {
+                    // State after this chunk, into its snapshot slot (after the
+                    // hand-off: off the chain's critical path).
+                    const int slot = snap_off[n] + c / snap_stride;
+                    float *dst = snaps + ((size_t)slot * Hv + h) * D * D + (size_t)j * D + 64 * h2;
+#pragma unroll
+                    for (int i = 0; i < 64; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) =
+                            make_float4(sigma * x[i], sigma * x[i + 1], sigma * x[i + 2],
+                                        sigma * x[i + 3]);
+                }
             }
         }
     } else {
@@ -1060,18 +1088,24 @@ bool encode_thd(CUtensorMap *map, const void *base, int64_t T, int H) {
 
 size_t prefill_tc_workspace_size(const gdn_problem &p) { return ws_layout(p).total; }
 
+int64_t prefill_tc_snapshot_slots(const gdn_problem &p, int snap_stride) {
+    return (ws_layout(p).max_chunks + snap_stride - 1) / snap_stride + p.num_seqs;
+}
+
 bool prefill_tc_supported(const gdn_problem &p) {
     return p.qkv_dtype == GDN_BF16 && p.head_dim_k == D && p.head_dim_v == D;
 }
 
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, const int32_t *cu,
-                             const float *h0, void *out, float *hT, cudaStream_t stream) {
+                             const float *h0, void *out, float *hT, float *snaps,
+                             int snap_stride, cudaStream_t stream) {
     if (p.num_seqs == 0) return GDN_OK;
     const WsLayout w = ws_layout(p);
     uint8_t *ws = static_cast<uint8_t *>(p.workspace);
     int *err = reinterpret_cast<int *>(ws + w.hdr);
     int *chunk_off = reinterpret_cast<int *>(ws + w.chunk_off);
+    int *snap_off = reinterpret_cast<int *>(ws + w.snap_off);
     int *order = reinterpret_cast<int *>(ws + w.order);
     int4 *table = reinterpret_cast<int4 *>(ws + w.table);
     float *gl = reinterpret_cast<float *>(ws + w.gl);
@@ -1092,7 +1126,8 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     }
 
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, p.num_seqs, p.total_tokens, w.max_chunks,
-                                                    err, chunk_off, order, table);
+                                                    snaps ? snap_stride : 0, err, chunk_off,
+                                                    snap_off, order, table);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
 
     if (p.total_tokens > 0) {
@@ -1112,7 +1147,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         return GDN_ERR_CUDA;
     gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
         tk, tv, to, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
-        err, p.num_seqs, p.num_k_heads, p.num_v_heads);
+        snaps, snaps ? snap_stride : 1, snap_off, err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -124,6 +124,47 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
                                      gdn_stream_t stream);
 
 /*
+ * Snapshot slots gdn_chunk_prefill_snapshots needs for this problem with
+ * one snapshot every snapshot_chunks chunks: ceil((ceil(T / 64) + N) /
+ * snapshot_chunks) + N, a bound on the batch's count (sum over sequences of
+ * ceil(chunks_n / snapshot_chunks)).  0 when the descriptor is invalid,
+ * snapshot_chunks < 1, or the configuration has no snapshot support.
+ */
+GDN_API int64_t gdn_chunk_prefill_snapshot_slots(const gdn_problem *problem,
+                                                 int32_t snapshot_chunks);
+
+/*
+ * gdn_chunk_prefill that also writes the state at chunk boundaries of every
+ * sequence, for prefix caching (page "reactapp.top", section "Pourquoi cela
+ * convient aux agents harness": the prefix cache keeps the DeltaNet
+ * recurrent state, not only the attention KV data; page "note.hsfp.cn",
+ * section "5. 三级缓存体系": cached prefix states are restored and only the
+ * rest of the prompt is prefilled).
+ *   snapshot_chunks  s >= 1: a snapshot after chunks s - 1, 2 s - 1, ... of
+ *              each sequence (every 64 s tokens) and after its last chunk
+ *   snapshots  fp32 [slots, Hv, dv, dk] (slots from the query above).
+ *              Sequence n owns slots base_n .. base_n + ceil(chunks_n / s) - 1,
+ *              base_n = sum_{m<n} ceil(chunks_m / s), chunks_n =
+ *              ceil(len_n / 64); its slot base_n + i holds the state after
+ *              token min(64 s (i + 1), len_n), ready to be passed back as an
+ *              initial state.  Slots past the batch's count are not written.
+ *              Must not alias the states.
+ * Only for bf16 q/k/v with dk = dv = 128 (the tensor-core path); other
+ * configurations return GDN_ERR_UNSUPPORTED.  Everything else as
+ * gdn_chunk_prefill (same workspace size).  The snapshot stores come from
+ * the warps that carry the state, so a snapshot after every chunk (s = 1)
+ * about doubles the call at 48 heads; s = 8 (512 tokens) costs far less.
+ */
+GDN_API gdn_status gdn_chunk_prefill_snapshots(const gdn_problem *problem,
+                                               const void *q, const void *k, const void *v,
+                                               const float *g, const float *beta,
+                                               const int32_t *cu_seqlens,
+                                               const float *initial_state,
+                                               void *out, float *final_state,
+                                               float *snapshots, int32_t snapshot_chunks,
+                                               gdn_stream_t stream);
+
+/*
  * One recurrent decode step for N sequences (one token each), updating the
  * state in place:
  *   q, k   [N, Hk, dk];  v, out [N, Hv, dv] (qkv dtype);  g, beta [N, Hv] fp32

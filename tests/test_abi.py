@@ -149,6 +149,26 @@ def test_verify_argument_errors(lib):
     assert verify(lib, prob(N=0, T=0), 4) == OK
 
 
+def test_snapshot_entry_points(lib):
+    p = prob(N=2, T=130, Hk=1, Hv=3, ws=A, wsb=1 << 40)
+    slots = lib.gdn_chunk_prefill_snapshot_slots
+    assert slots(ctypes.byref(p), 1) == (3 + 2) + 2
+    assert slots(ctypes.byref(p), 2) == 3 + 2
+    assert slots(ctypes.byref(p), 0) == 0
+    assert slots(ctypes.byref(prob(dtype=gdn.GDN_F32)), 1) == 0
+    assert slots(ctypes.byref(prob(dk=64, dv=64)), 1) == 0
+
+    def snap(p, snaps, s=1):
+        return lib.gdn_chunk_prefill_snapshots(ctypes.byref(p), A, A + 4096, A + 8192,
+                                               A + 12288, A + 16384, A + 20480, None,
+                                               A + 24576, None, snaps, s, None)
+    assert snap(p, None) == INVALID
+    assert snap(p, A + 32768, s=0) == INVALID
+    assert snap(p, A + 8) == MISALIGNED
+    assert snap(prob(N=1, T=64, dtype=gdn.GDN_F32), A + 32768) == UNSUPPORTED
+    assert snap(prob(N=1, T=64, dk=64, dv=64), A + 32768) == UNSUPPORTED
+
+
 def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
