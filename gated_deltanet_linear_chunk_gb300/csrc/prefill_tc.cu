@@ -666,6 +666,9 @@ __device__ __forceinline__ void store_state(uint32_t t_ns, uint32_t t_s, const f
     tmem_st32(t_s + 32, r);
 }
 
+// kSnaps: the instantiation that writes chunk-boundary snapshots (a separate
+// instantiation keeps the snapshot code out of the plain kernel's hot loop).
+template <bool kSnaps>
 __global__ void __launch_bounds__(kChainThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_o,
@@ -963,7 +966,7 @@ if (elect_one_sync()) {
                     tc_fence_before();
                     mbar_arrive(&sm.s16_ready);
                 }
-                if (snaps && ((c + 1) % snap_stride == 0 || c == nc - 1)) {
+                if (kSnaps && ((c + 1) % snap_stride == 0 || c == nc - 1)) {
                     // State after this chunk, into its snapshot slot (after the
                     // hand-off: off the chain's critical path).
                     const int slot = snap_off[n] + c / snap_stride;
@@ -1142,10 +1145,11 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
     const size_t smem = sizeof(ChainSmem) + 1024;
-    if (cudaFuncSetAttribute(gdn_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    auto chain = snaps ? gdn_chain_kernel<true> : gdn_chain_kernel<false>;
+    if (cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
         return GDN_ERR_CUDA;
-    gdn_chain_kernel<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
+    chain<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
         tk, tv, to, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
         snaps, snaps ? snap_stride : 1, snap_off, err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
