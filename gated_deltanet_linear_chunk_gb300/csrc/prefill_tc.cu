@@ -605,6 +605,11 @@ struct alignas(1024) ChainStage {  // 1024-aligned: the tiles are 128-byte-swizz
     float egdec[2 * C];     // e^{gamma_t}, then e^{gamma_L - gamma_t}
 };
 
+// The snapshot stores stage 8 warps x 8 KB in the K, Q~, V, W^T tiles.
+static_assert(offsetof(ChainStage, q) == 2 * kTile && offsetof(ChainStage, v) == 4 * kTile &&
+                  offsetof(ChainStage, wt) == 6 * kTile && offsetof(ChainStage, tb) == 8 * kTile,
+              "snapshot staging needs K, Q~, V, W^T contiguous");
+
 struct ChainSmem {
     ChainStage st[2];
     uint8_t ostage[3][C * D * 2];  // output tiles [64 tokens][128 dv] bf16, for TMA stores
@@ -666,12 +671,54 @@ __device__ __forceinline__ void store_state(uint32_t t_ns, uint32_t t_s, const f
     tmem_st32(t_s + 32, r);
 }
 
+// A state warp's 32 rows x 64 columns of sigma S^ (the state after chunk c)
+// into snapshot plane z of `map` ([planes, 128 dv, 128 dk] fp32).  Once o_done shows
+// chunk c's MMAs complete, the stage's K, Q~, V and W^T tiles (64 KB, 8 KB a
+// warp) are dead: the rows are staged there as two [32][32] fp32 boxes
+// (128-byte swizzle: conflict-free) and stored by TMA, so the global writes
+// bypass the load/store pipe that the chain's waits go through (row-per-
+// thread stores would touch 32 lines per instruction).  S^ is read from TMEM
+// again: it stays put until this warp's next dt_ready.  The stage goes back
+// to the producer once the stores have read it.  Out of line
+// and rarely taken, so the chain loop stays small in the instruction cache.
+// False when a bounded wait ran out.
+__device__ __noinline__ bool store_state_rows(ChainSmem &sm, const CUtensorMap *map, uint32_t t_s,
+                                              float sigma, int c, int z) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (!warp_wait_lean(&sm.o_done[c & 1], (c >> 1) & 1, &sm.abort)) return false;
+    uint8_t *stg = sm.st[c & 1].k + (warp - 2) * kTile;
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+        uint32_t r[32];
+        tmem_ld32(t_s + 32 * b, r);
+        tmem_ld_wait();
+        uint8_t *box = stg + b * (kTile / 2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4 *>(box + swz(lane, i)) = make_float4(
+                sigma * __uint_as_float(r[4 * i]), sigma * __uint_as_float(r[4 * i + 1]),
+                sigma * __uint_as_float(r[4 * i + 2]), sigma * __uint_as_float(r[4 * i + 3]));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        const int x = 64 * ((warp - 2) >> 2), y = 32 * (warp & 3);
+        tma_store_3d(map, x, y, z, stg);
+        tma_store_3d(map, x + 32, y, z, stg + kTile / 2);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+    mbar_arrive(&sm.empty[c & 1]);
+    return true;
+}
+
 // kSnaps: the instantiation that writes chunk-boundary snapshots (a separate
 // instantiation keeps the snapshot code out of the plain kernel's hot loop).
 template <bool kSnaps>
 __global__ void __launch_bounds__(kChainThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_o,
+                 const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_s,
                  const int *__restrict__ chunk_off, const int *__restrict__ order,
                  const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
                  const float *__restrict__ gl, const float *__restrict__ h0,
@@ -707,6 +754,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_o);
+        if (kSnaps) prefetch_tensormap(&tm_s);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1 + kStateThreads);
@@ -757,22 +805,26 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             #pragma unroll 1
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
-                if (c >= 2 && !warp_wait_spin(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
+                if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
                 ChainStage &st = sm.st[s];
                 uint64_t *bar = &sm.full[s];
                 const uint8_t *slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
-                mbar_arrive_expect_tx_w(bar, kStageBytes);
-                tma_load_3d_w(st.k, &tm_k, 0, hk, tok0, bar);
-                tma_load_3d_w(st.k + kTile, &tm_k, 64, hk, tok0, bar);
-                tma_load_3d_w(st.v, &tm_v, 0, h, tok0, bar);
-                tma_load_3d_w(st.v + kTile, &tm_v, 64, h, tok0, bar);
-                bulk_load_w(st.wt, slot + kSlotWT, 2 * kTile, bar);
-                bulk_load_w(st.tb, slot + kSlotTB, kTile, bar);
-                bulk_load_w(st.p, slot + kSlotP, kTile, bar);
-                bulk_load_w(st.q, slot + kSlotQ, 2 * kTile, bar);
-                bulk_load_w(st.egdec, slot + kSlotEG, 512, bar);
+                // One elected lane issues the stage's copies (per-copy
+                // elections cost code the instruction cache has to hold).
+                if (elect_one_sync()) {
+                    mbar_arrive_expect_tx(bar, kStageBytes);
+                    tma_load_3d(st.k, &tm_k, 0, hk, tok0, bar);
+                    tma_load_3d(st.k + kTile, &tm_k, 64, hk, tok0, bar);
+                    tma_load_3d(st.v, &tm_v, 0, h, tok0, bar);
+                    tma_load_3d(st.v + kTile, &tm_v, 64, h, tok0, bar);
+                    bulk_load(st.wt, slot + kSlotWT, 2 * kTile, bar);
+                    bulk_load(st.tb, slot + kSlotTB, kTile, bar);
+                    bulk_load(st.p, slot + kSlotP, kTile, bar);
+                    bulk_load(st.q, slot + kSlotQ, 2 * kTile, bar);
+                    bulk_load(st.egdec, slot + kSlotEG, 512, bar);
+                }
                 if (lane == 0) sm.issued = c + 1;
                 if (c + 2 + kPrefetch - 1 < nc && c >= 1) prefetch(c + 2 + kPrefetch - 1);
                 __syncwarp();
@@ -793,7 +845,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             // D = U^T = V^T (T diag b)^T             [M=128 dv, N=64, K=64 tokens]
             auto issue_u = [&](int c) -> bool {
                 const int s = c & 1;
-                if (!warp_wait_spin(&sm.full[s], (c >> 1) & 1, &sm.abort)) return false;
+                if (!warp_wait_lean(&sm.full[s], (c >> 1) & 1, &sm.abort)) return false;
                 tc_fence_after();
                 ChainStage &st = sm.st[s];
                 const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
@@ -819,7 +871,7 @@ if (elect_one_sync()) {
                 const uint64_t d_p = smem_desc(smem_u32(st.p), 16, 1024);
                 const uint32_t ns = kColNS + 64 * (c & 1);
                 const uint32_t ob = kColO + 64 * (c & 1);
-                if (!warp_wait_spin(&sm.s16_ready, c & 1, &sm.abort)) break;
+                if (!warp_wait_lean(&sm.s16_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // D += (-S0) W^T  ->  Delta^T            [M=128 dv, N=64, K=128 dk]
 if (elect_one_sync()) {
@@ -836,7 +888,7 @@ if (elect_one_sync()) {
                 // copy of its code: the issuing warp's loop has to stay small
                 // enough for the instruction cache, or its MMAs issue at
                 // instruction-fetch speed.
-                if (c >= 2 && !warp_wait_spin(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
+                if (c >= 2 && !warp_wait_lean(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
                 tc_fence_after();
 if (elect_one_sync()) {
 #pragma unroll
@@ -845,7 +897,7 @@ if (elect_one_sync()) {
                                     d_q + (k / 4) * (kTile / 16) + 2 * (k % 4), id_qn, k > 0);
                 }
                 __syncwarp();
-                if (!warp_wait_spin(&sm.dt_ready, c & 1, &sm.abort)) break;
+                if (!warp_wait_lean(&sm.dt_ready, c & 1, &sm.abort)) break;
                 tc_fence_after();
                 // S^ += (Delta^T diag(e^{gamma_L - gamma}) / sigma) K   [M=128, N=128, K=64]
                 // as two N = 64 halves (an N = 128 MMA with A in TMEM runs
@@ -885,6 +937,8 @@ if (elect_one_sync()) {
         const uint32_t t_s = tmem + lane_base + kColS + 64 * h2;
         float sigma = 1.f;
         bool ok = true;
+        // Snapshot countdown and plane (no division in the loop).
+        int snap_left = snap_stride, snap_z = kSnaps ? snap_off[n] * Hv + h : 0;
         {
             float x[64];
 #pragma unroll
@@ -903,7 +957,12 @@ if (elect_one_sync()) {
         for (int c = 0; ok && c < nc; ++c) {
             const float *dec = sm.st[c & 1].egdec + C;
             const float decay = gl[(size_t)(c_begin + c) * Hv + h];  // e^{gamma_L} of chunk c
-            if (!(ok = warp_wait(&sm.d_done, c & 1, &sm.abort))) break;
+            bool snap_here = false;
+            if (kSnaps) {
+                snap_here = --snap_left == 0 || c == nc - 1;
+                if (snap_left == 0) snap_left = snap_stride;
+            }
+            if (!(ok = warp_wait_lean(&sm.d_done, c & 1, &sm.abort))) break;
             tc_fence_after();
             float sigma_next = sigma * decay;
             if (!(sigma_next >= kRenorm)) {
@@ -941,8 +1000,8 @@ if (elect_one_sync()) {
             sigma = sigma_next;
             tc_fence_before();
             mbar_arrive(&sm.dt_ready);
-            mbar_arrive(&sm.empty[c & 1]);
-            if (!(ok = warp_wait(&sm.s_done, c & 1, &sm.abort))) break;
+            if (!snap_here) mbar_arrive(&sm.empty[c & 1]);  // else after the snapshot
+            if (!(ok = warp_wait_lean(&sm.s_done, c & 1, &sm.abort))) break;
             tc_fence_after();
             {
                 float x[64];
@@ -957,6 +1016,7 @@ if (elect_one_sync()) {
                                             sigma * x[i + 3]);
                     }
                 } else {
+                    // -S0 of chunk c + 1 for the MMAs (the hand-off).
                     uint32_t r[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -966,19 +1026,13 @@ if (elect_one_sync()) {
                     tc_fence_before();
                     mbar_arrive(&sm.s16_ready);
                 }
-                if (kSnaps && ((c + 1) % snap_stride == 0 || c == nc - 1)) {
-                    // State after this chunk, into its snapshot slot (after the
-                    // hand-off: off the chain's critical path).
-                    const int slot = snap_off[n] + c / snap_stride;
-                    float *dst = snaps + ((size_t)slot * Hv + h) * D * D + (size_t)j * D + 64 * h2;
-#pragma unroll
-                    for (int i = 0; i < 64; i += 4)
-                        *reinterpret_cast<float4 *>(dst + i) =
-                            make_float4(sigma * x[i], sigma * x[i + 1], sigma * x[i + 2],
-                                        sigma * x[i + 3]);
-                }
+            }
+            if (snap_here) {
+                if (!(ok = store_state_rows(sm, &tm_s, t_s, sigma, c, snap_z))) break;
+                snap_z += Hv;
             }
         }
+        if (kSnaps && lane == 0) bulk_wait_group<0>();
     } else {
         // ---------------- output warps 10-13: o_t = S0 (e^{gamma_t} q_t) +
         // (Delta^T P^T)_t for this warp's 32 value dims, read from this
@@ -994,7 +1048,7 @@ if (elect_one_sync()) {
         for (int c = 0; c < nc; ++c) {
             const int4 e = table[c_begin + c];
             const int tok0 = e.y, L = e.z;
-            if (!warp_wait(&sm.o_done[c & 1], (c >> 1) & 1, &sm.abort)) break;
+            if (!warp_wait_lean(&sm.o_done[c & 1], (c >> 1) & 1, &sm.abort)) break;
             tc_fence_after();
             uint32_t r[2][32];
             tmem_ld16x256b_x8(tmem + lane_base + kColO + 64 * (c & 1), r[0]);
@@ -1087,6 +1141,20 @@ bool encode_thd(CUtensorMap *map, const void *base, int64_t T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Snapshots as a [slots Hv, 128 dv, 128 dk] fp32 tensor; boxes of 32 dk x
+// 32 dv rows, 128-byte swizzle (the staging layout of the stores).
+bool encode_states(CUtensorMap *map, float *base, int64_t planes) {
+    auto enc = tensor_map_encoder();
+    if (!enc || planes < 1 || planes > (int64_t)UINT32_MAX) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
+    const cuuint32_t box[3] = {32u, 32u, 1u};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t prefill_tc_workspace_size(const gdn_problem &p) { return ws_layout(p).total; }
@@ -1144,13 +1212,17 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
                                                           p.num_v_heads);
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
+    CUtensorMap ts = to;
+    if (snaps && !encode_states(&ts, snaps,
+                                prefill_tc_snapshot_slots(p, snap_stride) * p.num_v_heads))
+        return GDN_ERR_CUDA;
     const size_t smem = sizeof(ChainSmem) + 1024;
     auto chain = snaps ? gdn_chain_kernel<true> : gdn_chain_kernel<false>;
     if (cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
     chain<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
-        tk, tv, to, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
+        tk, tv, to, ts, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
         snaps, snaps ? snap_stride : 1, snap_off, err, p.num_seqs, p.num_k_heads, p.num_v_heads);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

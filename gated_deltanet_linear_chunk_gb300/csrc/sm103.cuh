@@ -131,6 +131,27 @@ __device__ __forceinline__ bool warp_wait_spin(uint64_t *bar, uint32_t parity, v
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Bounded wait with the least code, for kernels whose loops have to fit the
+// instruction cache (the recurrence kernel: every inlined wait there is code
+// that its warps' loops share the cache with).  Every lane polls, so there is
+// no branch on the lane and no shuffle (a poll costs the warp one issue slot
+// either way, and all lanes read the same barrier, flag and clock, so they
+// decide alike); the abort flag and the clock limit are checked on every poll.
+// Returns false on time-out or when *abort is set, after setting *abort.
+__device__ __forceinline__ bool warp_wait_lean(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               long long limit = 4000000000ll) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+#pragma unroll 1
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort || clock64() - t0 > limit) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Single-thread bounded wait for the latency-critical roles (TMA producer,
 // MMA issuer): plain polling, no suspend hint, time limit checked every 256
 // polls.

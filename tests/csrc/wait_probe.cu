@@ -8,6 +8,8 @@
 //   1: both warps: sleeping wait (warp_wait) with the given limit
 //   2: warp 0 spins with the limit; warp 1 sleeps with a limit 100 times
 //      longer and must leave once warp 0 has raised the abort flag
+//   3: both warps: all-lane wait (warp_wait_lean) with the given limit
+//   4: as 2 with warp_wait_lean in both warps
 // out[4 w + 0] = wait result of warp w (1 = completed), out[4 w + 1] = abort
 // flag seen by warp w afterwards, out[4 w + 2] = cycles waited / 1024.
 #include <stdint.h>
@@ -33,9 +35,13 @@ extern "C" __global__ void __launch_bounds__(64) wait_probe_kernel(int mode, lon
         ok = warp_wait_spin(&bar, 0, &abort_flag, limit);
     else if (mode == 1)
         ok = warp_wait(&bar, 0, &abort_flag, limit);
-    else
+    else if (mode == 2)
         ok = warp == 0 ? warp_wait_spin(&bar, 0, &abort_flag, limit)
                        : warp_wait(&bar, 0, &abort_flag, 100 * limit);
+    else if (mode == 3)
+        ok = warp_wait_lean(&bar, 0, &abort_flag, limit);
+    else
+        ok = warp_wait_lean(&bar, 0, &abort_flag, warp == 0 ? limit : 100 * limit);
     const long long t1 = clock64();
     if (lane == 0) {
         out[4 * warp] = ok ? 1 : 0;

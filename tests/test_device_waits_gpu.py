@@ -51,17 +51,18 @@ def run(probe, mode, limit=LIMIT):
     return [dict(ok=o[4 * w], abort=o[4 * w + 1], kcycles=o[4 * w + 2]) for w in range(2)]
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 3])
 def test_bounded_wait_gives_up_and_raises_abort(probe, mode):
     for w in run(probe, mode):
         assert w["ok"] == 0 and w["abort"] == 1
         assert w["kcycles"] * 1024 >= LIMIT - 1024
 
 
-def test_abort_releases_the_other_waiters(probe):
+@pytest.mark.parametrize("mode", [2, 4])
+def test_abort_releases_the_other_waiters(probe, mode):
     """Warp 0 times out; warp 1, whose own limit is 100 times longer, leaves
     on the abort flag well before its limit."""
-    w0, w1 = run(probe, 2)
+    w0, w1 = run(probe, mode)
     assert w0["ok"] == 0 and w1["ok"] == 0 and w1["abort"] == 1
     assert w1["kcycles"] * 1024 < 10 * LIMIT
 
