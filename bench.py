@@ -35,6 +35,11 @@ L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
 # Algorithmic work per token per value head (d = 128, C = 64, G = 3), the
 # triangle-aware chunked count: 6 d^2 + C (dk + dv) + C dv + 2 C dk / G + C^2 / 3.
 FLOPS_PER_TOKEN_HEAD = 6 * 128 ** 2 + 64 * 256 + 64 * 128 + 2 * 64 * 128 // 3 + 64 ** 2 // 3
+# Its split between the two main kernels: the recurrence (state products
+# 6 d^2, U^T and Delta^T P^T 2 C d_v) and prep (W C d_k, K K^T and Q K^T
+# 2 C d_k / G, the triangular inverse C^2 / 3).
+FLOPS_RECURRENCE = 6 * 128 ** 2 + 2 * 64 * 128
+FLOPS_PREP = FLOPS_PER_TOKEN_HEAD - FLOPS_RECURRENCE
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -46,6 +51,23 @@ def load_peaks():
         return d, "measured"
     except (OSError, ValueError):
         return FALLBACK_PEAKS, "fallback"
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
+    summary, or None when the kernel source has changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "prefill_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, "gated_deltanet_linear_chunk_gb300", "csrc",
+                               "prefill_tc.cu"), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != digest or kernel not in rec.get("bytes_per_launch", {}):
+        return None
+    return rec["bytes_per_launch"][kernel]
 
 
 def prefill_bytes(T, Hk, Hv, d):
@@ -262,6 +284,18 @@ def run_ours(args, rank, world, local):
             ends[i].record(stream)
         torch.cuda.synchronize()
         barrier()
+        # Per-kernel times: the same steps again with the library recording
+        # events between its three launches on this stream (kept out of the
+        # headline steps: the extra records cost the call a few us), each
+        # step's times read after it.
+        gdn.gdn_prefill_timing(True)
+        kernel_ms = []
+        for i in range(args.steps):
+            flush.zero_()
+            prefill()
+            kernel_ms.append(gdn.gdn_prefill_kernel_ms())
+        gdn.gdn_prefill_timing(False)
+        torch.cuda.synchronize()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(ms_local, dev)
@@ -270,7 +304,14 @@ def run_ours(args, rank, world, local):
 
     flops = T * P["Hv"] * FLOPS_PER_TOKEN_HEAD
     peak_tf = peaks["bf16_tflops"]
-    achieved_tf = flops / (ms_local / 1e3) / 1e12
+    # Roofline of the dominant kernel: its algorithmic flops per launch over
+    # its mean launch time in the timed steps.
+    k_us = {name: 1e3 * statistics.mean(m[i] for m in kernel_ms)
+            for i, name in enumerate(("chunk_table", "prep", "recurrence"))}
+    dom = max(("prep", "recurrence"), key=lambda n: k_us[n])
+    dom_flops = T * P["Hv"] * (FLOPS_RECURRENCE if dom == "recurrence" else FLOPS_PREP)
+    achieved_tf = dom_flops / (k_us[dom] / 1e6) / 1e12
+    traffic = recorded_traffic(dom)
     pbytes = prefill_bytes(T, P["Hk"], P["Hv"], P["d"])
 
     # ---------------- the same call writing chunk-boundary snapshots ---------
@@ -400,9 +441,14 @@ def run_ours(args, rank, world, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": traffic,
+                     "kernel": dom, "kernel_us": k_us[dom],
                      "peak_kind": f"{peak_kind} bf16 burst",
-                     "flops_per_launch": flops, "algorithmic_bytes": pbytes},
+                     "flops_per_launch": dom_flops,
+                     "whole_prefill": {"flops": flops, "tflops": flops / (ms_local / 1e3) / 1e12,
+                                       "frac": flops / (ms_local / 1e3) / 1e12 / peak_tf,
+                                       "algorithmic_bytes": pbytes}},
+        "kernels_us": {n: {"us": v, "share": v / sum(k_us.values())} for n, v in k_us.items()},
         "e2e": {"value": job_throughput(T, world, e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "decode": {"workload": "64 sequences x 1 token, 16 key / 48 value heads, d=128, "

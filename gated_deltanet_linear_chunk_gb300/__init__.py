@@ -27,7 +27,7 @@ __all__ = [
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
-    "Problem",
+    "gdn_prefill_timing", "gdn_prefill_kernel_ms", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
@@ -107,8 +107,30 @@ def library() -> ctypes.CDLL:
     lib.gdn_verify_step.argtypes = [PP, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int32, P, P, P]
     lib.gdn_chunk_prefill_device_status.restype = ctypes.c_int
     lib.gdn_chunk_prefill_device_status.argtypes = [P, P]
+    lib.gdn_prefill_timing.restype = ctypes.c_int
+    lib.gdn_prefill_timing.argtypes = [ctypes.c_int32]
+    lib.gdn_prefill_kernel_ms.restype = ctypes.c_int
+    lib.gdn_prefill_kernel_ms.argtypes = [P]
     _lib = lib
     return lib
+
+
+def gdn_prefill_timing(enable: bool) -> None:
+    """Turns per-kernel event timing of the tensor-core prefill on or off (see
+    ``gdn_prefill_timing`` in include/gdn.h)."""
+    rc = library().gdn_prefill_timing(1 if enable else 0)
+    if rc != 0:
+        raise GDNError(rc, "gdn_prefill_timing")
+
+
+def gdn_prefill_kernel_ms() -> Tuple[float, float, float]:
+    """(chunk table, prep, recurrence) durations in ms of the last prefill
+    recorded while timing was on; waits for its events."""
+    ms = (ctypes.c_float * 3)()
+    rc = library().gdn_prefill_kernel_ms(ctypes.cast(ms, ctypes.c_void_p))
+    if rc != 0:
+        raise GDNError(rc, "gdn_prefill_kernel_ms")
+    return float(ms[0]), float(ms[1]), float(ms[2])
 
 
 def gdn_status_string(code: int) -> str:

@@ -183,6 +183,13 @@ GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace,
     return GDN_ERR_CUDA;
 }
 
+GDN_API gdn_status gdn_prefill_timing(int32_t enable) { return gdn::prefill_timing(enable != 0); }
+
+GDN_API gdn_status gdn_prefill_kernel_ms(float *ms) {
+    if (!ms) return GDN_ERR_INVALID_ARG;
+    return gdn::prefill_kernel_ms(ms);
+}
+
 GDN_API const char *gdn_status_string(gdn_status status) {
     switch (status) {
         case GDN_OK: return "GDN_OK";

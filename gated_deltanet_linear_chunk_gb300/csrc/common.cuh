@@ -60,6 +60,10 @@ size_t prefill_tc_workspace_size(const gdn_problem &p);
 bool prefill_tc_supported(const gdn_problem &p);
 // snaps: fp32 [slots, Hv, dv, dk] or nullptr: the state after every
 // snap_stride-th chunk and after the last chunk of every sequence.
+// Per-kernel timing of the tensor-core prefill (events around its launches).
+gdn_status prefill_timing(bool enable);
+gdn_status prefill_kernel_ms(float *ms);
+
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, const int32_t *cu_seqlens,
                              const float *h0, void *out, float *hT, float *snaps,

@@ -108,6 +108,7 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
     __shared__ int s_carry, s_carry2;
     __shared__ int s_bad;
     const int tid = threadIdx.x;
+    griddep_launch_dependents();  // prep may be scheduled; it waits for this grid
     if (tid == 0) {
         s_carry = 0;
         s_carry2 = 0;
@@ -289,6 +290,11 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ch = blockIdx.x, hk = blockIdx.y;
+    // Launched as a programmatic dependent of the chunk table kernel: let the
+    // recurrence kernel be scheduled once all of this grid is placed, then
+    // wait for the table.
+    griddep_launch_dependents();
+    griddep_wait();
     if (ch >= chunk_off[N]) return;
     const int4 e = table[ch];
     const int tok0 = e.y, L = e.z;
@@ -729,6 +735,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    griddep_wait();  // a programmatic dependent of prep: wait for its slots
     const int n = order[blockIdx.x / Hv], h = blockIdx.x % Hv;
     const int hk = h / (Hv / Hk);
     const int c_begin = chunk_off[n], nc = chunk_off[n + 1] - c_begin;
@@ -1155,7 +1162,51 @@ bool encode_states(CUtensorMap *map, float *base, int64_t planes) {
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch configuration with programmatic stream serialization (the kernel may
+// be scheduled before the previous one in the stream completes; it calls
+// griddep_wait before touching that kernel's output); `attr` must outlive
+// the launch call.
+cudaLaunchConfig_t pdl_config(dim3 grid, unsigned threads, size_t smem, cudaStream_t stream,
+                              bool pdl, cudaLaunchAttribute *attr) {
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cfg;
+}
+
+// Timing events (see gdn_prefill_timing): before the chunk table, after it,
+// after prep, after the recurrence.
+cudaEvent_t g_tev[4] = {};
+bool g_timing = false, g_timed = false;
+
+void time_mark(int i, cudaStream_t s) {
+    if (g_timing) cudaEventRecord(g_tev[i], s);
+}
+
 }  // namespace
+
+gdn_status prefill_timing(bool enable) {
+    if (enable && !g_tev[0]) {
+        for (auto &e : g_tev)
+            if (cudaEventCreate(&e) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    g_timing = enable;
+    return GDN_OK;
+}
+
+gdn_status prefill_kernel_ms(float *ms) {
+    if (!g_timed) return GDN_ERR_INVALID_ARG;
+    if (cudaEventSynchronize(g_tev[3]) != cudaSuccess) return GDN_ERR_CUDA;
+    for (int i = 0; i < 3; ++i)
+        if (cudaEventElapsedTime(&ms[i], g_tev[i], g_tev[i + 1]) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
 
 size_t prefill_tc_workspace_size(const gdn_problem &p) { return ws_layout(p).total; }
 
@@ -1196,22 +1247,31 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         memset(&to, 0, sizeof(to));
     }
 
+    // The prep and recurrence launches overlap their predecessor's tail
+    // (programmatic dependent launch), except while per-kernel timing records
+    // events between them.
+    const bool pdl = !g_timing;
+    time_mark(0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, p.num_seqs, p.total_tokens, w.max_chunks,
                                                     snaps ? snap_stride : 0, err, chunk_off,
                                                     snap_off, order, table);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    time_mark(1, stream);
 
     if (p.total_tokens > 0) {
         const size_t smem = sizeof(PrepSmem) + 1024;
         if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return GDN_ERR_CUDA;
-        dim3 grid((unsigned)w.max_chunks, p.num_k_heads);
-        gdn_prep_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, g, beta, chunk_off, table, slots,
-                                                          gl, err, p.num_seqs, p.num_k_heads,
-                                                          p.num_v_heads);
-        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+        cudaLaunchAttribute attr;
+        const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)w.max_chunks, p.num_k_heads),
+                                                  kThreads, smem, stream, pdl, &attr);
+        if (cudaLaunchKernelEx(&cfg, gdn_prep_kernel, tq, tk, g, beta, chunk_off,
+                               (const int4 *)table, slots, gl, err, p.num_seqs, p.num_k_heads,
+                               p.num_v_heads) != cudaSuccess)
+            return GDN_ERR_CUDA;
     }
+    time_mark(2, stream);
     CUtensorMap ts = to;
     if (snaps && !encode_states(&ts, snaps,
                                 prefill_tc_snapshot_slots(p, snap_stride) * p.num_v_heads))
@@ -1221,10 +1281,18 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     if (cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
-    chain<<<(unsigned)p.num_seqs * p.num_v_heads, kChainThreads, smem, stream>>>(
-        tk, tv, to, ts, chunk_off, order, table, slots, gl, h0, static_cast<__nv_bfloat16 *>(out), hT,
-        snaps, snaps ? snap_stride : 1, snap_off, err, p.num_seqs, p.num_k_heads, p.num_v_heads);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    cudaLaunchAttribute attr;
+    const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)p.num_seqs * p.num_v_heads),
+                                              kChainThreads, smem, stream, pdl, &attr);
+    if (cudaLaunchKernelEx(&cfg, chain, tk, tv, to, ts, (const int *)chunk_off,
+                           (const int *)order, (const int4 *)table, (const uint8_t *)slots,
+                           (const float *)gl, h0, static_cast<__nv_bfloat16 *>(out), hT, snaps,
+                           snaps ? snap_stride : 1, (const int *)snap_off, err, p.num_seqs,
+                           p.num_k_heads, p.num_v_heads) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    time_mark(3, stream);
+    if (g_timing) g_timed = true;
+    return GDN_OK;
 }
 
 }  // namespace gdn

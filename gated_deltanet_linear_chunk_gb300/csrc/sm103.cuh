@@ -131,6 +131,15 @@ __device__ __forceinline__ bool warp_wait_spin(uint64_t *bar, uint32_t parity, v
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) be scheduled
+// once every CTA of this grid has called it or exited; wait blocks until the
+// grids this one depends on have completed and their writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Bounded wait with the least code, for kernels whose loops have to fit the
 // instruction cache (the recurrence kernel: every inlined wait there is code
 // that its warps' loops share the cache with).  Every lane polls, so there is

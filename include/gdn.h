@@ -270,6 +270,24 @@ GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_problem *problem,
  */
 GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace, gdn_stream_t stream);
 
+/*
+ * Per-kernel timing of the tensor-core prefill (bf16, d = 128), for
+ * measurement; off by default and free when off.  While on, each such prefill
+ * records CUDA events on its stream before and after its three launches
+ * (chunk table, prep, recurrence); gdn_prefill_kernel_ms waits for the last
+ * recorded call's events and returns the three durations.  The events belong
+ * to the device current when timing was first enabled; one caller at a time.
+ *   gdn_prefill_timing(enable): nonzero creates the events (once) and turns
+ *       recording on, 0 turns it off.  GDN_ERR_CUDA if the events cannot be
+ *       created.
+ *   gdn_prefill_kernel_ms(ms): ms[0], ms[1], ms[2] = chunk table, prep and
+ *       recurrence of the last recorded call, in milliseconds.
+ *       GDN_ERR_INVALID_ARG if ms is NULL or no call was recorded,
+ *       GDN_ERR_CUDA if the events cannot be read.
+ */
+GDN_API gdn_status gdn_prefill_timing(int32_t enable);
+GDN_API gdn_status gdn_prefill_kernel_ms(float *ms);
+
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);
 

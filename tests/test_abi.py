@@ -174,3 +174,11 @@ def test_binding_rejects_cpu_tensors(lib):
     with pytest.raises(ValueError):
         gdn.gdn_decode_step(x, x, x, torch.zeros(4, 1), torch.zeros(4, 1),
                             torch.zeros(4, 1, 128, 128))
+
+
+def test_prefill_timing_argument_errors(lib):
+    """Off needs no device; reading times needs a recorded call and a buffer."""
+    assert lib.gdn_prefill_timing(0) == OK
+    assert lib.gdn_prefill_kernel_ms(None) == INVALID
+    buf = (ctypes.c_float * 3)()
+    assert lib.gdn_prefill_kernel_ms(ctypes.cast(buf, ctypes.c_void_p)) == INVALID
