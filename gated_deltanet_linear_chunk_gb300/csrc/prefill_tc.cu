@@ -998,7 +998,8 @@ if (elect_one_sync()) {
                     const float d0 = __uint_as_float(r[2 * i]), d1 = __uint_as_float(r[2 * i + 1]);
                     const float2 dv = *reinterpret_cast<const float2 *>(dec + 32 * h2 + 2 * i);
                     pd[i] = pack_bf16(d0, d1);
-                    ps[i] = pack_bf16(d0 * dv.x * inv, d1 * dv.y * inv);
+                    const float2 pr = mul2(mul2(make_float2(d0, d1), dv), make_float2(inv, inv));
+                    ps[i] = pack_bf16(pr.x, pr.y);
                 }
                 tmem_st16(tmem + lane_base + kColDT + 16 * h2, pd);
                 tmem_st16(tmem + lane_base + kColDTS + 16 * h2, ps);
@@ -1026,8 +1027,11 @@ if (elect_one_sync()) {
                     // -S0 of chunk c + 1 for the MMAs (the hand-off).
                     uint32_t r[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = pack_bf16(-sigma * x[2 * i], -sigma * x[2 * i + 1]);
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 pr = mul2(make_float2(x[2 * i], x[2 * i + 1]),
+                                               make_float2(-sigma, -sigma));
+                        r[i] = pack_bf16(pr.x, pr.y);
+                    }
                     tmem_st32(t_ns + 64 * ((c + 1) & 1), r);
                     tmem_st_wait();
                     tc_fence_before();

@@ -140,6 +140,14 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Two fp32 products in one instruction (IEEE round to nearest per lane).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 // Bounded wait with the least code, for kernels whose loops have to fit the
 // instruction cache (the recurrence kernel: every inlined wait there is code
 // that its warps' loops share the cache with).  Every lane polls, so there is
