@@ -193,9 +193,10 @@ def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> flo
     return units_per_rank * world / max_seconds
 
 
-def oracle_sample_prefill(tokens: int, num_threads: int = 0):
+def oracle_sample_prefill(tokens: int, num_threads: int = 0, min_seconds: float = 0.0):
     """Times the fp64 oracle on the first ``tokens`` tokens of the prefill
-    workload, all 48 value heads.  Returns (tokens/s/layer, seconds, threads)."""
+    workload, all 48 value heads, repeated until ``min_seconds`` have passed
+    (at least once).  Returns (tokens/s/layer, seconds, threads, repeats)."""
     import torch
 
     import oracle
@@ -204,10 +205,15 @@ def oracle_sample_prefill(tokens: int, num_threads: int = 0):
                               PREFILL["d"], dtype=torch.bfloat16, seed=0)
     arrs = [x.double().numpy() for x in (p.q, p.k, p.v, p.g, p.beta)]
     threads = num_threads or oracle.max_threads()
+    reps = 0
     t0 = time.perf_counter()
-    oracle.prefill(*arrs, p.cu_seqlens.numpy(), None, num_threads=threads)
-    dt = time.perf_counter() - t0
-    return tokens / dt, dt, min(threads, PREFILL["Hv"])
+    while True:
+        oracle.prefill(*arrs, p.cu_seqlens.numpy(), None, num_threads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or reps >= 200:
+            break
+    return tokens * reps / dt, dt, min(threads, PREFILL["Hv"]), reps
 
 
 def run_reference(args, rank):
@@ -216,11 +222,11 @@ def run_reference(args, rank):
         return
     tokens = args.ref_tokens
     for _ in range(args.warmup):
-        oracle_sample_prefill(max(16, tokens // 8))
+        oracle_sample_prefill(max(16, tokens // 8))[0]
     vals, secs = [], []
     threads = 1
     for _ in range(args.steps):
-        v, s, threads = oracle_sample_prefill(tokens)
+        v, s, threads, _ = oracle_sample_prefill(tokens)
         vals.append(v)
         secs.append(s)
     value = statistics.median(vals)
@@ -308,10 +314,15 @@ def run_ours(args, rank, world, local):
     # its mean launch time in the timed steps.
     k_us = {name: 1e3 * statistics.mean(m[i] for m in kernel_ms)
             for i, name in enumerate(("chunk_table", "prep", "recurrence"))}
+    k_flops = {"recurrence": T * P["Hv"] * FLOPS_RECURRENCE, "prep": T * P["Hv"] * FLOPS_PREP}
+    per_kernel = {n: {"us": k_us[n], "flops_per_launch": k_flops[n],
+                      "achieved": k_flops[n] / (k_us[n] / 1e6) / 1e12,
+                      "frac": k_flops[n] / (k_us[n] / 1e6) / 1e12 / peak_tf,
+                      "traffic": recorded_traffic(n)} for n in k_flops}
     dom = max(("prep", "recurrence"), key=lambda n: k_us[n])
-    dom_flops = T * P["Hv"] * (FLOPS_RECURRENCE if dom == "recurrence" else FLOPS_PREP)
-    achieved_tf = dom_flops / (k_us[dom] / 1e6) / 1e12
-    traffic = recorded_traffic(dom)
+    dom_flops = k_flops[dom]
+    achieved_tf = per_kernel[dom]["achieved"]
+    traffic = per_kernel[dom]["traffic"]
     pbytes = prefill_bytes(T, P["Hk"], P["Hv"], P["d"])
 
     # ---------------- the same call writing chunk-boundary snapshots ---------
@@ -444,7 +455,7 @@ def run_ours(args, rank, world, local):
                      "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": traffic,
                      "kernel": dom, "kernel_us": k_us[dom],
                      "peak_kind": f"{peak_kind} bf16 burst",
-                     "flops_per_launch": dom_flops,
+                     "flops_per_launch": dom_flops, "per_kernel": per_kernel,
                      "whole_prefill": {"flops": flops, "tflops": flops / (ms_local / 1e3) / 1e12,
                                        "frac": flops / (ms_local / 1e3) / 1e12 / peak_tf,
                                        "algorithmic_bytes": pbytes}},
@@ -468,11 +479,11 @@ def run_ours(args, rank, world, local):
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, s, threads = oracle_sample_prefill(args.ref_tokens)
+        v, s, threads, reps = oracle_sample_prefill(args.ref_tokens, min_seconds=10.0)
         line["cpu_baseline"] = {
             "value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {args.ref_tokens} of the 4000 tokens, all 48 value heads "
-                      f"(fp64 token recurrence, {s:.1f} s wall)"}
+            "sample": f"first {args.ref_tokens} of the 4000 tokens, all 48 value heads, "
+                      f"{reps} repeats (fp64 token recurrence, {s:.1f} s wall)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
