@@ -27,7 +27,8 @@ __all__ = [
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
-    "gdn_prefill_timing", "gdn_prefill_kernel_ms", "Problem",
+    "gdn_prefill_timing", "gdn_prefill_kernel_ms", "gdn_chunk_prefill_scan",
+    "gdn_chunk_prefill_scan_workspace_size", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
 
@@ -107,6 +108,10 @@ def library() -> ctypes.CDLL:
     lib.gdn_verify_step.argtypes = [PP, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int32, P, P, P]
     lib.gdn_chunk_prefill_device_status.restype = ctypes.c_int
     lib.gdn_chunk_prefill_device_status.argtypes = [P, P]
+    lib.gdn_chunk_prefill_scan_workspace_size.restype = ctypes.c_size_t
+    lib.gdn_chunk_prefill_scan_workspace_size.argtypes = [PP, ctypes.c_int32]
+    lib.gdn_chunk_prefill_scan.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_scan.argtypes = [PP, ctypes.c_int32] + [P] * 10
     lib.gdn_prefill_timing.restype = ctypes.c_int
     lib.gdn_prefill_timing.argtypes = [ctypes.c_int32]
     lib.gdn_prefill_kernel_ms.restype = ctypes.c_int
@@ -218,7 +223,7 @@ def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 
 def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, output_final_state,
-             workspace, stream, snapshots, snapshot_chunks):
+             workspace, stream, snapshots, snapshot_chunks, scan_group=None):
     """Checks, workspace and dispatch of both prefill entry points
     (``snapshots``: _NO_SNAPSHOTS, None to allocate, or a tensor)."""
     T, Hk, dk = q.shape
@@ -244,10 +249,23 @@ def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, outp
         _check(final_state, "final_state", torch.float32, (N, Hv, dv, dk))
     lib = library()
     p = make_problem(N, T, Hk, Hv, dk, dv, dt)
-    need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
+    if scan_group is not None:
+        need = int(lib.gdn_chunk_prefill_scan_workspace_size(ctypes.byref(p), scan_group))
+        if need == 0 and N > 0:
+            raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_prefill_scan")
+    else:
+        need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
     if workspace is None:
         workspace = _workspace(q.device, need)
     p = make_problem(N, T, Hk, Hv, dk, dv, dt, workspace)
+    if scan_group is not None:
+        rc = lib.gdn_chunk_prefill_scan(ctypes.byref(p), scan_group, _ptr(q), _ptr(k), _ptr(v),
+                                        _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                        _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                        _stream(stream))
+        if rc != 0:
+            raise GDNError(rc, "gdn_chunk_prefill_scan")
+        return out, final_state
     if snapshots is _NO_SNAPSHOTS:
         rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                    _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state), _ptr(out),
@@ -286,6 +304,31 @@ def gdn_chunk_prefill_snapshots(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
     fp32); sequence n's snapshot i is slot sum_{m<n} ceil(chunks_m / s) + i."""
     return _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
                     output_final_state, workspace, stream, snapshots, snapshot_chunks)
+
+
+def gdn_chunk_prefill_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           g: torch.Tensor, beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                           initial_state: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None,
+                           final_state: Optional[torch.Tensor] = None,
+                           output_final_state: bool = False, chunks_per_group: int = 0,
+                           workspace: Optional[torch.Tensor] = None, stream=None):
+    """``gdn_chunk_prefill`` with the chunk recurrence as a chunk-parallel scan
+    over groups of ``chunks_per_group`` chunks (0: chosen to fill the SMs);
+    see ``gdn_chunk_prefill_scan`` in include/gdn.h.  Returns (out,
+    final_state)."""
+    return _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                    output_final_state, workspace, stream, _NO_SNAPSHOTS, 0,
+                    scan_group=int(chunks_per_group))
+
+
+def gdn_chunk_prefill_scan_workspace_size(N: int, T: int, Hk: int, Hv: int, dk: int, dv: int,
+                                          chunks_per_group: int = 0,
+                                          dtype=torch.bfloat16) -> int:
+    """Workspace bytes of ``gdn_chunk_prefill_scan`` (0 if unsupported)."""
+    p = make_problem(N, T, Hk, Hv, dk, dv, dtype)
+    return int(library().gdn_chunk_prefill_scan_workspace_size(ctypes.byref(p),
+                                                                 chunks_per_group))
 
 
 def gdn_chunk_prefill_device_status(workspace: Optional[torch.Tensor] = None,

@@ -56,11 +56,12 @@ namespace {
 gdn_status prefill_impl(const gdn_problem *problem, const void *q, const void *k, const void *v,
                         const float *g, const float *beta, const int32_t *cu_seqlens,
                         const float *initial_state, void *out, float *final_state, float *snaps,
-                        int snap_stride, bool want_snaps, gdn_stream_t stream) {
+                        int snap_stride, bool want_snaps, gdn_stream_t stream,
+                        int scan_group = -1) {
     const gdn_status st = check_problem(problem);
     if (st != GDN_OK) return st;
     const gdn_problem &p = *problem;
-    if (want_snaps && !prefill_tc_supported(p)) return GDN_ERR_UNSUPPORTED;
+    if ((want_snaps || scan_group >= 0) && !prefill_tc_supported(p)) return GDN_ERR_UNSUPPORTED;
     if (p.num_seqs == 0) return p.total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
     if (p.total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
@@ -70,12 +71,17 @@ gdn_status prefill_impl(const gdn_problem *problem, const void *q, const void *k
     if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return GDN_ERR_MISALIGNED;
     if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
     if (snaps && (snaps == initial_state || snaps == final_state)) return GDN_ERR_INVALID_ARG;
-    const size_t need = gdn_chunk_prefill_workspace_size(problem);
+    if (scan_group == 0) scan_group = prefill_scan_auto_group(p);
+    const size_t need = scan_group > 0 ? prefill_scan_workspace_size(p, scan_group)
+                                       : gdn_chunk_prefill_workspace_size(problem);
     if (need > 0) {
         if (!p.workspace || p.workspace_bytes < need) return GDN_ERR_WORKSPACE;
         if (!aligned16(p.workspace)) return GDN_ERR_WORKSPACE;
     }
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    if (scan_group > 0)
+        return launch_prefill_scan(p, scan_group, q, k, v, g, beta, cu_seqlens, initial_state, out,
+                                   final_state, st_);
     if (prefill_tc_supported(p))
         return launch_prefill_tc(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
                                  snaps, snap_stride, st_);
@@ -111,6 +117,25 @@ GDN_API gdn_status gdn_chunk_prefill_snapshots(const gdn_problem *problem, const
                                                int32_t snapshot_chunks, gdn_stream_t stream) {
     return prefill_impl(problem, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
                         snapshots, snapshot_chunks, true, stream);
+}
+
+GDN_API size_t gdn_chunk_prefill_scan_workspace_size(const gdn_problem *problem,
+                                                    int32_t chunks_per_group) {
+    if (check_problem(problem) != GDN_OK || !prefill_tc_supported(*problem) ||
+        chunks_per_group < 0)
+        return 0;
+    const int L = chunks_per_group > 0 ? chunks_per_group : prefill_scan_auto_group(*problem);
+    return prefill_scan_workspace_size(*problem, L);
+}
+
+GDN_API gdn_status gdn_chunk_prefill_scan(const gdn_problem *problem, int32_t chunks_per_group,
+                                          const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta,
+                                          const int32_t *cu_seqlens, const float *initial_state,
+                                          void *out, float *final_state, gdn_stream_t stream) {
+    if (chunks_per_group < 0) return GDN_ERR_INVALID_ARG;
+    return prefill_impl(problem, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                        nullptr, 1, false, stream, chunks_per_group);
 }
 
 GDN_API gdn_status gdn_decode_step(const gdn_problem *problem, const void *q, const void *k,

@@ -60,6 +60,14 @@ size_t prefill_tc_workspace_size(const gdn_problem &p);
 bool prefill_tc_supported(const gdn_problem &p);
 // snaps: fp32 [slots, Hv, dv, dk] or nullptr: the state after every
 // snap_stride-th chunk and after the last chunk of every sequence.
+// Chunk-parallel scan of the tensor-core prefill (chunks_per_group >= 1).
+size_t prefill_scan_workspace_size(const gdn_problem &p, int chunks_per_group);
+int prefill_scan_auto_group(const gdn_problem &p);
+gdn_status launch_prefill_scan(const gdn_problem &p, int chunks_per_group, const void *q,
+                               const void *k, const void *v, const float *g, const float *beta,
+                               const int32_t *cu, const float *h0, void *out, float *hT,
+                               cudaStream_t stream);
+
 // Per-kernel timing of the tensor-core prefill (events around its launches).
 gdn_status prefill_timing(bool enable);
 gdn_status prefill_kernel_ms(float *ms);

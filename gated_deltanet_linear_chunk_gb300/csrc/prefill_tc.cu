@@ -42,6 +42,7 @@
 // last real token.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -721,7 +722,12 @@ __device__ __noinline__ bool store_state_rows(ChainSmem &sm, const CUtensorMap *
 
 // kSnaps: the instantiation that writes chunk-boundary snapshots (a separate
 // instantiation keeps the snapshot code out of the plain kernel's hot loop).
-template <bool kSnaps>
+// kLinear: the instantiation for the chunk-parallel scan that runs the
+// recurrence's linear part alone: the initial state is the identity and U is
+// zero, so the final state is the product of the chunks' transition matrices
+// (the output it writes is not used).  kNoOut: only the final state is
+// wanted (the scan's group passes): no output MMAs, output warps or Q~/P loads.
+template <bool kSnaps, bool kLinear = false, bool kNoOut = false>
 __global__ void __launch_bounds__(kChainThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_s,
@@ -821,15 +827,20 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 // One elected lane issues the stage's copies (per-copy
                 // elections cost code the instruction cache has to hold).
                 if (elect_one_sync()) {
-                    mbar_arrive_expect_tx(bar, kStageBytes);
+                    mbar_arrive_expect_tx(bar, kStageBytes - (kNoOut ? 3 * kTile : 0) -
+                                                   (kLinear ? 3 * kTile : 0));
                     tma_load_3d(st.k, &tm_k, 0, hk, tok0, bar);
                     tma_load_3d(st.k + kTile, &tm_k, 64, hk, tok0, bar);
-                    tma_load_3d(st.v, &tm_v, 0, h, tok0, bar);
-                    tma_load_3d(st.v + kTile, &tm_v, 64, h, tok0, bar);
+                    if (!kLinear) {
+                        tma_load_3d(st.v, &tm_v, 0, h, tok0, bar);
+                        tma_load_3d(st.v + kTile, &tm_v, 64, h, tok0, bar);
+                        bulk_load(st.tb, slot + kSlotTB, kTile, bar);
+                    }
                     bulk_load(st.wt, slot + kSlotWT, 2 * kTile, bar);
-                    bulk_load(st.tb, slot + kSlotTB, kTile, bar);
-                    bulk_load(st.p, slot + kSlotP, kTile, bar);
-                    bulk_load(st.q, slot + kSlotQ, 2 * kTile, bar);
+                    if (!kNoOut) {
+                        bulk_load(st.p, slot + kSlotP, kTile, bar);
+                        bulk_load(st.q, slot + kSlotQ, 2 * kTile, bar);
+                    }
                     bulk_load(st.egdec, slot + kSlotEG, 512, bar);
                 }
                 if (lane == 0) sm.issued = c + 1;
@@ -857,7 +868,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 ChainStage &st = sm.st[s];
                 const uint64_t d_v = smem_desc(smem_u32(st.v), kTile, 1024);
                 const uint64_t d_tb = smem_desc(smem_u32(st.tb), 16, 1024);
-if (elect_one_sync()) {
+if (!kLinear && elect_one_sync()) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_bf16(tmem + kColD, d_v + 128 * k, d_tb + 2 * k, id_u, k > 0);
@@ -884,7 +895,8 @@ if (elect_one_sync()) {
 if (elect_one_sync()) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_bf16_ta(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w, 1);
+                        mma_bf16_ta(tmem + kColD, tmem + ns + 8 * k, d_wt + 128 * k, id_w,
+                                    !kLinear || k > 0);
                     mma_commit(&sm.d_done);
                 }
                 __syncwarp();
@@ -895,9 +907,11 @@ if (elect_one_sync()) {
                 // copy of its code: the issuing warp's loop has to stay small
                 // enough for the instruction cache, or its MMAs issue at
                 // instruction-fetch speed.
-                if (c >= 2 && !warp_wait_lean(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort)) break;
+                if (!kNoOut && c >= 2 &&
+                    !warp_wait_lean(&sm.o_free[c & 1], ((c >> 1) - 1) & 1, &sm.abort))
+                    break;
                 tc_fence_after();
-if (elect_one_sync()) {
+if (!kNoOut && elect_one_sync()) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         mma_bf16_ta(tmem + ob, tmem + ns + 8 * k,
@@ -922,7 +936,7 @@ if (elect_one_sync()) {
                 // O += Delta^T P^T                       [M=128 dv, N=64, K=64 tokens]
 if (elect_one_sync()) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                    for (int k = 0; k < (kNoOut ? 0 : 4); ++k)
                         mma_bf16_ta(tmem + ob, tmem + kColDT + 8 * k, d_p + 2 * k, id_q, 1);
                     mma_commit(&sm.o_done[c & 1]);
                     mma_commit(&sm.empty[s]);
@@ -950,9 +964,13 @@ if (elect_one_sync()) {
             float x[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
-                const float4 v4 = h0 ? *reinterpret_cast<const float4 *>(
-                                           h0 + state_off + (size_t)j * D + 64 * h2 + c)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 v4 = h0 ? *reinterpret_cast<const float4 *>(
+                                     h0 + state_off + (size_t)j * D + 64 * h2 + c)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kLinear) {
+                    const int k0 = 64 * h2 + c;
+                    v4 = make_float4(j == k0, j == k0 + 1, j == k0 + 2, j == k0 + 3);
+                }
                 x[c] = v4.x; x[c + 1] = v4.y; x[c + 2] = v4.z; x[c + 3] = v4.w;
             }
             store_state(t_ns, t_s, x, 1.f);
@@ -1056,7 +1074,7 @@ if (elect_one_sync()) {
         const int hh = q >> 1;                  // dv half of this warp's rows
         const int k8 = lane & 7, d8 = lane >> 3; // stmatrix row and matrix of this lane
 #pragma unroll 1
-        for (int c = 0; c < nc; ++c) {
+        for (int c = 0; c < (kNoOut ? 0 : nc); ++c) {
             const int4 e = table[c_begin + c];
             const int tok0 = e.y, L = e.z;
             if (!warp_wait_lean(&sm.o_done[c & 1], (c >> 1) & 1, &sm.abort)) break;
@@ -1118,6 +1136,157 @@ if (elect_one_sync()) {
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ chunk-parallel scan
+// The chunk step is affine in the state, S_{c+1} = S_c M_c + B_c (with
+// M_c = e^{gamma_L} I - W^T diag(e^{gamma_L - gamma}) K and
+// B_c = U^T diag(e^{gamma_L - gamma}) K), and composes by
+// (M, B) then (M', B') = (M M', B M' + B').  A sequence is cut into groups
+// of L chunks (pseudo-sequences that the prep and recurrence kernels treat
+// like sequences): the recurrence from a zero state gives each group's B,
+// the kLinear recurrence (identity state, U = 0) its M, the combine kernel
+// below carries the state across groups, and a last recurrence pass from
+// each group's initial state writes the outputs.
+
+// One CTA of 1024 threads.  Checks cu_seqlens like the chunk table kernel,
+// then goff[n] = groups before sequence n (G_n = ceil(chunks_n / L), 0 for an
+// empty sequence) and cu2 = the pseudo-sequences' token offsets, padded with
+// T up to n2 + 1 entries.  A malformed cu_seqlens gives cu2[0] = 1, which the
+// chunk table kernel rejects (the whole call is then a no-op).
+__global__ void __launch_bounds__(1024)
+gdn_scan_split_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int L, int n2,
+                      int32_t *__restrict__ cu2, int *__restrict__ goff) {
+    __shared__ int s_scan[1024];
+    __shared__ int s_carry, s_bad;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_carry = 0;
+        s_bad = (cu[0] != 0 || (int64_t)cu[N] != T) ? 1 : 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        int gn = 0;
+        if (n < N) {
+            const int len = cu[n + 1] - cu[n];
+            if (len < 0) s_bad = 1;
+            const int nch = len > 0 ? (len + C - 1) / C : 0;
+            gn = (nch + L - 1) / L;
+        }
+        s_scan[tid] = gn;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {
+            const int x = tid >= off ? s_scan[tid - off] : 0;
+            __syncthreads();
+            s_scan[tid] += x;
+            __syncthreads();
+        }
+        if (n < N) {
+            const int first = s_carry + s_scan[tid] - gn;
+            goff[n] = first;
+            for (int gi = 0; gi < gn && first + gi < n2; ++gi)
+                cu2[first + gi] = cu[n] + C * L * gi;
+        }
+        __syncthreads();
+        if (tid == 1023) s_carry += s_scan[1023];
+        __syncthreads();
+    }
+    const int total = s_carry;
+    if (tid == 0) goff[N] = total;
+    for (int i = total + tid; i <= n2; i += 1024) cu2[i] = (int32_t)T;
+    __syncthreads();
+    if (tid == 0 && (s_bad || total > n2)) cu2[0] = 1;
+}
+
+// Carries the state across the groups of each (sequence, value head):
+// Hbuf[group] = the state entering the group, S <- S M_g + B_g, and the
+// final state into hT.  Rows are independent, so CTA y owns rows
+// 16y..16y+15 (grid N Hv x 8, 128 threads).  Warp w computes columns
+// 32w..32w+31; lane l a 4 x 4 tile (rows 4 (l / 8).., columns 32w + 4 (l % 8)..),
+// reading S transposed and M from shared memory (two 16-byte loads per 16
+// FMAs).  The next group's M is fetched with cp.async into the other buffer
+// while this one is used.  fp32 throughout.  Does nothing when the chunk
+// table kernel rejected cu_seqlens.
+constexpr int kCombineRows = 16;
+constexpr int kCombineThreads = 128;
+
+__device__ __forceinline__ void combine_fetch_m(float *dst, const float *src, int tid) {
+    const uint32_t d = smem_u32(dst);
+#pragma unroll 4
+    for (int i = tid; i < D * D / 4; i += kCombineThreads)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16 * i),
+                     "l"(src + 4 * i)
+                     : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kCombineThreads)
+gdn_scan_combine_kernel(const int *__restrict__ goff, const float *__restrict__ h0,
+                        const float *__restrict__ mbuf, const float *__restrict__ bbuf,
+                        float *__restrict__ hbuf, float *__restrict__ hT,
+                        const int *__restrict__ err, int Hv) {
+    extern __shared__ __align__(16) float cm_smem[];
+    float *ms = cm_smem;                   // M of two groups [2][128][128]
+    float *st = cm_smem + 2 * D * D;       // S transposed [128 k][16 rows]
+    if (*err != kErrNone) return;
+    const int n = blockIdx.x / Hv, h = blockIdx.x % Hv;
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int r0 = 4 * (l >> 3), c0 = 32 * w + 4 * (l & 7);
+    const int row0 = kCombineRows * blockIdx.y + r0;
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 x = h0 ? *reinterpret_cast<const float4 *>(
+                                  h0 + ((size_t)(n * Hv + h) * D + row0 + i) * D + c0)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        s[i][0] = x.x; s[i][1] = x.y; s[i][2] = x.z; s[i][3] = x.w;
+    }
+    const int g_begin = goff[n], g_end = goff[n + 1];
+    if (g_begin < g_end) combine_fetch_m(ms, mbuf + (size_t)(g_begin * Hv + h) * D * D, tid);
+#pragma unroll 1
+    for (int gi = g_begin; gi < g_end; ++gi) {
+        const size_t plane = (size_t)gi * Hv + h;
+        const float *mcur = ms + ((gi - g_begin) & 1) * D * D;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            *reinterpret_cast<float4 *>(hbuf + (plane * D + row0 + i) * D + c0) =
+                make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) st[(c0 + jj) * kCombineRows + r0 + i] = s[i][jj];
+        }
+        if (gi + 1 < g_end) {
+            combine_fetch_m(ms + ((gi + 1 - g_begin) & 1) * D * D, mbuf + (plane + Hv) * D * D,
+                            tid);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 b = *reinterpret_cast<const float4 *>(
+                bbuf + (plane * D + row0 + i) * D + c0);
+            s[i][0] = b.x; s[i][1] = b.y; s[i][2] = b.z; s[i][3] = b.w;
+        }
+#pragma unroll 4
+        for (int k = 0; k < D; ++k) {
+            const float4 a = *reinterpret_cast<const float4 *>(st + k * kCombineRows + r0);
+            const float4 m = *reinterpret_cast<const float4 *>(mcur + k * D + c0);
+            const float av[4] = {a.x, a.y, a.z, a.w}, mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) s[i][jj] = fmaf(av[i], mv[jj], s[i][jj]);
+        }
+        __syncthreads();
+    }
+    if (hT) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4 *>(hT + ((size_t)(n * Hv + h) * D + row0 + i) * D + c0) =
+                make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -1222,46 +1391,49 @@ bool prefill_tc_supported(const gdn_problem &p) {
     return p.qkv_dtype == GDN_BF16 && p.head_dim_k == D && p.head_dim_v == D;
 }
 
-gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
-                             const float *g, const float *beta, const int32_t *cu,
-                             const float *h0, void *out, float *hT, float *snaps,
-                             int snap_stride, cudaStream_t stream) {
-    if (p.num_seqs == 0) return GDN_OK;
-    const WsLayout w = ws_layout(p);
-    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
-    int *err = reinterpret_cast<int *>(ws + w.hdr);
-    int *chunk_off = reinterpret_cast<int *>(ws + w.chunk_off);
-    int *snap_off = reinterpret_cast<int *>(ws + w.snap_off);
-    int *order = reinterpret_cast<int *>(ws + w.order);
-    int4 *table = reinterpret_cast<int4 *>(ws + w.table);
-    float *gl = reinterpret_cast<float *>(ws + w.gl);
-    uint8_t *slots = ws + w.tiles;
+namespace {
 
+struct TcMaps {
     CUtensorMap tq, tk, tv, to;
-    if (p.total_tokens > 0) {
-        if (!encode_thd(&tq, q, p.total_tokens, p.num_k_heads) ||
-            !encode_thd(&tk, k, p.total_tokens, p.num_k_heads) ||
-            !encode_thd(&tv, v, p.total_tokens, p.num_v_heads) ||
-            !encode_thd(&to, out, p.total_tokens, p.num_v_heads))
-            return GDN_ERR_CUDA;
-    } else {
-        memset(&tq, 0, sizeof(tq));
-        memset(&tk, 0, sizeof(tk));
-        memset(&tv, 0, sizeof(tv));
-        memset(&to, 0, sizeof(to));
-    }
+};
 
-    // The prep and recurrence launches overlap their predecessor's tail
-    // (programmatic dependent launch), except while per-kernel timing records
-    // events between them.
-    const bool pdl = !g_timing;
+struct TcPtrs {
+    int *err, *chunk_off, *snap_off, *order;
+    int4 *table;
+    float *gl;
+    uint8_t *slots;
+};
+
+TcPtrs tc_ptrs(const WsLayout &w, void *workspace) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    return {reinterpret_cast<int *>(ws + w.hdr), reinterpret_cast<int *>(ws + w.chunk_off),
+            reinterpret_cast<int *>(ws + w.snap_off), reinterpret_cast<int *>(ws + w.order),
+            reinterpret_cast<int4 *>(ws + w.table), reinterpret_cast<float *>(ws + w.gl),
+            ws + w.tiles};
+}
+
+bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void *v, void *out,
+                 TcMaps &m) {
+    if (p.total_tokens == 0) {
+        memset(&m, 0, sizeof(m));
+        return true;
+    }
+    return encode_thd(&m.tq, q, p.total_tokens, p.num_k_heads) &&
+           encode_thd(&m.tk, k, p.total_tokens, p.num_k_heads) &&
+           encode_thd(&m.tv, v, p.total_tokens, p.num_v_heads) &&
+           encode_thd(&m.to, out, p.total_tokens, p.num_v_heads);
+}
+
+// Chunk table, then prep (a programmatic dependent of the table kernel).
+gdn_status launch_table_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
+                             const TcMaps &m, const float *g, const float *beta,
+                             const int32_t *cu, int snap_stride, cudaStream_t stream, bool pdl) {
     time_mark(0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, p.num_seqs, p.total_tokens, w.max_chunks,
-                                                    snaps ? snap_stride : 0, err, chunk_off,
-                                                    snap_off, order, table);
+                                                    snap_stride, t.err, t.chunk_off, t.snap_off,
+                                                    t.order, t.table);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     time_mark(1, stream);
-
     if (p.total_tokens > 0) {
         const size_t smem = sizeof(PrepSmem) + 1024;
         if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1270,33 +1442,156 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         cudaLaunchAttribute attr;
         const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)w.max_chunks, p.num_k_heads),
                                                   kThreads, smem, stream, pdl, &attr);
-        if (cudaLaunchKernelEx(&cfg, gdn_prep_kernel, tq, tk, g, beta, chunk_off,
-                               (const int4 *)table, slots, gl, err, p.num_seqs, p.num_k_heads,
-                               p.num_v_heads) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, gdn_prep_kernel, m.tq, m.tk, g, beta,
+                               (const int *)t.chunk_off, (const int4 *)t.table, t.slots, t.gl,
+                               t.err, p.num_seqs, p.num_k_heads, p.num_v_heads) != cudaSuccess)
             return GDN_ERR_CUDA;
     }
     time_mark(2, stream);
-    CUtensorMap ts = to;
-    if (snaps && !encode_states(&ts, snaps,
-                                prefill_tc_snapshot_slots(p, snap_stride) * p.num_v_heads))
-        return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+// The recurrence kernel over the chunk table of `p` (a programmatic
+// dependent of the kernel before it when `pdl`).
+template <bool kSnaps, bool kLinear, bool kNoOut = false>
+gdn_status launch_chain(const gdn_problem &p, const TcPtrs &t, const TcMaps &m,
+                        const CUtensorMap &ts, const float *h0, void *out, float *hT,
+                        float *snaps, int snap_stride, cudaStream_t stream, bool pdl) {
     const size_t smem = sizeof(ChainSmem) + 1024;
-    auto chain = snaps ? gdn_chain_kernel<true> : gdn_chain_kernel<false>;
+    auto chain = gdn_chain_kernel<kSnaps, kLinear, kNoOut>;
     if (cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
     cudaLaunchAttribute attr;
     const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)p.num_seqs * p.num_v_heads),
                                               kChainThreads, smem, stream, pdl, &attr);
-    if (cudaLaunchKernelEx(&cfg, chain, tk, tv, to, ts, (const int *)chunk_off,
-                           (const int *)order, (const int4 *)table, (const uint8_t *)slots,
-                           (const float *)gl, h0, static_cast<__nv_bfloat16 *>(out), hT, snaps,
-                           snaps ? snap_stride : 1, (const int *)snap_off, err, p.num_seqs,
+    if (cudaLaunchKernelEx(&cfg, chain, m.tk, m.tv, m.to, ts, (const int *)t.chunk_off,
+                           (const int *)t.order, (const int4 *)t.table, (const uint8_t *)t.slots,
+                           (const float *)t.gl, h0, static_cast<__nv_bfloat16 *>(out), hT, snaps,
+                           snap_stride, (const int *)t.snap_off, t.err, p.num_seqs,
                            p.num_k_heads, p.num_v_heads) != cudaSuccess)
         return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
+                             const float *g, const float *beta, const int32_t *cu,
+                             const float *h0, void *out, float *hT, float *snaps,
+                             int snap_stride, cudaStream_t stream) {
+    if (p.num_seqs == 0) return GDN_OK;
+    const WsLayout w = ws_layout(p);
+    const TcPtrs t = tc_ptrs(w, p.workspace);
+    TcMaps m;
+    if (!encode_maps(p, q, k, v, out, m)) return GDN_ERR_CUDA;
+    // The prep and recurrence launches overlap their predecessor's tail
+    // (programmatic dependent launch), except while per-kernel timing records
+    // events between them.
+    const bool pdl = !g_timing;
+    gdn_status st = launch_table_prep(p, w, t, m, g, beta, cu, snaps ? snap_stride : 0, stream, pdl);
+    if (st != GDN_OK) return st;
+    CUtensorMap ts = m.to;
+    if (snaps && !encode_states(&ts, snaps,
+                                prefill_tc_snapshot_slots(p, snap_stride) * p.num_v_heads))
+        return GDN_ERR_CUDA;
+    st = snaps ? launch_chain<true, false>(p, t, m, ts, h0, out, hT, snaps, snap_stride, stream, pdl)
+               : launch_chain<false, false>(p, t, m, ts, h0, out, hT, nullptr, 1, stream, pdl);
+    if (st != GDN_OK) return st;
     time_mark(3, stream);
     if (g_timing) g_timed = true;
     return GDN_OK;
+}
+
+namespace {
+
+// Workspace of the chunk-parallel scan: the prefill workspace of the problem
+// whose sequences are the groups (n2 of them at most), then the groups'
+// token offsets, the group offsets of each sequence, and the groups' M, B and
+// initial states ([n2 Hv, 128, 128] fp32 each).
+struct ScanLayout {
+    gdn_problem p2;
+    WsLayout w2;
+    size_t cu2, goff, mbuf, bbuf, hbuf, total;
+    int n2;
+};
+
+ScanLayout scan_layout(const gdn_problem &p, int L) {
+    ScanLayout sl;
+    const int64_t chunks = (p.total_tokens + C - 1) / C + p.num_seqs;
+    sl.n2 = (int)std::min<int64_t>(p.num_seqs + (chunks + L - 1) / L, INT32_MAX / 2);
+    sl.p2 = p;
+    sl.p2.num_seqs = sl.n2;
+    sl.w2 = ws_layout(sl.p2);
+    const size_t plane = (size_t)sl.n2 * p.num_v_heads * D * D * 4;
+    sl.cu2 = align_up(sl.w2.total, 256);
+    sl.goff = align_up(sl.cu2 + 4 * ((size_t)sl.n2 + 1), 256);
+    sl.mbuf = align_up(sl.goff + 4 * ((size_t)p.num_seqs + 1), 1024);
+    sl.bbuf = sl.mbuf + plane;
+    sl.hbuf = sl.bbuf + plane;
+    sl.total = sl.hbuf + plane;
+    return sl;
+}
+
+}  // namespace
+
+size_t prefill_scan_workspace_size(const gdn_problem &p, int chunks_per_group) {
+    return scan_layout(p, chunks_per_group).total;
+}
+
+int prefill_scan_auto_group(const gdn_problem &p) {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 148;
+    }
+    // Enough groups that groups x value heads about fills the SMs once.
+    const int64_t chunks = (p.total_tokens + C - 1) / C + p.num_seqs;
+    const int64_t groups = std::max<int64_t>(1, sms / std::max(1, p.num_v_heads));
+    return (int)std::max<int64_t>(4, (chunks + groups - 1) / groups);
+}
+
+gdn_status launch_prefill_scan(const gdn_problem &p, int L, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const int32_t *cu, const float *h0, void *out, float *hT,
+                               cudaStream_t stream) {
+    if (p.num_seqs == 0) return GDN_OK;
+    const ScanLayout sl = scan_layout(p, L);
+    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
+    int32_t *cu2 = reinterpret_cast<int32_t *>(ws + sl.cu2);
+    int *goff = reinterpret_cast<int *>(ws + sl.goff);
+    float *mb = reinterpret_cast<float *>(ws + sl.mbuf);
+    float *bb = reinterpret_cast<float *>(ws + sl.bbuf);
+    float *hb = reinterpret_cast<float *>(ws + sl.hbuf);
+    const TcPtrs t = tc_ptrs(sl.w2, p.workspace);
+    TcMaps m;
+    if (!encode_maps(p, q, k, v, out, m)) return GDN_ERR_CUDA;
+
+    gdn_scan_split_kernel<<<1, 1024, 0, stream>>>(cu, p.num_seqs, p.total_tokens, L, sl.n2, cu2,
+                                                   goff);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    gdn_status st = launch_table_prep(sl.p2, sl.w2, t, m, g, beta, cu2, 0, stream, false);
+    if (st != GDN_OK) return st;
+    // B of every group (the state from zero), then M (identity state, U = 0);
+    // these passes write no output.
+    st = launch_chain<false, false, true>(sl.p2, t, m, m.to, nullptr, out, bb, nullptr, 1, stream,
+                                          true);
+    if (st != GDN_OK) return st;
+    st = launch_chain<false, true, true>(sl.p2, t, m, m.to, nullptr, out, mb, nullptr, 1, stream,
+                                         true);
+    if (st != GDN_OK) return st;
+    const size_t smem = (size_t)(2 * D * D + kCombineRows * D) * 4;
+    if (cudaFuncSetAttribute(gdn_scan_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    gdn_scan_combine_kernel<<<dim3((unsigned)p.num_seqs * p.num_v_heads, D / kCombineRows),
+                              kCombineThreads, smem, stream>>>(goff, h0, mb, bb, hb, hT, t.err, p.num_v_heads);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    // Outputs: every group from the state entering it.
+    return launch_chain<false, false>(sl.p2, t, m, m.to, hb, out, nullptr, nullptr, 1, stream,
+                                      false);
 }
 
 }  // namespace gdn

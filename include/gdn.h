@@ -165,6 +165,42 @@ GDN_API gdn_status gdn_chunk_prefill_snapshots(const gdn_problem *problem,
                                                gdn_stream_t stream);
 
 /*
+ * gdn_chunk_prefill with the chunk recurrence run as a chunk-parallel scan,
+ * for batches with few (sequence, value head) pairs and long sequences.
+ *
+ * The chunk step of a head is affine in the state, S_{c+1} = S_c M_c + B_c.
+ * That is a restatement of the chunk recurrence of the pages (page
+ * "cf-1.com", section "三个优化", item 2: the inter-chunk state propagation
+ * is the sequential part that dominates the layer's time).  Steps:
+ *   1. Each sequence is cut into groups of chunks_per_group chunks.
+ *   2. Every group's composite (M, B) is computed in parallel: B is the
+ *      recurrence from a zero state, M the recurrence of the linear part
+ *      from the identity.
+ *   3. The state is carried across groups in fp32.
+ *   4. The outputs of every group are produced in parallel from the state
+ *      entering it.
+ * Results are those of gdn_chunk_prefill up to rounding order.
+ *
+ *   chunks_per_group  >= 1 chunks (64 tokens each) per group, or 0 to choose
+ *              one so that groups x value heads about fills the GPU's SMs
+ *   problem->workspace, workspace_bytes: at least
+ *              gdn_chunk_prefill_scan_workspace_size(problem, chunks_per_group)
+ *   everything else as gdn_chunk_prefill
+ *
+ * Only for bf16 q/k/v with dk = dv = 128.  Other configurations return
+ * GDN_ERR_UNSUPPORTED, and the size query returns 0 for them.  The query
+ * also returns 0 for an invalid descriptor or chunks_per_group < 0; the call
+ * returns GDN_ERR_INVALID_ARG for chunks_per_group < 0.
+ */
+GDN_API size_t gdn_chunk_prefill_scan_workspace_size(const gdn_problem *problem,
+                                                    int32_t chunks_per_group);
+GDN_API gdn_status gdn_chunk_prefill_scan(const gdn_problem *problem, int32_t chunks_per_group,
+                                          const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta,
+                                          const int32_t *cu_seqlens, const float *initial_state,
+                                          void *out, float *final_state, gdn_stream_t stream);
+
+/*
  * One recurrent decode step for N sequences (one token each), updating the
  * state in place:
  *   q, k   [N, Hk, dk];  v, out [N, Hv, dv] (qkv dtype);  g, beta [N, Hv] fp32

@@ -182,3 +182,28 @@ def test_prefill_timing_argument_errors(lib):
     assert lib.gdn_prefill_kernel_ms(None) == INVALID
     buf = (ctypes.c_float * 3)()
     assert lib.gdn_prefill_kernel_ms(ctypes.cast(buf, ctypes.c_void_p)) == INVALID
+
+
+def scan(lib, p, L, out=A + 24576):
+    return lib.gdn_chunk_prefill_scan(ctypes.byref(p) if p is not None else None, L, A, A + 4096,
+                                      A + 8192, A + 12288, A + 16384, A + 20480, None, out,
+                                      None, None)
+
+
+def test_scan_argument_errors(lib):
+    """Checks that need no device: sizes, unsupported shapes, bad group
+    sizes, missing workspace."""
+    p = prob(N=2, T=5000, Hk=16, Hv=48)
+    size = lib.gdn_chunk_prefill_scan_workspace_size
+    assert size(ctypes.byref(p), 8) > lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p))
+    assert size(ctypes.byref(p), 0) > 0
+    assert size(ctypes.byref(p), -1) == 0
+    assert size(ctypes.byref(prob(dk=64, dv=64)), 4) == 0
+    assert size(None, 4) == 0
+    assert scan(lib, None, 4) == INVALID
+    assert scan(lib, p, -1) == INVALID
+    assert scan(lib, prob(dk=64, dv=64), 4) == UNSUPPORTED
+    assert scan(lib, p, 4) == WORKSPACE
+    assert scan(lib, prob(N=2, T=5000, Hk=16, Hv=48, ws=A, wsb=size(ctypes.byref(p), 4) - 16),
+                4) == WORKSPACE
+    assert scan(lib, prob(N=0, T=0), 4) == OK
