@@ -280,34 +280,30 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
     for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const float *__restrict__ g, const float *__restrict__ beta,
-                const int *__restrict__ chunk_off, const int4 *__restrict__ table,
-                uint8_t *__restrict__ slots, float *__restrict__ gl, int *__restrict__ err, int N,
-                int Hk, int Hv) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ch = blockIdx.x, hk = blockIdx.y;
-    // Launched as a programmatic dependent of the chunk table kernel: let the
-    // recurrence kernel be scheduled once all of this grid is placed, then
-    // wait for the table.
-    griddep_launch_dependents();
-    griddep_wait();
-    if (ch >= chunk_off[N]) return;
-    const int4 e = table[ch];
-    const int tok0 = e.y, L = e.z;
+// One prep unit: kThreads threads with local index `ltid`, its own PrepSmem
+// and named barrier `bar`; it works through items item0, item0 + stride, ...
+// below n_items (item = chunk * Hk + key head, chunk-major).  With `flags`,
+// each finished item publishes `epoch` into flags[item] (release, device
+// scope) once its workspace slot writes are visible.  kLoop = false: exactly
+// one item (the per-chunk kernel), compiled without the loop.
+template <bool kLoop>
+__device__ __forceinline__ void prep_unit(
+    PrepSmem &sm, const CUtensorMap *tm_q, const CUtensorMap *tm_k, const float *__restrict__ g,
+    const float *__restrict__ beta, const int *__restrict__ chunk_off,
+    const int4 *__restrict__ table, uint8_t *__restrict__ slots, float *__restrict__ gl,
+    int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int item0, int stride,
+    int n_items, unsigned *flags, unsigned epoch) {
+    const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
-    // Epilogue warps 2-9: TMEM quadrant q (lanes 32q..32q+31), column half.
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    // Epilogue warps 2-9: TMEM quadrant q (of the physical warp: lanes
+    // 32q..32q+31), column half.
+    const int q = (threadIdx.x >> 5) & 3, half = (warp - 2) >> 2;
     const int c0 = 32 * half;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 
     if (tid == 0) {
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(tm_q);
+        prefetch_tensormap(tm_k);
         mbar_init(&sm.tma_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
@@ -317,284 +313,328 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    named_barrier(bar, kThreads);
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
-        tma_load_3d(sm.kq + 0 * kTile, &tm_k, 0, hk, tok0, &sm.tma_bar);
-        tma_load_3d(sm.kq + 1 * kTile, &tm_q, 0, hk, tok0, &sm.tma_bar);
-        tma_load_3d(sm.kq + 2 * kTile, &tm_k, 64, hk, tok0, &sm.tma_bar);
-        tma_load_3d(sm.kq + 3 * kTile, &tm_q, 64, hk, tok0, &sm.tma_bar);
-    }
-    // gamma, b and the decay factors of the first round of value heads,
-    // while the K and Q tiles are in flight.
-    auto head_gamma = [&](int j0, int nh) {
-        if (warp >= 1 && warp <= nh) {
-            const int j = warp - 1, h = hk * G + j0 + j;
-            chunk_gamma(g, tok0, L, Hv, h, sm.gam[j], sm.beta[j], beta, sm.eg[j], sm.dec[j]);
-            float *slot_f = reinterpret_cast<float *>(slots + ((size_t)ch * Hv + h) * kSlotBytes);
-            slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[j][2 * lane];
-            slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
-            slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
-            slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
-            if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[j][C - 1];
+    bool bad = false;
+    uint32_t mph = 0, tph = 0;
+    const int n_ch = chunk_off[N];
+#pragma unroll 1
+    for (int item = item0; item < n_items && !bad; item += stride) {
+    // (blockIdx when there is one item: registers the compiler can re-read)
+    const int ch = kLoop ? item / Hk : (int)blockIdx.x;
+    const int hk = kLoop ? item % Hk : (int)blockIdx.y;
+    if (ch >= n_ch) break;  // chunk-major: every later item is past the table
+    const int4 e = table[ch];
+    const int tok0 = e.y, L = e.z;
+        if (tid == 0) {
+            // The previous item's generic reads of these tiles are ordered
+            // before the TMA writes (unit barrier, then this fence).
+            if (kLoop) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
+            tma_load_3d(sm.kq + 0 * kTile, tm_k, 0, hk, tok0, &sm.tma_bar);
+            tma_load_3d(sm.kq + 1 * kTile, tm_q, 0, hk, tok0, &sm.tma_bar);
+            tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, hk, tok0, &sm.tma_bar);
+            tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, hk, tok0, &sm.tma_bar);
         }
-    };
-    head_gamma(0, min(kPrepHeads, G));
-    bool bad = !warp_wait(&sm.tma_bar, 0, nullptr);
-    uint32_t mph = 0;
-    if (tid == 0 && !bad) {
-        tc_fence_after();
-        const uint32_t base = smem_u32(sm.kq);
-        constexpr uint32_t id = idesc_bf16(128, 64, false, false);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * (2 * kTile) + (k % 4) * 32;
-            mma_bf16(tmem + kPColKQ, smem_desc(base + off, 16, 1024),
-                     smem_desc(base + off, 16, 1024), id, k > 0);
+        // gamma, b and the decay factors of the first round of value heads,
+        // while the K and Q tiles are in flight.
+        auto head_gamma = [&](int j0, int nh) {
+            if (warp >= 1 && warp <= nh) {
+                const int j = warp - 1, h = hk * G + j0 + j;
+                chunk_gamma(g, tok0, L, Hv, h, sm.gam[j], sm.beta[j], beta, sm.eg[j], sm.dec[j]);
+                float *slot_f = reinterpret_cast<float *>(slots + ((size_t)ch * Hv + h) * kSlotBytes);
+                slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[j][2 * lane];
+                slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
+                slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
+                slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
+                if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[j][C - 1];
+            }
+        };
+        head_gamma(0, min(kPrepHeads, G));
+        bad = !warp_wait(&sm.tma_bar, kLoop ? tph : 0, nullptr);
+        tph ^= 1;
+        if (tid == 0 && !bad) {
+            tc_fence_after();
+            const uint32_t base = smem_u32(sm.kq);
+            constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+    #pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k / 4) * (2 * kTile) + (k % 4) * 32;
+                mma_bf16(tmem + kPColKQ, smem_desc(base + off, 16, 1024),
+                         smem_desc(base + off, 16, 1024), id, k > 0);
+            }
+            mma_commit(&sm.mma_bar);
         }
-        mma_commit(&sm.mma_bar);
-    }
-    for (int j0 = 0; j0 < G; j0 += kPrepHeads) {
-        const int nh = min(kPrepHeads, G - j0);
-        if (j0 > 0) head_gamma(j0, nh);
-        if (j0 == 0) {
+        for (int j0 = 0; j0 < G; j0 += kPrepHeads) {
+            const int nh = min(kPrepHeads, G - j0);
+            if (j0 > 0) head_gamma(j0, nh);
+            if (j0 == 0) {
+                bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+                mph ^= 1;
+            }
+            tc_fence_after();
+            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
+            // ---- A blocks, E and P from the rows of [K K^T; Q K^T].
+            if (warp >= 2) {
+                const int row = 32 * q + lane;
+                float x[32];
+                tmem_ld32f(tmem + lane_base + kPColKQ + c0, x);
+                if (q < 2) {
+                    const int t = row;
+                    for (int j = 0; j < nh; ++j) {
+                        // Decay factors first (shared loads), then the stores.
+                        const float gt = sm.gam[j][t], bt = sm.beta[j][t];
+                        float av[32];
+    #pragma unroll
+                        for (int u = 0; u < 32; u += 4) {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
+                            const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
+    #pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const int i = c0 + u + w;
+                                av[u + w] = i < t ? bt * ex2_approx((gt - gi[w]) * kLog2e) * x[u + w] : 0.f;
+                            }
+                        }
+    #pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            float ev[8];
+    #pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const int i = c0 + 8 * cc + u;
+                                ev[u] = (t >= 32 && i < 32) ? av[8 * cc + u] : 0.f;
+                            }
+                            *reinterpret_cast<uint4 *>(sm.e[j] + swz(t, (c0 >> 3) + cc)) = pack8(ev);
+                        }
+                        if ((t >> 5) == half) {  // diagonal block: this thread's columns are in it
+                            float *dst = ad_row(sm.n[j], half, t & 31);
+    #pragma unroll
+                            for (int u = 0; u < 32; u += 4)
+                                *reinterpret_cast<float4 *>(dst + ad_f4(u >> 2, t)) =
+                                    make_float4(av[u], av[u + 1], av[u + 2], av[u + 3]);
+                        }
+                    }
+                } else {
+                    const int r = row - 64;
+                    for (int j = 0; j < nh; ++j) {
+                        const int h = hk * G + j0 + j;
+                        const float gr = sm.gam[j][r];
+                        float pv[32];
+    #pragma unroll
+                        for (int u = 0; u < 32; u += 4) {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
+                            const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
+    #pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const int i = c0 + u + w;
+                                pv[u + w] = i <= r ? ex2_approx((gr - gi[w]) * kLog2e) * x[u + w] : 0.f;
+                            }
+                        }
+                        uint8_t *pdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotP;
+    #pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv + 8 * cc);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            named_barrier(bar, kThreads);
+            // ---- D' = blockdiag((I + A_bb)^-1): one column of one block per thread.
+            if (tid >= 64 && tid < 64 + 64 * nh) {
+                const int idx = tid - 64, j = idx >> 6, blk = (idx >> 5) & 1, col = idx & 31;
+                float xc[32];
+    #pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    float a0 = (t == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    const float *Ar = ad_row(sm.n[j], blk, t);
+    #pragma unroll
+                    for (int i = 0; i < (t & ~3); i += 4) {
+                        const float4 av = *reinterpret_cast<const float4 *>(Ar + ad_f4(i >> 2, t));
+                        a0 = fmaf(-av.x, xc[i], a0);
+                        a1 = fmaf(-av.y, xc[i + 1], a1);
+                        a2 = fmaf(-av.z, xc[i + 2], a2);
+                        a3 = fmaf(-av.w, xc[i + 3], a3);
+                    }
+    #pragma unroll
+                    for (int i = (t & ~3); i < t; ++i)
+                        a0 = fmaf(-Ar[ad_f4(i >> 2, t) + (i & 3)], xc[i], a0);
+                    xc[t] = (a0 + a1) + (a2 + a3);
+                }
+                const int ccol = 32 * blk + col;
+                uint8_t *dp = sm.dp[j];
+    #pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    const float val = ((t >> 5) == blk) ? xc[t & 31] : 0.f;
+                    *reinterpret_cast<__nv_bfloat16 *>(dp + swz(t, ccol >> 3) + 2 * (ccol & 7)) =
+                        __float2bfloat16_rn(val);
+                }
+            } else if (tid < 64 || tid >= 256) {
+                // Meanwhile the other four warps write diag(e^gamma) Q of every
+                // value head of the round: the same swizzled image as Q's tiles,
+                // scaled row by row.
+                const int w = tid < 64 ? tid : tid - 192;  // 0 .. 127
+    #pragma unroll 8
+                for (int idx = w; idx < nh * 2 * C * 8; idx += 128) {
+                    const int j = idx / (2 * C * 8), a = (idx / (C * 8)) & 1;
+                    const int r = (idx >> 3) & (C - 1), cc = idx & 7;
+                    const uint32_t off = swz(r, cc);
+                    float x[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(sm.kq + (2 * a + 1) * kTile + off), x);
+                    const float sc = sm.eg[j][r];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) x[u] *= sc;
+                    const int h = hk * G + j0 + j;
+                    *reinterpret_cast<uint4 *>(slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotQ +
+                                               a * kTile + off) = pack8(x);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_barrier(bar, kThreads);
+            // ---- N = D' E  (M = 64, N = 64, K = 64)
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+                for (int j = 0; j < nh; ++j) {
+                    const uint32_t a = smem_u32(sm.dp[j]), b = smem_u32(sm.e[j]);
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
+                                 smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
+                }
+                mma_commit(&sm.mma_bar);
+            }
             bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
             mph ^= 1;
-        }
-        tc_fence_after();
-        if (__syncthreads_or(bad)) break;
-        // ---- A blocks, E and P from the rows of [K K^T; Q K^T].
-        if (warp >= 2) {
-            const int row = 32 * q + lane;
-            float x[32];
-            tmem_ld32f(tmem + lane_base + kPColKQ + c0, x);
-            if (q < 2) {
-                const int t = row;
+            tc_fence_after();
+            if (warp >= 2) {
                 for (int j = 0; j < nh; ++j) {
-                    // Decay factors first (shared loads), then the stores.
-                    const float gt = sm.gam[j][t], bt = sm.beta[j][t];
-                    float av[32];
-#pragma unroll
-                    for (int u = 0; u < 32; u += 4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
-                        const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int i = c0 + u + w;
-                            av[u + w] = i < t ? bt * ex2_approx((gt - gi[w]) * kLog2e) * x[u + w] : 0.f;
-                        }
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float ev[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int i = c0 + 8 * cc + u;
-                            ev[u] = (t >= 32 && i < 32) ? av[8 * cc + u] : 0.f;
-                        }
-                        *reinterpret_cast<uint4 *>(sm.e[j] + swz(t, (c0 >> 3) + cc)) = pack8(ev);
-                    }
-                    if ((t >> 5) == half) {  // diagonal block: this thread's columns are in it
-                        float *dst = ad_row(sm.n[j], half, t & 31);
-#pragma unroll
-                        for (int u = 0; u < 32; u += 4)
-                            *reinterpret_cast<float4 *>(dst + ad_f4(u >> 2, t)) =
-                                make_float4(av[u], av[u + 1], av[u + 2], av[u + 3]);
+                    float x[32];
+                    tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, x);
+                    if (lane < 16) {
+                        const int r = 16 * q + lane;
+    #pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            *reinterpret_cast<uint4 *>(sm.n[j] + swz(r, (c0 >> 3) + cc)) =
+                                pack8(x + 8 * cc);
                     }
                 }
-            } else {
-                const int r = row - 64;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
+            // ---- Y = N D'  (M = 64, N = 64, K = 64), into the same columns
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+                for (int j = 0; j < nh; ++j) {
+                    const uint32_t a = smem_u32(sm.n[j]), b = smem_u32(sm.dp[j]);
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
+                                 smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
+                }
+                mma_commit(&sm.mma_bar);
+            }
+            bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+            mph ^= 1;
+            tc_fence_after();
+            // ---- T = D' - Y;  T diag(b) -> e (and the workspace), T diag(b e^gamma) -> n
+            if (warp >= 2) {
+                for (int j = 0; j < nh; ++j) {
+                    float y[32];
+                    tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, y);
+                    if (lane < 16) {
+                        const int r = 16 * q + lane, h = hk * G + j0 + j;
+                        uint8_t *tdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotTB;
+    #pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const uint32_t off = swz(r, (c0 >> 3) + cc);
+                            float dv[8], tb[8], tbg[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(sm.dp[j] + off), dv);
+    #pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const int i = c0 + 8 * cc + u;
+                                tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[j][i];
+                                tbg[u] = tb[u] * sm.eg[j][i];
+                            }
+                            const uint4 wtb = pack8(tb);
+                            *reinterpret_cast<uint4 *>(sm.e[j] + off) = wtb;
+                            *reinterpret_cast<uint4 *>(sm.n[j] + off) = pack8(tbg);
+                            *reinterpret_cast<uint4 *>(tdst + off) = wtb;
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
+            // ---- W^T = K^T (T diag(b e^gamma))^T  (M = 128 dk, N = 64, K = 64 tokens)
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_bf16(128, 64, true, false);
+                const uint32_t a = smem_u32(sm.kq);
+                for (int j = 0; j < nh; ++j) {
+                    const uint32_t b = smem_u32(sm.n[j]);
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + kPColW + 64 * j, smem_desc(a + 2048 * k, 2 * kTile, 1024),
+                                 smem_desc(b + 32 * k, 16, 1024), id, k > 0);
+                }
+                mma_commit(&sm.mma_bar);
+            }
+            bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+            mph ^= 1;
+            tc_fence_after();
+            if (warp >= 2) {
+                const int row = 32 * q + lane;  // key dimension
                 for (int j = 0; j < nh; ++j) {
                     const int h = hk * G + j0 + j;
-                    const float gr = sm.gam[j][r];
-                    float pv[32];
-#pragma unroll
-                    for (int u = 0; u < 32; u += 4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
-                        const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int i = c0 + u + w;
-                            pv[u + w] = i <= r ? ex2_approx((gr - gi[w]) * kLog2e) * x[u + w] : 0.f;
-                        }
-                    }
-                    uint8_t *pdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotP;
-#pragma unroll
+                    float x[32];
+                    tmem_ld32f(tmem + lane_base + kPColW + 64 * j + c0, x);
+                    uint8_t *wdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotWT;
+    #pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
-                        *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv + 8 * cc);
+                        *reinterpret_cast<uint4 *>(wdst + swz(row, (c0 >> 3) + cc)) = pack8(x + 8 * cc);
                 }
             }
+            tc_fence_before();
+            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- D' = blockdiag((I + A_bb)^-1): one column of one block per thread.
-        if (tid >= 64 && tid < 64 + 64 * nh) {
-            const int idx = tid - 64, j = idx >> 6, blk = (idx >> 5) & 1, col = idx & 31;
-            float xc[32];
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                float a0 = (t == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                const float *Ar = ad_row(sm.n[j], blk, t);
-#pragma unroll
-                for (int i = 0; i < (t & ~3); i += 4) {
-                    const float4 av = *reinterpret_cast<const float4 *>(Ar + ad_f4(i >> 2, t));
-                    a0 = fmaf(-av.x, xc[i], a0);
-                    a1 = fmaf(-av.y, xc[i + 1], a1);
-                    a2 = fmaf(-av.z, xc[i + 2], a2);
-                    a3 = fmaf(-av.w, xc[i + 3], a3);
-                }
-#pragma unroll
-                for (int i = (t & ~3); i < t; ++i)
-                    a0 = fmaf(-Ar[ad_f4(i >> 2, t) + (i & 3)], xc[i], a0);
-                xc[t] = (a0 + a1) + (a2 + a3);
-            }
-            const int ccol = 32 * blk + col;
-            uint8_t *dp = sm.dp[j];
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                const float val = ((t >> 5) == blk) ? xc[t & 31] : 0.f;
-                *reinterpret_cast<__nv_bfloat16 *>(dp + swz(t, ccol >> 3) + 2 * (ccol & 7)) =
-                    __float2bfloat16_rn(val);
-            }
-        } else if (tid < 64 || tid >= 256) {
-            // Meanwhile the other four warps write diag(e^gamma) Q of every
-            // value head of the round: the same swizzled image as Q's tiles,
-            // scaled row by row.
-            const int w = tid < 64 ? tid : tid - 192;  // 0 .. 127
-#pragma unroll 8
-            for (int idx = w; idx < nh * 2 * C * 8; idx += 128) {
-                const int j = idx / (2 * C * 8), a = (idx / (C * 8)) & 1;
-                const int r = (idx >> 3) & (C - 1), cc = idx & 7;
-                const uint32_t off = swz(r, cc);
-                float x[8];
-                unpack8(*reinterpret_cast<const uint4 *>(sm.kq + (2 * a + 1) * kTile + off), x);
-                const float sc = sm.eg[j][r];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] *= sc;
-                const int h = hk * G + j0 + j;
-                *reinterpret_cast<uint4 *>(slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotQ +
-                                           a * kTile + off) = pack8(x);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- N = D' E  (M = 64, N = 64, K = 64)
+    if (kLoop && flags && !bad) {
+        __threadfence();
+        named_barrier(bar, kThreads);
         if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-            for (int j = 0; j < nh; ++j) {
-                const uint32_t a = smem_u32(sm.dp[j]), b = smem_u32(sm.e[j]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
-                             smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
-            }
-            mma_commit(&sm.mma_bar);
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + item), "r"(epoch)
+                         : "memory");
         }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-        mph ^= 1;
-        tc_fence_after();
-        if (warp >= 2) {
-            for (int j = 0; j < nh; ++j) {
-                float x[32];
-                tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, x);
-                if (lane < 16) {
-                    const int r = 16 * q + lane;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        *reinterpret_cast<uint4 *>(sm.n[j] + swz(r, (c0 >> 3) + cc)) =
-                            pack8(x + 8 * cc);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) break;
-        // ---- Y = N D'  (M = 64, N = 64, K = 64), into the same columns
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-            for (int j = 0; j < nh; ++j) {
-                const uint32_t a = smem_u32(sm.n[j]), b = smem_u32(sm.dp[j]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
-                             smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
-            }
-            mma_commit(&sm.mma_bar);
-        }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-        mph ^= 1;
-        tc_fence_after();
-        // ---- T = D' - Y;  T diag(b) -> e (and the workspace), T diag(b e^gamma) -> n
-        if (warp >= 2) {
-            for (int j = 0; j < nh; ++j) {
-                float y[32];
-                tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, y);
-                if (lane < 16) {
-                    const int r = 16 * q + lane, h = hk * G + j0 + j;
-                    uint8_t *tdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotTB;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint32_t off = swz(r, (c0 >> 3) + cc);
-                        float dv[8], tb[8], tbg[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(sm.dp[j] + off), dv);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int i = c0 + 8 * cc + u;
-                            tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[j][i];
-                            tbg[u] = tb[u] * sm.eg[j][i];
-                        }
-                        const uint4 wtb = pack8(tb);
-                        *reinterpret_cast<uint4 *>(sm.e[j] + off) = wtb;
-                        *reinterpret_cast<uint4 *>(sm.n[j] + off) = pack8(tbg);
-                        *reinterpret_cast<uint4 *>(tdst + off) = wtb;
-                    }
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) break;
-        // ---- W^T = K^T (T diag(b e^gamma))^T  (M = 128 dk, N = 64, K = 64 tokens)
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(128, 64, true, false);
-            const uint32_t a = smem_u32(sm.kq);
-            for (int j = 0; j < nh; ++j) {
-                const uint32_t b = smem_u32(sm.n[j]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + kPColW + 64 * j, smem_desc(a + 2048 * k, 2 * kTile, 1024),
-                             smem_desc(b + 32 * k, 16, 1024), id, k > 0);
-            }
-            mma_commit(&sm.mma_bar);
-        }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-        mph ^= 1;
-        tc_fence_after();
-        if (warp >= 2) {
-            const int row = 32 * q + lane;  // key dimension
-            for (int j = 0; j < nh; ++j) {
-                const int h = hk * G + j0 + j;
-                float x[32];
-                tmem_ld32f(tmem + lane_base + kPColW + 64 * j + c0, x);
-                uint8_t *wdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotWT;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(wdst + swz(row, (c0 >> 3) + cc)) = pack8(x + 8 * cc);
-            }
-        }
-        tc_fence_before();
-        if (__syncthreads_or(bad)) break;
+    }
+    if (!kLoop) break;
     }
     if (bad && tid == 0) atomicExch(err, kErrTimeout);
     tc_fence_before();
-    __syncthreads();
+    named_barrier(bar, kThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const float *__restrict__ g, const float *__restrict__ beta,
+                const int *__restrict__ chunk_off, const int4 *__restrict__ table,
+                uint8_t *__restrict__ slots, float *__restrict__ gl, int *__restrict__ err, int N,
+                int Hk, int Hv) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    PrepSmem &sm = *reinterpret_cast<PrepSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Launched as a programmatic dependent of the chunk table kernel: let the
+    // recurrence kernel be scheduled once all of this grid is placed, then
+    // wait for the table.
+    griddep_launch_dependents();
+    griddep_wait();
+    if ((int)blockIdx.x >= chunk_off[N]) return;
+    const int item = blockIdx.x * Hk + blockIdx.y;
+    prep_unit<false>(sm, &tm_q, &tm_k, g, beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
+                     threadIdx.x, 1, item, 1, item + 1, nullptr, 0u);
 }
 
 // ------------------------------------------------------------------ kernel 3
