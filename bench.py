@@ -53,6 +53,11 @@ def load_peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
+def flops_of(T, Hv):
+    """Algorithmic flops of a prefill of T tokens over Hv value heads."""
+    return T * Hv * FLOPS_PER_TOKEN_HEAD
+
+
 def recorded_traffic(kernel):
     """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
     summary, or None when the kernel source has changed since it was taken."""
@@ -295,11 +300,12 @@ def run_ours(args, rank, world, local):
         # headline steps: the extra records cost the call a few us), each
         # step's times read after it.
         gdn.gdn_prefill_timing(True)
-        kernel_ms = []
+        kernel_ms, fused = [], []
         for i in range(args.steps):
             flush.zero_()
             prefill()
             kernel_ms.append(gdn.gdn_prefill_kernel_ms())
+            fused.append(gdn.gdn_prefill_last_fused())
         gdn.gdn_prefill_timing(False)
         torch.cuda.synchronize()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -312,9 +318,18 @@ def run_ours(args, rank, world, local):
     peak_tf = peaks["bf16_tflops"]
     # Roofline of the dominant kernel: its algorithmic flops per launch over
     # its mean launch time in the timed steps.
-    k_us = {name: 1e3 * statistics.mean(m[i] for m in kernel_ms)
-            for i, name in enumerate(("chunk_table", "prep", "recurrence"))}
-    k_flops = {"recurrence": T * P["Hv"] * FLOPS_RECURRENCE, "prep": T * P["Hv"] * FLOPS_PREP}
+    # (When the call runs prep and the recurrence as one fused launch, that
+    # launch is the kernel, with the whole call's algorithmic flops.)
+    ran_fused = all(fused)
+    if ran_fused:
+        launches_per_step = 2  # chunk table + the fused kernel
+    names = ("chunk_table", "prep", "fused") if ran_fused else ("chunk_table", "prep", "recurrence")
+    k_us = {name: 1e3 * statistics.mean(m[i] for m in kernel_ms) for i, name in enumerate(names)}
+    if ran_fused:
+        del k_us["prep"]
+        k_flops = {"fused": flops_of(T, P["Hv"])}
+    else:
+        k_flops = {"recurrence": T * P["Hv"] * FLOPS_RECURRENCE, "prep": T * P["Hv"] * FLOPS_PREP}
     per_kernel = {n: {"us": k_us[n], "flops_per_launch": k_flops[n],
                       "achieved": k_flops[n] / (k_us[n] / 1e6) / 1e12,
                       "frac": k_flops[n] / (k_us[n] / 1e6) / 1e12 / peak_tf,
@@ -322,7 +337,10 @@ def run_ours(args, rank, world, local):
     # The longer kernel; within 2 % (a tie: their event times differ by less
     # than the timer's resolution) the recurrence, which holds 88 % of the
     # algorithmic work.
-    dom = "prep" if k_us["prep"] > 1.02 * k_us["recurrence"] else "recurrence"
+    if ran_fused:
+        dom = "fused"
+    else:
+        dom = "prep" if k_us["prep"] > 1.02 * k_us["recurrence"] else "recurrence"
     dom_flops = k_flops[dom]
     achieved_tf = per_kernel[dom]["achieved"]
     traffic = per_kernel[dom]["traffic"]

@@ -27,7 +27,8 @@ __all__ = [
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
-    "gdn_prefill_timing", "gdn_prefill_kernel_ms", "gdn_chunk_prefill_scan",
+    "gdn_prefill_timing", "gdn_prefill_kernel_ms", "gdn_prefill_last_fused",
+    "gdn_chunk_prefill_scan",
     "gdn_chunk_prefill_scan_workspace_size", "Problem",
     "GDN_BF16", "GDN_F32",
 ]
@@ -116,6 +117,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_prefill_timing.argtypes = [ctypes.c_int32]
     lib.gdn_prefill_kernel_ms.restype = ctypes.c_int
     lib.gdn_prefill_kernel_ms.argtypes = [P]
+    lib.gdn_prefill_last_fused.restype = ctypes.c_int32
+    lib.gdn_prefill_last_fused.argtypes = []
     _lib = lib
     return lib
 
@@ -136,6 +139,12 @@ def gdn_prefill_kernel_ms() -> Tuple[float, float, float]:
     if rc != 0:
         raise GDNError(rc, "gdn_prefill_kernel_ms")
     return float(ms[0]), float(ms[1]), float(ms[2])
+
+
+def gdn_prefill_last_fused() -> bool:
+    """Whether the last prefill recorded with timing on ran prep and the
+    recurrence as one fused launch."""
+    return bool(library().gdn_prefill_last_fused())
 
 
 def gdn_status_string(code: int) -> str:

@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -73,7 +74,7 @@ constexpr int kSlotBytes = kSlotDEC + 256;    // 49664
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-    size_t hdr, chunk_off, snap_off, order, table, gl, tiles, total;
+    size_t hdr, chunk_off, snap_off, order, table, gl, tiles, flags, total;
     int64_t max_chunks;
 };
 
@@ -89,7 +90,9 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.table = align_up(w.order + 4 * (size_t)p.num_seqs, 256);
     w.gl = align_up(w.table + 16 * (size_t)w.max_chunks, 256);  // e^{gamma_L} per (chunk, value head)
     w.tiles = align_up(w.gl + 4 * (size_t)w.max_chunks * p.num_v_heads, 1024);
-    w.total = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
+    // Ready flag per (chunk, key head) for the fused prep + recurrence kernel.
+    w.flags = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
+    w.total = align_up(w.flags + 4 * (size_t)w.max_chunks * p.num_k_heads, 256);
     return w;
 }
 
@@ -104,12 +107,13 @@ __global__ void __launch_bounds__(1024)
 gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t max_chunks,
                        int snap_stride, int *__restrict__ err, int *__restrict__ chunk_off,
                        int *__restrict__ snap_off, int *__restrict__ order,
-                       int4 *__restrict__ table) {
+                       int4 *__restrict__ table, unsigned *__restrict__ flags, int n_flags) {
     __shared__ int s_scan[1024], s_scan2[1024];
     __shared__ int s_carry, s_carry2;
     __shared__ int s_bad;
     const int tid = threadIdx.x;
     griddep_launch_dependents();  // prep may be scheduled; it waits for this grid
+    for (int i = tid; i < n_flags; i += 1024) flags[i] = 0u;
     if (tid == 0) {
         s_carry = 0;
         s_carry2 = 0;
@@ -310,7 +314,9 @@ __device__ __forceinline__ void prep_unit(
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, kPrepTmemCols);
-        tmem_relinquish();
+        // The permit is the CTA's: with two units in one CTA (kLoop) the
+        // other unit may still have to allocate.
+        if (!kLoop) tmem_relinquish();
     }
     tc_fence_before();
     named_barrier(bar, kThreads);
@@ -767,22 +773,24 @@ __device__ __noinline__ bool store_state_rows(ChainSmem &sm, const CUtensorMap *
 // zero, so the final state is the product of the chunks' transition matrices
 // (the output it writes is not used).  kNoOut: only the final state is
 // wanted (the scan's group passes): no output MMAs, output warps or Q~/P loads.
-template <bool kSnaps, bool kLinear = false, bool kNoOut = false>
-__global__ void __launch_bounds__(kChainThreads, 1)
-gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_s,
-                 const int *__restrict__ chunk_off, const int *__restrict__ order,
-                 const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
-                 const float *__restrict__ gl, const float *__restrict__ h0,
-                 __nv_bfloat16 *__restrict__ out,
-                 float *__restrict__ hT, float *__restrict__ snaps, int snap_stride,
-                 const int *__restrict__ snap_off, int *__restrict__ err, int N, int Hk, int Hv) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// The recurrence for (sequence, value head) number `bid` of the sorted order.
+// Warps: 0 loads, 1 MMAs, kS0..kS0+7 state, kS0+8..kS0+11 output, any other
+// idle.  kFused: inside the persistent kernel that also runs prep (below):
+// each warpgroup sets its register budget first (0-3: 72, state and output:
+// 128, the idle fifth: 24), the loads of chunk c wait for its ready flag,
+// and the chunk decay comes from the stage instead of the workspace.
+template <bool kSnaps, bool kLinear, bool kNoOut, int kS0, bool kFused>
+__device__ __forceinline__ void chain_role(
+    ChainSmem &sm, int bid, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+    const CUtensorMap *tm_o, const CUtensorMap *tm_s, const int *__restrict__ chunk_off,
+    const int *__restrict__ order, const int4 *__restrict__ table,
+    const uint8_t *__restrict__ slots, const float *__restrict__ gl,
+    const float *__restrict__ h0, __nv_bfloat16 *__restrict__ out, float *__restrict__ hT,
+    float *__restrict__ snaps, int snap_stride, const int *__restrict__ snap_off,
+    int *__restrict__ err, int N, int Hk, int Hv, const unsigned *__restrict__ flags) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     griddep_wait();  // a programmatic dependent of prep: wait for its slots
-    const int n = order[blockIdx.x / Hv], h = blockIdx.x % Hv;
+    const int n = order[bid / Hv], h = bid % Hv;
     const int hk = h / (Hv / Hk);
     const int c_begin = chunk_off[n], nc = chunk_off[n + 1] - c_begin;
     const size_t state_off = ((size_t)n * Hv + h) * D * D;
@@ -794,7 +802,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (nc == 0) {
         // Empty sequence (or a rejected chunk table): final state = initial state.
         if (hT && !(chunk_off[N] == 0 && *err != kErrNone)) {
-            for (int i = tid; i < D * D / 4; i += kChainThreads) {
+            for (int i = tid; i < D * D / 4; i += kFused ? (int)blockDim.x : kChainThreads) {
                 const float4 x = h0 ? reinterpret_cast<const float4 *>(h0 + state_off)[i]
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 reinterpret_cast<float4 *>(hT + state_off)[i] = x;
@@ -804,10 +812,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
 
     if (tid == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        prefetch_tensormap(&tm_o);
-        if (kSnaps) prefetch_tensormap(&tm_s);
+        prefetch_tensormap(tm_k);
+        prefetch_tensormap(tm_v);
+        prefetch_tensormap(tm_o);
+        if (kSnaps) prefetch_tensormap(tm_s);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1 + kStateThreads);
@@ -834,6 +842,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
 
+    if (kFused ? warp < 4 : warp < 2) {
+    if (kFused) setmaxnreg_dec<72>();
     if (warp == 0) {
         // ---------------- producer: TMA tiles and the prep kernel's slot;
         // chunks kPrefetch ahead are pulled into L2 so that a stage's loads
@@ -846,10 +856,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 if (lane != 0) return;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
-                tma_prefetch_3d(&tm_k, 0, hk, tok0);
-                tma_prefetch_3d(&tm_k, 64, hk, tok0);
-                tma_prefetch_3d(&tm_v, 0, h, tok0);
-                tma_prefetch_3d(&tm_v, 64, h, tok0);
+                tma_prefetch_3d(tm_k, 0, hk, tok0);
+                tma_prefetch_3d(tm_k, 64, hk, tok0);
+                tma_prefetch_3d(tm_v, 0, h, tok0);
+                tma_prefetch_3d(tm_v, 64, h, tok0);
                 bulk_prefetch_l2(slots + ((size_t)ch * Hv + h) * kSlotBytes, kSlotBytes);
             };
             #pragma unroll 1
@@ -859,6 +869,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
+                if (kFused && !wait_ready(flags + (size_t)(c_begin + c) * Hk + hk, &sm.abort))
+                    break;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
                 ChainStage &st = sm.st[s];
@@ -869,11 +881,11 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 if (elect_one_sync()) {
                     mbar_arrive_expect_tx(bar, kStageBytes - (kNoOut ? 3 * kTile : 0) -
                                                    (kLinear ? 3 * kTile : 0));
-                    tma_load_3d(st.k, &tm_k, 0, hk, tok0, bar);
-                    tma_load_3d(st.k + kTile, &tm_k, 64, hk, tok0, bar);
+                    tma_load_3d(st.k, tm_k, 0, hk, tok0, bar);
+                    tma_load_3d(st.k + kTile, tm_k, 64, hk, tok0, bar);
                     if (!kLinear) {
-                        tma_load_3d(st.v, &tm_v, 0, h, tok0, bar);
-                        tma_load_3d(st.v + kTile, &tm_v, 64, h, tok0, bar);
+                        tma_load_3d(st.v, tm_v, 0, h, tok0, bar);
+                        tma_load_3d(st.v + kTile, tm_v, 64, h, tok0, bar);
                         bulk_load(st.tb, slot + kSlotTB, kTile, bar);
                     }
                     bulk_load(st.wt, slot + kSlotWT, 2 * kTile, bar);
@@ -986,14 +998,16 @@ if (elect_one_sync()) {
             }
             mma_commit_w(&sm.fin);
         }
-    } else if (warp < 10) {
+    }
+    } else if (warp < kS0 + 8) {  // (warps below kS0 took the branch above)
+        if (kFused) setmaxnreg_inc<128>();
         // ---------------- state warps 2-9: row j, half h2 of the state's
         // columns (and of Delta's 64 tokens).  The state is kept in TMEM as
         // S^ with S = sigma S^: the chunk decay e^{gamma_L} folds into sigma,
         // and 1 / sigma into the Delta operand of the update, so the fp32
         // state is only rewritten when sigma gets small (renormalisation).
         // E3: Delta^T -> bf16 A operands; E6: S -> -S0 (bf16).
-        const int h2 = (warp - 2) >> 2;
+        const int h2 = (warp - kS0) >> 2;
         const uint32_t t_ns = tmem + lane_base + kColNS + 32 * h2;  // + 64 * (chunk & 1)
         const uint32_t t_s = tmem + lane_base + kColS + 64 * h2;
         float sigma = 1.f;
@@ -1021,7 +1035,9 @@ if (elect_one_sync()) {
         #pragma unroll 1
         for (int c = 0; ok && c < nc; ++c) {
             const float *dec = sm.st[c & 1].egdec + C;
-            const float decay = gl[(size_t)(c_begin + c) * Hv + h];  // e^{gamma_L} of chunk c
+            // e^{gamma_L} of chunk c (in the fused kernel from the stage, which
+            // holds e^{gamma_t} with gamma constant past the chunk's end)
+            const float decay_g = kFused ? 1.f : gl[(size_t)(c_begin + c) * Hv + h];
             bool snap_here = false;
             if (kSnaps) {
                 snap_here = --snap_left == 0 || c == nc - 1;
@@ -1029,6 +1045,7 @@ if (elect_one_sync()) {
             }
             if (!(ok = warp_wait_lean(&sm.d_done, c & 1, &sm.abort))) break;
             tc_fence_after();
+            const float decay = kFused ? sm.st[c & 1].egdec[C - 1] : decay_g;
             float sigma_next = sigma * decay;
             if (!(sigma_next >= kRenorm)) {
                 // Fold sigma_next into S^ (sigma becomes 1).  G6 of the previous
@@ -1097,20 +1114,21 @@ if (elect_one_sync()) {
                 }
             }
             if (snap_here) {
-                if (!(ok = store_state_rows(sm, &tm_s, t_s, sigma, c, snap_z))) break;
+                if (!(ok = store_state_rows(sm, tm_s, t_s, sigma, c, snap_z))) break;
                 snap_z += Hv;
             }
         }
         if (kSnaps && lane == 0) bulk_wait_group<0>();
-    } else {
-        // ---------------- output warps 10-13: o_t = S0 (e^{gamma_t} q_t) +
+    } else if (!kFused || warp < kS0 + 12) {
+        if (kFused) setmaxnreg_inc<128>();
+        // ---------------- output warps: o_t = S0 (e^{gamma_t} q_t) +
         // (Delta^T P^T)_t for this warp's 32 value dims, read from this
         // chunk's output accumulator with the 16x256b TMEM shape (the m8n8
         // fragment layout) and written transposed with stmatrix into a
         // [64 tokens][128 dv] tile held as two 128-byte-swizzled halves, then
         // stored by TMA (a short last chunk, whose tile would reach into the
         // next sequence, is copied out row by row instead).
-        const bool leader = (warp == 10 && lane == 0);
+        const bool leader = (warp == kS0 + 8 && lane == 0);
         const int hh = q >> 1;                  // dv half of this warp's rows
         const int k8 = lane & 7, d8 = lane >> 3; // stmatrix row and matrix of this lane
 #pragma unroll 1
@@ -1144,14 +1162,14 @@ if (elect_one_sync()) {
                 fence_proxy_async_smem();
                 named_barrier(1, kOutThreads);
                 if (leader) {
-                    tma_store_3d(&tm_o, 0, h, tok0, stg);
-                    tma_store_3d(&tm_o, 64, h, tok0, stg + kTile);
+                    tma_store_3d(tm_o, 0, h, tok0, stg);
+                    tma_store_3d(tm_o, 64, h, tok0, stg + kTile);
                     bulk_commit_group();
                 }
             } else {
                 named_barrier(1, kOutThreads);
                 // Rows t < L: 16 chunks of 16 bytes each, un-swizzled.
-                const int tid_o = tid - 10 * 32;
+                const int tid_o = tid - (kS0 + 8) * 32;
                 for (int idx = tid_o; idx < L * 16; idx += kOutThreads) {
                     const int t = idx >> 4, cc = idx & 15;
                     const uint4 v = *reinterpret_cast<const uint4 *>(stg + (cc >> 3) * kTile +
@@ -1161,6 +1179,8 @@ if (elect_one_sync()) {
             }
         }
         if (leader) bulk_wait_group<0>();
+    } else if (kFused) {
+        setmaxnreg_dec<24>();  // the idle warpgroup
     }
     __syncthreads();
     if (sm.abort) {
@@ -1176,6 +1196,69 @@ if (elect_one_sync()) {
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <bool kSnaps, bool kLinear = false, bool kNoOut = false>
+__global__ void __launch_bounds__(kChainThreads, 1)
+gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_s,
+                 const int *__restrict__ chunk_off, const int *__restrict__ order,
+                 const int4 *__restrict__ table, const uint8_t *__restrict__ slots,
+                 const float *__restrict__ gl, const float *__restrict__ h0,
+                 __nv_bfloat16 *__restrict__ out,
+                 float *__restrict__ hT, float *__restrict__ snaps, int snap_stride,
+                 const int *__restrict__ snap_off, int *__restrict__ err, int N, int Hk, int Hv) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    ChainSmem &sm = *reinterpret_cast<ChainSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    chain_role<kSnaps, kLinear, kNoOut, 2, false>(sm, blockIdx.x, &tm_k, &tm_v, &tm_o, &tm_s,
+                                                  chunk_off, order, table, slots, gl, h0, out, hT,
+                                                  snaps, snap_stride, snap_off, err, N, Hk, Hv,
+                                                  nullptr);
+}
+
+// ------------------------------------------------------------------ fused prep + recurrence
+// One persistent cooperative launch, one CTA per SM.  CTAs below n_chain run
+// the recurrence of one (sequence, value head) each (warps 0, 1 and 4-15);
+// the others run two prep units each (warps 0-9 and 10-19) over the (chunk,
+// key head) items in chunk order, publishing a ready flag per item, and the
+// recurrence waits for the flag of each chunk before loading it.  Prep never
+// waits for the recurrence and all CTAs are resident (cooperative launch), so
+// every wait ends.  Prep runs on the SMs the recurrence leaves idle, during
+// the recurrence instead of before it.
+constexpr int kFusedThreads = 2 * kThreads;
+constexpr size_t kPrepUnitBytes = (sizeof(PrepSmem) + 1023) / 1024 * 1024;
+constexpr size_t kFusedSmemBytes =
+    (sizeof(ChainSmem) > 2 * kPrepUnitBytes ? sizeof(ChainSmem) : 2 * kPrepUnitBytes) + 1024;
+// The register budgets of the recurrence role (72 x 128 + 128 x 384 + 24 x 128
+// threads) are the launch allocation of 640 threads at 96 registers.
+static_assert(72 * 128 + 128 * 384 + 24 * 128 == kFusedThreads * 96, "register split");
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const float *__restrict__ g, const float *__restrict__ beta,
+                 const int *__restrict__ chunk_off, const int *__restrict__ order,
+                 const int4 *__restrict__ table, uint8_t *__restrict__ slots,
+                 float *__restrict__ gl, const float *__restrict__ h0,
+                 __nv_bfloat16 *__restrict__ out, float *__restrict__ hT, int *__restrict__ err,
+                 unsigned *__restrict__ flags, int N, int Hk, int Hv, int n_chain, int n_items) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if ((int)blockIdx.x < n_chain) {
+        chain_role<false, false, false, 4, true>(
+            *reinterpret_cast<ChainSmem *>(base), blockIdx.x, &tm_k, &tm_v, &tm_o, &tm_o,
+            chunk_off, order, table, slots, gl, h0, out, hT, nullptr, 1, nullptr, err, N, Hk, Hv,
+            flags);
+    } else {
+        const int u = threadIdx.x / kThreads;
+        const int pcta = blockIdx.x - n_chain, ncta = gridDim.x - n_chain;
+        prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
+                        beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
+                        threadIdx.x - u * kThreads, 1 + u, 2 * pcta + u, 2 * ncta, n_items, flags,
+                        1u);
+    }
 }
 
 // ------------------------------------------------------------------ chunk-parallel scan
@@ -1396,7 +1479,7 @@ cudaLaunchConfig_t pdl_config(dim3 grid, unsigned threads, size_t smem, cudaStre
 // Timing events (see gdn_prefill_timing): before the chunk table, after it,
 // after prep, after the recurrence.
 cudaEvent_t g_tev[4] = {};
-bool g_timing = false, g_timed = false;
+bool g_timing = false, g_timed = false, g_timed_fused = false;
 
 void time_mark(int i, cudaStream_t s) {
     if (g_timing) cudaEventRecord(g_tev[i], s);
@@ -1412,6 +1495,8 @@ gdn_status prefill_timing(bool enable) {
     g_timing = enable;
     return GDN_OK;
 }
+
+bool prefill_timed_fused() { return g_timed_fused; }
 
 gdn_status prefill_kernel_ms(float *ms) {
     if (!g_timed) return GDN_ERR_INVALID_ARG;
@@ -1442,6 +1527,7 @@ struct TcPtrs {
     int4 *table;
     float *gl;
     uint8_t *slots;
+    unsigned *flags;
 };
 
 TcPtrs tc_ptrs(const WsLayout &w, void *workspace) {
@@ -1449,7 +1535,7 @@ TcPtrs tc_ptrs(const WsLayout &w, void *workspace) {
     return {reinterpret_cast<int *>(ws + w.hdr), reinterpret_cast<int *>(ws + w.chunk_off),
             reinterpret_cast<int *>(ws + w.snap_off), reinterpret_cast<int *>(ws + w.order),
             reinterpret_cast<int4 *>(ws + w.table), reinterpret_cast<float *>(ws + w.gl),
-            ws + w.tiles};
+            ws + w.tiles, reinterpret_cast<unsigned *>(ws + w.flags)};
 }
 
 bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void *v, void *out,
@@ -1464,16 +1550,22 @@ bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void 
            encode_thd(&m.to, out, p.total_tokens, p.num_v_heads);
 }
 
-// Chunk table, then prep (a programmatic dependent of the table kernel).
-gdn_status launch_table_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
-                             const TcMaps &m, const float *g, const float *beta,
-                             const int32_t *cu, int snap_stride, cudaStream_t stream, bool pdl) {
+// The chunk table kernel (with `zero_flags`, it also clears the ready flags of
+// the fused kernel).
+gdn_status launch_table(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
+                        const int32_t *cu, int snap_stride, bool zero_flags, cudaStream_t stream) {
     time_mark(0, stream);
-    gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu, p.num_seqs, p.total_tokens, w.max_chunks,
-                                                    snap_stride, t.err, t.chunk_off, t.snap_off,
-                                                    t.order, t.table);
+    gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(
+        cu, p.num_seqs, p.total_tokens, w.max_chunks, snap_stride, t.err, t.chunk_off, t.snap_off,
+        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_k_heads) : 0);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     time_mark(1, stream);
+    return GDN_OK;
+}
+
+// Prep (a programmatic dependent of the chunk table kernel).
+gdn_status launch_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, const TcMaps &m,
+                       const float *g, const float *beta, cudaStream_t stream, bool pdl) {
     if (p.total_tokens > 0) {
         const size_t smem = sizeof(PrepSmem) + 1024;
         if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1489,6 +1581,13 @@ gdn_status launch_table_prep(const gdn_problem &p, const WsLayout &w, const TcPt
     }
     time_mark(2, stream);
     return GDN_OK;
+}
+
+gdn_status launch_table_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
+                             const TcMaps &m, const float *g, const float *beta,
+                             const int32_t *cu, int snap_stride, cudaStream_t stream, bool pdl) {
+    const gdn_status st = launch_table(p, w, t, cu, snap_stride, false, stream);
+    return st != GDN_OK ? st : launch_prep(p, w, t, m, g, beta, stream, pdl);
 }
 
 // The recurrence kernel over the chunk table of `p` (a programmatic
@@ -1514,6 +1613,62 @@ gdn_status launch_chain(const gdn_problem &p, const TcPtrs &t, const TcMaps &m,
     return GDN_OK;
 }
 
+// SMs the fused kernel can run on (one CTA each), or 0 when it cannot be
+// used on this device: no cooperative launch, a register count other than the
+// 96 its warpgroup budgets are split from, or less than one CTA per SM.
+// GDN_PREFILL_FUSED=0 in the environment turns it off.
+int fused_grid() {
+    static int grid = -1;
+    if (grid >= 0) return grid;
+    grid = 0;
+    const char *env = getenv("GDN_PREFILL_FUSED");
+    if (env && env[0] == '0') return grid;
+    int dev = 0, sms = 0, coop = 0, blocks = 0;
+    cudaFuncAttributes fa;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(gdn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFusedSmemBytes) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, gdn_fused_kernel) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gdn_fused_kernel, kFusedThreads,
+                                                      kFusedSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return grid;
+    }
+    if (coop && fa.numRegs == 96 && blocks >= 1) grid = sms;
+    return grid;
+}
+
+// Chunk table, then the fused kernel: prep and the recurrence in one launch.
+// False when the launch was refused (the caller then runs the separate
+// kernels; the chunk table is already in place).
+bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, const TcMaps &m,
+                  const float *g, const float *beta, const float *h0, void *out, float *hT,
+                  int grid, cudaStream_t stream) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;
+    attr.val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = kFusedSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const int n_chain = p.num_seqs * p.num_v_heads;
+    const int n_items = (int)(w.max_chunks * p.num_k_heads);
+    if (cudaLaunchKernelEx(&cfg, gdn_fused_kernel, m.tq, m.tk, m.tv, m.to, g, beta,
+                           (const int *)t.chunk_off, (const int *)t.order, (const int4 *)t.table,
+                           t.slots, t.gl, h0, static_cast<__nv_bfloat16 *>(out), hT, t.err,
+                           t.flags, p.num_seqs, p.num_k_heads, p.num_v_heads, n_chain,
+                           n_items) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
 }  // namespace
 
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
@@ -1529,6 +1684,29 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     // (programmatic dependent launch), except while per-kernel timing records
     // events between them.
     const bool pdl = !g_timing;
+    // One sequence whose (sequence x value head) recurrences leave SMs for
+    // prep: the fused kernel (not while per-kernel timing is on).
+    const int grid = (snaps || p.total_tokens == 0 || p.num_seqs != 1) ? 0 : fused_grid();
+    if (grid > 0 && p.num_seqs * p.num_v_heads + 16 <= grid) {
+        gdn_status st = launch_table(p, w, t, cu, 0, true, stream);
+        if (st != GDN_OK) return st;
+        time_mark(2, stream);  // (no separate prep launch)
+        if (launch_fused(p, w, t, m, g, beta, h0, out, hT, grid, stream)) {
+            time_mark(3, stream);
+            if (g_timing) g_timed = g_timed_fused = true;
+            return GDN_OK;
+        }
+        st = launch_prep(p, w, t, m, g, beta, stream, false);
+        if (st != GDN_OK) return st;
+        st = launch_chain<false, false>(p, t, m, m.to, h0, out, hT, nullptr, 1, stream, false);
+        if (st != GDN_OK) return st;
+        time_mark(3, stream);
+        if (g_timing) {
+            g_timed = true;
+            g_timed_fused = false;
+        }
+        return GDN_OK;
+    }
     gdn_status st = launch_table_prep(p, w, t, m, g, beta, cu, snaps ? snap_stride : 0, stream, pdl);
     if (st != GDN_OK) return st;
     CUtensorMap ts = m.to;
@@ -1539,7 +1717,10 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
                : launch_chain<false, false>(p, t, m, ts, h0, out, hT, nullptr, 1, stream, pdl);
     if (st != GDN_OK) return st;
     time_mark(3, stream);
-    if (g_timing) g_timed = true;
+    if (g_timing) {
+        g_timed = true;
+        g_timed_fused = false;
+    }
     return GDN_OK;
 }
 

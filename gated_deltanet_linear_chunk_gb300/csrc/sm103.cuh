@@ -169,6 +169,42 @@ __device__ __forceinline__ bool warp_wait_lean(uint64_t *bar, uint32_t parity, v
     return true;
 }
 
+// Register budget of the executing warpgroup (all four warps execute it).
+// The increase waits until enough registers of the CTA's launch allocation
+// are free, so the budgets of all warpgroups must sum to at most that.
+template <int N> __device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N> __device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Waits (bounded, every lane polling with an acquire load at device scope)
+// until the 32-bit flag written by another CTA of the grid is nonzero, then
+// orders the async proxy (TMA and bulk copies this thread issues next) after
+// the data that the flag's writer published.  Returns false, after setting
+// *abort, on time-out or when *abort is set.
+__device__ __forceinline__ bool wait_ready(const unsigned *flag, volatile int *abort,
+                                           long long limit = 4000000000ll) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == 0) {
+        const long long t0 = clock64();
+#pragma unroll 1
+        while (true) {
+            __nanosleep(64);
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+            if (v != 0) break;
+            if (*abort || clock64() - t0 > limit) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
 // Single-thread bounded wait for the latency-critical roles (TMA producer,
 // MMA issuer): plain polling, no suspend hint, time limit checked every 256
 // polls.

@@ -26,8 +26,10 @@
  *
  * Ownership and threading: the caller owns every buffer.  The library never
  * allocates device memory, never frees, never synchronises, and launches only
- * on the given stream.  Calls are reentrant; the only process-wide state is a
- * per-device cache of device attributes filled on first use.
+ * on the given stream.  Calls are reentrant.  The process-wide state is:
+ *   - device attributes (SM count, whether the fused prefill kernel fits),
+ *     cached on first use for the then-current device;
+ *   - the opt-in timing events of gdn_prefill_timing.
  *
  * Errors: argument errors are detected on the host before any launch and
  * leave every output untouched.  Launch failures return GDN_ERR_CUDA.  Faults
@@ -114,6 +116,13 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem);
  *                  initial_state (in-place resume)
  * q and k must already be L2-normalised by the caller.  All tensor pointers
  * must be 16-byte aligned.
+ *
+ * For bf16, dk = dv = 128 and one sequence whose Hv recurrences leave at
+ * least 16 SMs free, the intra-chunk prep and the recurrence run as one
+ * cooperative launch: prep on the free SMs, publishing each chunk as it is
+ * done, and the recurrence following it.  Otherwise they are separate
+ * kernels.  The results are the same either way.  GDN_PREFILL_FUSED=0 in the
+ * environment (read once) keeps them separate.
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
                                      const void *q, const void *k, const void *v,
@@ -151,9 +160,10 @@ GDN_API int64_t gdn_chunk_prefill_snapshot_slots(const gdn_problem *problem,
  *              Must not alias the states.
  * Only for bf16 q/k/v with dk = dv = 128 (the tensor-core path); other
  * configurations return GDN_ERR_UNSUPPORTED.  Everything else as
- * gdn_chunk_prefill (same workspace size).  The snapshot stores come from
- * the warps that carry the state, so a snapshot after every chunk (s = 1)
- * about doubles the call at 48 heads; s = 8 (512 tokens) costs far less.
+ * gdn_chunk_prefill (same workspace size).  The states are staged in shared
+ * memory and stored by TMA after each selected chunk: at 4000 tokens x 48
+ * heads, s = 1 costs about half a plain call more, s = 8 (512 tokens) about
+ * a tenth.
  */
 GDN_API gdn_status gdn_chunk_prefill_snapshots(const gdn_problem *problem,
                                                const void *q, const void *k, const void *v,
@@ -317,12 +327,17 @@ GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace, gdn_st
  *       recording on, 0 turns it off.  GDN_ERR_CUDA if the events cannot be
  *       created.
  *   gdn_prefill_kernel_ms(ms): ms[0], ms[1], ms[2] = chunk table, prep and
- *       recurrence of the last recorded call, in milliseconds.
+ *       recurrence of the last recorded call, in milliseconds.  When that
+ *       call ran prep and the recurrence as one fused launch (see
+ *       gdn_chunk_prefill), ms[1] is 0 and ms[2] is the fused kernel.
  *       GDN_ERR_INVALID_ARG if ms is NULL or no call was recorded,
  *       GDN_ERR_CUDA if the events cannot be read.
+ *   gdn_prefill_last_fused(): 1 if the last recorded call ran the fused
+ *       kernel, else 0.
  */
 GDN_API gdn_status gdn_prefill_timing(int32_t enable);
 GDN_API gdn_status gdn_prefill_kernel_ms(float *ms);
+GDN_API int32_t gdn_prefill_last_fused(void);
 
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);
