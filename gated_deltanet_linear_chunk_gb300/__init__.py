@@ -28,6 +28,7 @@ __all__ = [
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
     "gdn_prefill_timing", "gdn_prefill_kernel_ms", "gdn_prefill_last_fused",
+    "gdn_prefill_fused_mode",
     "gdn_chunk_prefill_scan",
     "gdn_chunk_prefill_scan_workspace_size", "Problem",
     "GDN_BF16", "GDN_F32",
@@ -119,6 +120,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_prefill_kernel_ms.argtypes = [P]
     lib.gdn_prefill_last_fused.restype = ctypes.c_int32
     lib.gdn_prefill_last_fused.argtypes = []
+    lib.gdn_prefill_fused_mode.restype = ctypes.c_int32
+    lib.gdn_prefill_fused_mode.argtypes = [ctypes.c_int32]
     _lib = lib
     return lib
 
@@ -139,6 +142,13 @@ def gdn_prefill_kernel_ms() -> Tuple[float, float, float]:
     if rc != 0:
         raise GDNError(rc, "gdn_prefill_kernel_ms")
     return float(ms[0]), float(ms[1]), float(ms[2])
+
+
+def gdn_prefill_fused_mode(mode: int = -1) -> int:
+    """Sets when prefills use the fused prep + recurrence kernel (0 never,
+    1 whenever possible, 2 when expected faster; default 2) and returns the
+    previous mode; -1 only queries."""
+    return int(library().gdn_prefill_fused_mode(int(mode)))
 
 
 def gdn_prefill_last_fused() -> bool:

@@ -217,6 +217,8 @@ GDN_API gdn_status gdn_prefill_kernel_ms(float *ms) {
 
 GDN_API int32_t gdn_prefill_last_fused(void) { return gdn::prefill_timed_fused() ? 1 : 0; }
 
+GDN_API int32_t gdn_prefill_fused_mode(int32_t mode) { return gdn::prefill_fused_mode(mode); }
+
 GDN_API const char *gdn_status_string(gdn_status status) {
     switch (status) {
         case GDN_OK: return "GDN_OK";

@@ -72,6 +72,7 @@ gdn_status launch_prefill_scan(const gdn_problem &p, int chunks_per_group, const
 gdn_status prefill_timing(bool enable);
 gdn_status prefill_kernel_ms(float *ms);
 bool prefill_timed_fused();
+int prefill_fused_mode(int mode);
 
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, const int32_t *cu_seqlens,

@@ -74,7 +74,7 @@ constexpr int kSlotBytes = kSlotDEC + 256;    // 49664
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-    size_t hdr, chunk_off, snap_off, order, table, gl, tiles, flags, total;
+    size_t hdr, chunk_off, snap_off, order, table, gl, tiles, flags, porder, total;
     int64_t max_chunks;
 };
 
@@ -92,7 +92,9 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.tiles = align_up(w.gl + 4 * (size_t)w.max_chunks * p.num_v_heads, 1024);
     // Ready flag per (chunk, key head) for the fused prep + recurrence kernel.
     w.flags = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
-    w.total = align_up(w.flags + 4 * (size_t)w.max_chunks * p.num_k_heads, 256);
+    // and the order in which its prep units take the chunks.
+    w.porder = align_up(w.flags + 4 * (size_t)w.max_chunks * p.num_k_heads, 256);
+    w.total = align_up(w.porder + 4 * (size_t)w.max_chunks, 256);
     return w;
 }
 
@@ -107,7 +109,8 @@ __global__ void __launch_bounds__(1024)
 gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t max_chunks,
                        int snap_stride, int *__restrict__ err, int *__restrict__ chunk_off,
                        int *__restrict__ snap_off, int *__restrict__ order,
-                       int4 *__restrict__ table, unsigned *__restrict__ flags, int n_flags) {
+                       int4 *__restrict__ table, unsigned *__restrict__ flags, int n_flags,
+                       int *__restrict__ porder) {
     __shared__ int s_scan[1024], s_scan2[1024];
     __shared__ int s_carry, s_carry2;
     __shared__ int s_bad;
@@ -176,6 +179,17 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
         const int c = ch - chunk_off[lo];
         const int tok0 = cu[lo] + c * C;
         table[ch] = make_int4(lo, tok0, min(C, cu[lo + 1] - tok0), c);
+        if (porder) {
+            // Rank of the chunk by (position in its sequence, sequence): the
+            // fused kernel's prep takes every sequence's chunk c before any
+            // chunk c + 1.
+            int rank = 0;
+            for (int m = 0; m < N; ++m) {
+                const int nm = chunk_off[m + 1] - chunk_off[m];
+                rank += min(c, nm) + ((m < lo && nm > c) ? 1 : 0);
+            }
+            porder[rank] = ch;
+        }
     }
     for (int n = tid; n < N; n += 1024) {
         if (N > kMaxSortSeqs) {
@@ -296,7 +310,7 @@ __device__ __forceinline__ void prep_unit(
     const float *__restrict__ beta, const int *__restrict__ chunk_off,
     const int4 *__restrict__ table, uint8_t *__restrict__ slots, float *__restrict__ gl,
     int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int item0, int stride,
-    int n_items, unsigned *flags, unsigned epoch) {
+    int n_items, unsigned *flags, unsigned epoch, const int *__restrict__ porder = nullptr) {
     const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
     // Epilogue warps 2-9: TMEM quadrant q (of the physical warp: lanes
@@ -328,9 +342,10 @@ __device__ __forceinline__ void prep_unit(
 #pragma unroll 1
     for (int item = item0; item < n_items && !bad; item += stride) {
     // (blockIdx when there is one item: registers the compiler can re-read)
-    const int ch = kLoop ? item / Hk : (int)blockIdx.x;
+    const int ci = kLoop ? item / Hk : (int)blockIdx.x;
+    if (ci >= n_ch) break;  // chunk-major: every later item is past the table
+    const int ch = (kLoop && porder) ? porder[ci] : ci;
     const int hk = kLoop ? item % Hk : (int)blockIdx.y;
-    if (ch >= n_ch) break;  // chunk-major: every later item is past the table
     const int4 e = table[ch];
     const int tok0 = e.y, L = e.z;
         if (tid == 0) {
@@ -611,7 +626,8 @@ __device__ __forceinline__ void prep_unit(
         __threadfence();
         named_barrier(bar, kThreads);
         if (tid == 0) {
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + item), "r"(epoch)
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)ch * Hk + hk),
+                         "r"(epoch)
                          : "memory");
         }
     }
@@ -1242,7 +1258,8 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const int4 *__restrict__ table, uint8_t *__restrict__ slots,
                  float *__restrict__ gl, const float *__restrict__ h0,
                  __nv_bfloat16 *__restrict__ out, float *__restrict__ hT, int *__restrict__ err,
-                 unsigned *__restrict__ flags, int N, int Hk, int Hv, int n_chain, int n_items) {
+                 unsigned *__restrict__ flags, const int *__restrict__ porder, int N, int Hk,
+                 int Hv, int n_chain, int n_items) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1257,7 +1274,7 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                         threadIdx.x - u * kThreads, 1 + u, 2 * pcta + u, 2 * ncta, n_items, flags,
-                        1u);
+                        1u, porder);
     }
 }
 
@@ -1485,6 +1502,20 @@ void time_mark(int i, cudaStream_t s) {
     if (g_timing) cudaEventRecord(g_tev[i], s);
 }
 
+// Fused path mode (gdn_prefill_fused_mode): 0 off, 1 whenever it can run,
+// 2 when the cost model below expects it to be faster.  The environment
+// variable GDN_PREFILL_FUSED (0, 1 or 2) sets the initial mode.
+int g_fused_mode = -1;
+
+int fused_mode() {
+    if (g_fused_mode < 0) {
+        const char *env = getenv("GDN_PREFILL_FUSED");
+        g_fused_mode = (env && env[0] >= '0' && env[0] <= '2') ? env[0] - '0' : 2;
+    }
+    return g_fused_mode;
+}
+
+
 }  // namespace
 
 gdn_status prefill_timing(bool enable) {
@@ -1497,6 +1528,12 @@ gdn_status prefill_timing(bool enable) {
 }
 
 bool prefill_timed_fused() { return g_timed_fused; }
+
+int prefill_fused_mode(int mode) {
+    const int old = fused_mode();
+    if (mode >= 0 && mode <= 2) g_fused_mode = mode;
+    return old;
+}
 
 gdn_status prefill_kernel_ms(float *ms) {
     if (!g_timed) return GDN_ERR_INVALID_ARG;
@@ -1528,6 +1565,7 @@ struct TcPtrs {
     float *gl;
     uint8_t *slots;
     unsigned *flags;
+    int *porder;
 };
 
 TcPtrs tc_ptrs(const WsLayout &w, void *workspace) {
@@ -1535,7 +1573,8 @@ TcPtrs tc_ptrs(const WsLayout &w, void *workspace) {
     return {reinterpret_cast<int *>(ws + w.hdr), reinterpret_cast<int *>(ws + w.chunk_off),
             reinterpret_cast<int *>(ws + w.snap_off), reinterpret_cast<int *>(ws + w.order),
             reinterpret_cast<int4 *>(ws + w.table), reinterpret_cast<float *>(ws + w.gl),
-            ws + w.tiles, reinterpret_cast<unsigned *>(ws + w.flags)};
+            ws + w.tiles, reinterpret_cast<unsigned *>(ws + w.flags),
+            reinterpret_cast<int *>(ws + w.porder)};
 }
 
 bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void *v, void *out,
@@ -1557,7 +1596,8 @@ gdn_status launch_table(const gdn_problem &p, const WsLayout &w, const TcPtrs &t
     time_mark(0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(
         cu, p.num_seqs, p.total_tokens, w.max_chunks, snap_stride, t.err, t.chunk_off, t.snap_off,
-        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_k_heads) : 0);
+        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_k_heads) : 0,
+        zero_flags ? t.porder : nullptr);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     time_mark(1, stream);
     return GDN_OK;
@@ -1616,13 +1656,10 @@ gdn_status launch_chain(const gdn_problem &p, const TcPtrs &t, const TcMaps &m,
 // SMs the fused kernel can run on (one CTA each), or 0 when it cannot be
 // used on this device: no cooperative launch, a register count other than the
 // 96 its warpgroup budgets are split from, or less than one CTA per SM.
-// GDN_PREFILL_FUSED=0 in the environment turns it off.
 int fused_grid() {
     static int grid = -1;
     if (grid >= 0) return grid;
     grid = 0;
-    const char *env = getenv("GDN_PREFILL_FUSED");
-    if (env && env[0] == '0') return grid;
     int dev = 0, sms = 0, coop = 0, blocks = 0;
     cudaFuncAttributes fa;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1638,6 +1675,24 @@ int fused_grid() {
     }
     if (coop && fa.numRegs == 96 && blocks >= 1) grid = sms;
     return grid;
+}
+
+// Whether the fused kernel should beat the separate ones, from measured rates
+// on this GPU: a persistent prep unit takes ~27 us per (chunk, key head)
+// item, a wave of the separate prep kernel (two items per SM) ~21 us, a
+// recurrence chunk step ~1.3 us.  Fused: prep on the SMs the recurrences
+// leave, the recurrence following (it cannot finish before its last chunk is
+// prepped).  Separate: prep on every SM, then the recurrence.  The longest
+// sequence is estimated as T / N tokens (as long as T for one sequence).
+bool fused_pays(const gdn_problem &p, int grid) {
+    const int64_t n_chain = (int64_t)p.num_seqs * p.num_v_heads;
+    if (n_chain + 16 > grid) return false;
+    const int64_t chunks = (p.total_tokens + C - 1) / C + p.num_seqs - 1;
+    const int64_t items = chunks * p.num_k_heads;
+    const double chain = 1.3 * (double)((p.total_tokens / p.num_seqs + C - 1) / C);
+    const double prep_f = 27.0 * (double)((items + 2 * (grid - n_chain) - 1) / (2 * (grid - n_chain)));
+    const double prep_s = 21.0 * (double)((items + 2 * grid - 1) / (2 * grid));
+    return std::max(prep_f, chain + 27.0) < prep_s + chain + 5.0;
 }
 
 // Chunk table, then the fused kernel: prep and the recurrence in one launch.
@@ -1661,8 +1716,8 @@ bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, cons
     if (cudaLaunchKernelEx(&cfg, gdn_fused_kernel, m.tq, m.tk, m.tv, m.to, g, beta,
                            (const int *)t.chunk_off, (const int *)t.order, (const int4 *)t.table,
                            t.slots, t.gl, h0, static_cast<__nv_bfloat16 *>(out), hT, t.err,
-                           t.flags, p.num_seqs, p.num_k_heads, p.num_v_heads, n_chain,
-                           n_items) != cudaSuccess) {
+                           t.flags, (const int *)t.porder, p.num_seqs, p.num_k_heads,
+                           p.num_v_heads, n_chain, n_items) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -1684,10 +1739,12 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     // (programmatic dependent launch), except while per-kernel timing records
     // events between them.
     const bool pdl = !g_timing;
-    // One sequence whose (sequence x value head) recurrences leave SMs for
-    // prep: the fused kernel (not while per-kernel timing is on).
-    const int grid = (snaps || p.total_tokens == 0 || p.num_seqs != 1) ? 0 : fused_grid();
-    if (grid > 0 && p.num_seqs * p.num_v_heads + 16 <= grid) {
+    // (sequence x value head) recurrences that leave SMs for prep: the fused
+    // kernel.
+    const int grid = (snaps || p.total_tokens == 0) ? 0 : fused_grid();
+    const int mode = fused_mode();
+    if (grid > 0 && mode > 0 &&
+        (mode == 1 ? (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid : fused_pays(p, grid))) {
         gdn_status st = launch_table(p, w, t, cu, 0, true, stream);
         if (st != GDN_OK) return st;
         time_mark(2, stream);  // (no separate prep launch)

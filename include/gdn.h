@@ -117,12 +117,14 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem);
  * q and k must already be L2-normalised by the caller.  All tensor pointers
  * must be 16-byte aligned.
  *
- * For bf16, dk = dv = 128 and one sequence whose Hv recurrences leave at
- * least 16 SMs free, the intra-chunk prep and the recurrence run as one
- * cooperative launch: prep on the free SMs, publishing each chunk as it is
- * done, and the recurrence following it.  Otherwise they are separate
- * kernels.  The results are the same either way.  GDN_PREFILL_FUSED=0 in the
- * environment (read once) keeps them separate.
+ * For bf16 and dk = dv = 128, when the N x Hv recurrences leave at least 16
+ * SMs free, the intra-chunk prep and the recurrence run as one cooperative
+ * launch: prep on the free SMs, publishing each chunk as it is done (every
+ * sequence's chunk c before any chunk c + 1), and the recurrences following.  Otherwise they are separate
+ * kernels.  The results are the same either way.  By default the fused
+ * kernel is used when a cost model of the two paths expects it to be faster
+ * (long sequences with few (sequence, value head) pairs); see
+ * gdn_prefill_fused_mode.
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
                                      const void *q, const void *k, const void *v,
@@ -338,6 +340,14 @@ GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace, gdn_st
 GDN_API gdn_status gdn_prefill_timing(int32_t enable);
 GDN_API gdn_status gdn_prefill_kernel_ms(float *ms);
 GDN_API int32_t gdn_prefill_last_fused(void);
+
+/*
+ * Choice of the fused prep + recurrence kernel for later prefills (process
+ * wide): 0 never, 1 whenever it can run, 2 when expected to be faster (the
+ * default; the environment variable GDN_PREFILL_FUSED = 0, 1 or 2 sets the
+ * initial mode).  Any other value only queries.  Returns the previous mode.
+ */
+GDN_API int32_t gdn_prefill_fused_mode(int32_t mode);
 
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);

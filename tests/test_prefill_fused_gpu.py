@@ -1,0 +1,68 @@
+"""The fused prep + recurrence kernel against the separate kernels and the
+fp64 oracle.  Both paths run the same arithmetic per chunk, so their outputs
+and final states are equal bit for bit; the fused path is forced on for
+batches the cost model would send to the separate kernels."""
+import pytest
+import torch
+
+import gated_deltanet_linear_chunk_gb300 as gdn
+from gated_deltanet_linear_chunk_gb300 import inputs
+from gpu_util import TOL_BF16, f64, oracle_prefill, rel
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    gdn.gdn_prefill_fused_mode(2)
+
+
+def run(p, mode):
+    gdn.gdn_prefill_fused_mode(mode)
+    dev = torch.device("cuda")
+    gdn.gdn_prefill_timing(True)
+    out, fin = gdn.gdn_chunk_prefill(
+        p.q.to(dev), p.k.to(dev), p.v.to(dev), p.g.to(dev), p.beta.to(dev),
+        p.cu_seqlens.to(dev), None if p.initial_state is None else p.initial_state.to(dev),
+        output_final_state=True)
+    gdn.gdn_prefill_kernel_ms()
+    fused = gdn.gdn_prefill_last_fused()
+    gdn.gdn_prefill_timing(False)
+    torch.cuda.synchronize()
+    return out, fin, fused
+
+
+@pytest.mark.parametrize("lens,Hk,Hv", [
+    ([130, 1, 64, 0, 77, 400], 2, 6),   # ragged, empty and one-token sequences
+    ([1000], 1, 3),
+    ([2000, 2000], 4, 12),
+    ([300, 2500, 900], 8, 24),
+])
+def test_fused_equals_separate_and_oracle(lens, Hk, Hv):
+    p = inputs.prefill_inputs(lens, Hk, Hv, 128, 128, dtype=torch.bfloat16, seed=21,
+                              initial_state_std=0.02)
+    o1, f1, fused1 = run(p, 1)
+    o0, f0, fused0 = run(p, 0)
+    assert fused1 and not fused0
+    assert torch.equal(o1, o0), "outputs differ between the fused and separate kernels"
+    assert torch.equal(f1, f0), "final states differ"
+    o_ref, f_ref, vh = oracle_prefill(p)
+    e_o, e_f = rel(f64(o1[:, vh]), o_ref), rel(f64(f1[:, vh]), f_ref)
+    print(f"[parity] fused lens={lens} {Hk}/{Hv}: out {e_o:.3e} final {e_f:.3e}")
+    assert e_o <= TOL_BF16 and e_f <= TOL_BF16
+
+
+def test_fused_mode_query_and_default():
+    old = gdn.gdn_prefill_fused_mode(-1)
+    assert old in (0, 1, 2)
+    assert gdn.gdn_prefill_fused_mode(2) == old
+    assert gdn.gdn_prefill_fused_mode(7) == 2   # out of range: query only
+    p = inputs.prefill_inputs([4000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
+    _, _, fused = run(p, 2)
+    assert fused, "the cost model picks the fused kernel for one 4000-token sequence"
+    p = inputs.prefill_inputs([2000, 2000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
+    _, _, fused = run(p, 2)
+    assert not fused, "two sequences x 48 heads leave too few SMs for prep"
