@@ -28,7 +28,7 @@ __all__ = [
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
     "gdn_prefill_timing", "gdn_prefill_kernel_ms", "gdn_prefill_last_fused",
-    "gdn_prefill_fused_mode",
+    "gdn_prefill_fused_mode", "gdn_chunk_prefill_host",
     "gdn_chunk_prefill_scan",
     "gdn_chunk_prefill_scan_workspace_size", "Problem",
     "GDN_BF16", "GDN_F32",
@@ -120,6 +120,8 @@ def library() -> ctypes.CDLL:
     lib.gdn_prefill_kernel_ms.argtypes = [P]
     lib.gdn_prefill_last_fused.restype = ctypes.c_int32
     lib.gdn_prefill_last_fused.argtypes = []
+    lib.gdn_chunk_prefill_host.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_host.argtypes = [PP, ctypes.c_int32] + [P] * 16 + [P]
     lib.gdn_prefill_fused_mode.restype = ctypes.c_int32
     lib.gdn_prefill_fused_mode.argtypes = [ctypes.c_int32]
     _lib = lib
@@ -142,6 +144,63 @@ def gdn_prefill_kernel_ms() -> Tuple[float, float, float]:
     if rc != 0:
         raise GDNError(rc, "gdn_prefill_kernel_ms")
     return float(ms[0]), float(ms[1]), float(ms[2])
+
+
+_staging = {}
+
+
+def gdn_chunk_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           g: torch.Tensor, beta: torch.Tensor, out: torch.Tensor,
+                           initial_state: Optional[torch.Tensor] = None,
+                           final_state: Optional[torch.Tensor] = None, pieces: int = 4,
+                           device=None, stream=None) -> torch.Tensor:
+    """Prefill of one sequence whose q, k, v, g, beta and out live in (pinned)
+    host memory; the transfers overlap the computation (see
+    ``gdn_chunk_prefill_host`` in include/gdn.h).  initial_state and
+    final_state, if given, are device tensors [1, Hv, dv, dk].  The device
+    staging buffers are kept by this module per shape.  Returns out."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported q/k/v dtype {dt}")
+    for t, name, tdt, shape in ((q, "q", dt, (T, Hk, dk)), (k, "k", dt, (T, Hk, dk)),
+                                (v, "v", dt, (T, Hv, dv)), (g, "g", torch.float32, (T, Hv)),
+                                (beta, "beta", torch.float32, (T, Hv)),
+                                (out, "out", dt, (T, Hv, dv))):
+        if t.device.type != "cpu" or t.dtype != tdt or tuple(t.shape) != shape or \
+                not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor {tdt} {shape}")
+    dev = torch.device(device if device is not None else "cuda")
+    key = (dev.index, T, Hk, Hv, dk, dv, dt)
+    st = _staging.get(key)
+    if st is None:
+        st = dict(q=torch.empty((T, Hk, dk), dtype=dt, device=dev),
+                  k=torch.empty((T, Hk, dk), dtype=dt, device=dev),
+                  v=torch.empty((T, Hv, dv), dtype=dt, device=dev),
+                  g=torch.empty((T, Hv), dtype=torch.float32, device=dev),
+                  beta=torch.empty((T, Hv), dtype=torch.float32, device=dev),
+                  out=torch.empty((T, Hv, dv), dtype=dt, device=dev),
+                  cu=torch.empty(128, dtype=torch.int32, device=dev),
+                  state=torch.empty((Hv, dv, dk), dtype=torch.float32, device=dev))
+        _staging.clear()
+        _staging[key] = st
+    for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
+        if t is not None:
+            _check(t, name, torch.float32, (1, Hv, dv, dk))
+    lib = library()
+    p = make_problem(1, T, Hk, Hv, dk, dv, dt)
+    need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
+    ws = _workspace(dev, need)
+    p = make_problem(1, T, Hk, Hv, dk, dv, dt, ws)
+    rc = lib.gdn_chunk_prefill_host(
+        ctypes.byref(p), int(pieces), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+        _ptr(initial_state), _ptr(final_state), _ptr(st["q"]), _ptr(st["k"]), _ptr(st["v"]),
+        _ptr(st["g"]), _ptr(st["beta"]), _ptr(st["out"]), _ptr(st["cu"]), _ptr(st["state"]),
+        _stream(stream))
+    if rc != 0:
+        raise GDNError(rc, "gdn_chunk_prefill_host")
+    return out
 
 
 def gdn_prefill_fused_mode(mode: int = -1) -> int:

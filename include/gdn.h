@@ -135,6 +135,45 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
                                      gdn_stream_t stream);
 
 /*
+ * gdn_chunk_prefill of ONE sequence from HOST memory, with the transfers
+ * overlapped with the computation.
+ *
+ * The sequence is cut into `pieces` pieces of whole 64-token chunks; the
+ * output is that of one gdn_chunk_prefill, because chunks restart every 64
+ * tokens and each piece starts from the previous piece's state.  Piece p's
+ * inputs are copied up on an upload stream while piece p - 1 is computed on
+ * `stream`, and its output is copied back on a download stream while piece
+ * p + 1 is computed.  Overlapping the link's two directions with the
+ * computation is how a host-resident prompt reaches the GPU fastest.
+ *
+ * Host buffers (pinned, or the copies do not overlap; layouts as above):
+ *   q_h, k_h, v_h, g_h, beta_h   inputs, read
+ *   out_h                        output, written
+ * Device buffers:
+ *   initial_state, final_state   as in gdn_chunk_prefill (NULL allowed)
+ *   q_d, k_d, v_d, g_d, beta_d, out_d   staging, full size, as the
+ *                                device tensors of gdn_chunk_prefill
+ *   cu_d                         scratch int32 [128], 16-byte aligned
+ *   state_d                      scratch fp32 [Hv, dv, dk], 16-byte aligned
+ *   problem->workspace           as for gdn_chunk_prefill of the whole problem
+ * Arguments:
+ *   problem   num_seqs must be 1
+ *   pieces    1-64; fewer when the sequence has fewer chunks
+ *
+ * On return everything is enqueued; `stream` completes after the last
+ * output byte is back in out_h.  The upload and download streams and their
+ * events are created once per process (on the device current at the first
+ * call), so calls must not run concurrently from several host threads.
+ * Returns GDN_ERR_INVALID_ARG for num_seqs != 1, a pieces value out of range
+ * or a missing buffer; otherwise the errors of gdn_chunk_prefill.
+ */
+GDN_API gdn_status gdn_chunk_prefill_host(
+    const gdn_problem *problem, int32_t pieces, const void *q_h, const void *k_h,
+    const void *v_h, const float *g_h, const float *beta_h, void *out_h,
+    const float *initial_state, float *final_state, void *q_d, void *k_d, void *v_d, float *g_d,
+    float *beta_d, void *out_d, int32_t *cu_d, float *state_d, gdn_stream_t stream);
+
+/*
  * Snapshot slots gdn_chunk_prefill_snapshots needs for this problem with
  * one snapshot every snapshot_chunks chunks: ceil((ceil(T / 64) + N) /
  * snapshot_chunks) + N, a bound on the batch's count (sum over sequences of

@@ -207,3 +207,14 @@ def test_scan_argument_errors(lib):
     assert scan(lib, prob(N=2, T=5000, Hk=16, Hv=48, ws=A, wsb=size(ctypes.byref(p), 4) - 16),
                 4) == WORKSPACE
     assert scan(lib, prob(N=0, T=0), 4) == OK
+
+
+def test_host_pipeline_argument_errors(lib):
+    def call(p, pieces):
+        return lib.gdn_chunk_prefill_host(ctypes.byref(p) if p is not None else None, pieces,
+                                          *([A] * 8), None, None, *([A] * 8), None)
+    assert call(None, 4) == INVALID
+    assert call(prob(N=2, T=128), 4) == INVALID     # one sequence only
+    assert call(prob(N=1, T=128), 0) == INVALID
+    assert call(prob(N=1, T=128), 65) == INVALID
+    assert call(prob(N=1, T=128, dtype=gdn.GDN_F16), 2) == UNSUPPORTED
