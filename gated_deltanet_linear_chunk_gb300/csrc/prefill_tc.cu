@@ -623,9 +623,12 @@ __device__ __forceinline__ void prep_unit(
             if ((bad = named_barrier_or(bar, kThreads, bad))) break;
         }
     if (kLoop && flags && !bad) {
-        __threadfence();
+        // Every thread's slot writes are ordered before the barrier; one
+        // thread that is not needed until the next item's epilogue makes them
+        // visible device-wide and publishes the flag, and the others go on.
         named_barrier(bar, kThreads);
-        if (tid == 0) {
+        if (tid == 128) {
+            __threadfence();
             asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)ch * Hk + hk),
                          "r"(epoch)
                          : "memory");
