@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional, Tuple
 
 import torch
@@ -146,7 +147,7 @@ def gdn_prefill_kernel_ms() -> Tuple[float, float, float]:
     return float(ms[0]), float(ms[1]), float(ms[2])
 
 
-_staging = {}
+_staging = threading.local()  # per host thread: .key, .bufs
 
 
 def gdn_chunk_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -158,7 +159,8 @@ def gdn_chunk_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     host memory; the transfers overlap the computation (see
     ``gdn_chunk_prefill_host`` in include/gdn.h).  initial_state and
     final_state, if given, are device tensors [1, Hv, dv, dk].  The device
-    staging buffers are kept by this module per shape.  Returns out."""
+    staging buffers are kept per host thread for the last shape, so calls
+    from several threads do not share them.  Returns out."""
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     dt = q.dtype
@@ -172,34 +174,46 @@ def gdn_chunk_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                 not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous host tensor {tdt} {shape}")
     dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    cs = _stream_obj(stream, dev)
     key = (dev.index, T, Hk, Hv, dk, dv, dt)
-    st = _staging.get(key)
+    st = getattr(_staging, "bufs", None) if getattr(_staging, "key", None) == key else None
+    done = getattr(_staging, "done", None)  # (stream handle, event) of the last call
     if st is None:
-        st = dict(q=torch.empty((T, Hk, dk), dtype=dt, device=dev),
-                  k=torch.empty((T, Hk, dk), dtype=dt, device=dev),
-                  v=torch.empty((T, Hv, dv), dtype=dt, device=dev),
-                  g=torch.empty((T, Hv), dtype=torch.float32, device=dev),
-                  beta=torch.empty((T, Hv), dtype=torch.float32, device=dev),
-                  out=torch.empty((T, Hv, dv), dtype=dt, device=dev),
-                  cu=torch.empty(128, dtype=torch.int32, device=dev),
-                  state=torch.empty((Hv, dv, dk), dtype=torch.float32, device=dev))
-        _staging.clear()
-        _staging[key] = st
+        if done is not None:
+            done[1].synchronize()  # the old buffers may still be in use
+            done = _staging.done = None
+        with torch.cuda.stream(cs):
+            st = dict(q=torch.empty((T, Hk, dk), dtype=dt, device=dev),
+                      k=torch.empty((T, Hk, dk), dtype=dt, device=dev),
+                      v=torch.empty((T, Hv, dv), dtype=dt, device=dev),
+                      g=torch.empty((T, Hv), dtype=torch.float32, device=dev),
+                      beta=torch.empty((T, Hv), dtype=torch.float32, device=dev),
+                      out=torch.empty((T, Hv, dv), dtype=dt, device=dev),
+                      cu=torch.empty(128, dtype=torch.int32, device=dev),
+                      state=torch.empty((Hv, dv, dk), dtype=torch.float32, device=dev))
+        _staging.key, _staging.bufs = key, st
+    elif done is not None and done[0] != cs.cuda_stream:
+        cs.wait_event(done[1])  # the last call on these buffers ran on another stream
     for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
         if t is not None:
             _check(t, name, torch.float32, (1, Hv, dv, dk))
     lib = library()
     p = make_problem(1, T, Hk, Hv, dk, dv, dt)
     need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
-    ws = _workspace(dev, need)
+    ws = _workspace(dev, need, cs)
     p = make_problem(1, T, Hk, Hv, dk, dv, dt, ws)
     rc = lib.gdn_chunk_prefill_host(
         ctypes.byref(p), int(pieces), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
         _ptr(initial_state), _ptr(final_state), _ptr(st["q"]), _ptr(st["k"]), _ptr(st["v"]),
         _ptr(st["g"]), _ptr(st["beta"]), _ptr(st["out"]), _ptr(st["cu"]), _ptr(st["state"]),
-        _stream(stream))
+        cs.cuda_stream)
     if rc != 0:
         raise GDNError(rc, "gdn_chunk_prefill_host")
+    ev = torch.cuda.Event()
+    ev.record(cs)
+    _staging.done = (cs.cuda_stream, ev)
     return out
 
 
@@ -261,17 +275,37 @@ def _check(t: torch.Tensor, name: str, dtype, shape) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+# Prefill scratch kept by this module, one per (device, stream, host thread):
+# calls that could run concurrently never share one, and each is allocated on
+# the stream that uses it, so the caching allocator reuses it only after that
+# stream's work.
 _workspaces = {}
 _NO_SNAPSHOTS = object()
 
 
-def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
+def _stream_obj(stream, device: torch.device):
+    """The torch stream object for `stream` (None: the current stream)."""
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if hasattr(stream, "cuda_stream"):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
+def _workspace_key(device: torch.device, stream) -> tuple:
+    dev = device.index if device.index is not None else torch.cuda.current_device()
+    dev = torch.device("cuda", dev)
+    return (dev.index, _stream_obj(stream, dev).cuda_stream, threading.get_ident())
+
+
+def _workspace(device: torch.device, nbytes: int, stream=None) -> Optional[torch.Tensor]:
     if nbytes == 0:
         return None
-    key = device.index if device.index is not None else torch.cuda.current_device()
+    key = _workspace_key(device, stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        with torch.cuda.stream(_stream_obj(stream, torch.device("cuda", key[0]))):
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=torch.device("cuda", key[0]))
         _workspaces[key] = ws
     return ws
 
@@ -334,7 +368,7 @@ def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, outp
     else:
         need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
     if workspace is None:
-        workspace = _workspace(q.device, need)
+        workspace = _workspace(q.device, need, stream)
     p = make_problem(N, T, Hk, Hv, dk, dv, dt, workspace)
     if scan_group is not None:
         rc = lib.gdn_chunk_prefill_scan(ctypes.byref(p), scan_group, _ptr(q), _ptr(k), _ptr(v),
@@ -416,13 +450,15 @@ def gdn_chunk_prefill_device_status(workspace: Optional[torch.Tensor] = None,
     stream and returns GDN_OK, GDN_ERR_INVALID_ARG (malformed cu_seqlens),
     GDN_ERR_TIMEOUT (a bounded device wait ran out) or GDN_ERR_CUDA.
     ``workspace``: the one the call used; by default the workspace this
-    module keeps for the current device, or with ``noalloc`` the built-in
+    module keeps for the current device, `stream` and host thread, or with
+    ``noalloc`` the built-in
     scratch of ``gdn_chunk_prefill_noalloc``."""
     if noalloc:
         ptr = None
     else:
         if workspace is None:
-            workspace = _workspaces.get(torch.cuda.current_device())
+            workspace = _workspaces.get(
+                _workspace_key(torch.device("cuda", torch.cuda.current_device()), stream))
             if workspace is None:
                 raise ValueError("no workspace: no prefill has run through this module")
         ptr = workspace.data_ptr()

@@ -19,21 +19,31 @@ namespace {
 using namespace gdn;
 
 constexpr int kMaxPieces = 64;
+constexpr int kMaxDevices = 64;
 
-// Streams and events of the pipeline, created once per process for the
-// device current at the first call (non-blocking streams; events without
-// timing).
+// Streams and events of the pipeline, one set per device, created at that
+// device's first call (non-blocking streams; events without timing).  Calls
+// on one device hold its mutex while they issue their work, so concurrent
+// callers never re-record an event another call is still about to wait on;
+// a wait takes the event as it stands when the wait is issued, so the next
+// call may re-record it at once.
 struct Pipe {
     cudaStream_t up = nullptr, down = nullptr;
     cudaEvent_t start = nullptr, up_done[kMaxPieces] = {}, comp_done[kMaxPieces] = {},
                 down_done = nullptr;
     bool ok = false;
+    std::once_flag once;
+    std::mutex mu;
 };
 
-Pipe &pipe() {
-    static Pipe p;
-    static std::once_flag once;
-    std::call_once(once, [] {
+Pipe g_pipes[kMaxDevices];
+
+// The current device's pipeline, or nullptr if it cannot be created.
+Pipe *pipe() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    Pipe &p = g_pipes[dev];
+    std::call_once(p.once, [&p] {
         bool ok = cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) == cudaSuccess &&
@@ -43,7 +53,7 @@ Pipe &pipe() {
                  cudaEventCreateWithFlags(&p.comp_done[i], cudaEventDisableTiming) == cudaSuccess;
         p.ok = ok;
     });
-    return p;
+    return p.ok ? &p : nullptr;
 }
 
 struct PieceLens {
@@ -84,8 +94,10 @@ GDN_API gdn_status gdn_chunk_prefill_host(
     const size_t v_row = (size_t)p.num_v_heads * p.head_dim_v * el;
     const size_t gb_row = (size_t)p.num_v_heads * 4;
     const size_t state_bytes = (size_t)p.num_v_heads * p.head_dim_v * p.head_dim_k * 4;
-    Pipe &pp = pipe();
-    if (!pp.ok) return GDN_ERR_CUDA;
+    Pipe *ppp = pipe();
+    if (!ppp) return GDN_ERR_CUDA;
+    Pipe &pp = *ppp;
+    std::lock_guard<std::mutex> lock(pp.mu);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
     // Piece boundaries at whole chunks.

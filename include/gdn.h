@@ -29,7 +29,8 @@
  * on the given stream.  Calls are reentrant.  The process-wide state is:
  *   - device attributes (SM count, whether the fused prefill kernel fits),
  *     cached on first use for the then-current device;
- *   - the opt-in timing events of gdn_prefill_timing.
+ *   - the opt-in timing events of gdn_prefill_timing;
+ *   - per device, the upload and download streams of gdn_chunk_prefill_host.
  *
  * Errors: argument errors are detected on the host before any launch and
  * leave every output untouched.  Launch failures return GDN_ERR_CUDA.  Faults
@@ -161,9 +162,10 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
  *   pieces    1-64; fewer when the sequence has fewer chunks
  *
  * On return everything is enqueued; `stream` completes after the last
- * output byte is back in out_h.  The upload and download streams and their
- * events are created once per process (on the device current at the first
- * call), so calls must not run concurrently from several host threads.
+ * output byte is back in out_h.  Each device has one upload and one download
+ * stream with their events, created at the first call on that device (the
+ * current device); calls on one device from several host threads take turns
+ * while they enqueue, and their transfers share those two streams.
  * Returns GDN_ERR_INVALID_ARG for num_seqs != 1, a pieces value out of range
  * or a missing buffer; otherwise the errors of gdn_chunk_prefill.
  */
