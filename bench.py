@@ -32,6 +32,8 @@ UNIT = "tokens/s/layer"
 PREFILL = dict(seqlens=[4000], Hk=16, Hv=48, d=128)
 DECODE = dict(N=64, Hk=16, Hv=48, d=128)
 L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
+WORKLOAD = ("GDN prefill, 1 sequence, T=4000, 16 key / 48 value heads, d_k=d_v=128, "
+            "bf16 q/k/v, fp32 g/beta/state, zero initial state")
 E2E_PIECES = 4                      # pieces of the end-to-end host-input prefill
 # Algorithmic work per token per value head (d = 128, C = 64, G = 3), the
 # triangle-aware chunked count: 6 d^2 + C (dk + dv) + C dv + 2 C dk / G + C^2 / 3.
@@ -243,7 +245,7 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "GDN prefill T=4000, 16 key / 48 value heads, d=128",
+        "config": {"workload": WORKLOAD, "parallelism": f"host cores ({threads} threads)",
                    "sample_tokens": tokens},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -507,8 +509,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "GDN prefill, 1 sequence, T=4000, 16 key / 48 value heads, "
-                               "d_k=d_v=128, bf16 q/k/v, fp32 g/beta/state, zero initial state",
+        "config": {"workload": WORKLOAD,
                    "l2": "flushed before every step (512 MB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches_per_step * args.steps,
