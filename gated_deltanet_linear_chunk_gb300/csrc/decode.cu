@@ -21,7 +21,8 @@
 // elements of a row (16-byte loads for an fp32 state with dk = 128, 8-byte
 // loads for a 16-bit one), the two dot products are warp-shuffle reductions,
 // and kDecodeRows rows are loaded before any is reduced so that every lane
-// keeps several loads in flight.  Loads and stores carry the streaming
+// keeps several loads in flight; the next batch of rows is loaded while the
+// current one is reduced and stored.  Loads and stores carry the streaming
 // (evict-first) hint: the state is touched once per step.
 #include <cuda_fp16.h>
 
@@ -129,11 +130,25 @@ gdn_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     const TIn *vrow = v + (size_t)nh * DV;
     TIn *orow = out + (size_t)nh * DV;
 
-    for (int r0 = warp * kDecodeRows; r0 < DV; r0 += kDecodeWarps * kDecodeRows) {
-        using IO = StateIO<TS, EPT>;
-        typename IO::Raw raw[kDecodeRows];
+    // Rows in batches of kDecodeRows per warp; the next batch is loaded
+    // before this one is reduced, updated and stored, so its loads are in
+    // flight meanwhile (the two batches are disjoint rows).
+    using IO = StateIO<TS, EPT>;
+    constexpr int kStep = kDecodeWarps * kDecodeRows;
+    typename IO::Raw raw[kDecodeRows], nxt[kDecodeRows];
+    if (warp * kDecodeRows < DV) {
 #pragma unroll
-        for (int r = 0; r < kDecodeRows; ++r) raw[r] = IO::load(S + (size_t)(r0 + r) * DK + lane * EPT);
+        for (int r = 0; r < kDecodeRows; ++r)
+            nxt[r] = IO::load(S + (size_t)(warp * kDecodeRows + r) * DK + lane * EPT);
+    }
+    for (int r0 = warp * kDecodeRows; r0 < DV; r0 += kStep) {
+#pragma unroll
+        for (int r = 0; r < kDecodeRows; ++r) raw[r] = nxt[r];
+        if (r0 + kStep < DV) {
+#pragma unroll
+            for (int r = 0; r < kDecodeRows; ++r)
+                nxt[r] = IO::load(S + (size_t)(r0 + kStep + r) * DK + lane * EPT);
+        }
         float vr = lane < kDecodeRows ? to_f32(vrow[r0 + lane]) : 0.f;
         float x[kDecodeRows], y[kDecodeRows];
 #pragma unroll
