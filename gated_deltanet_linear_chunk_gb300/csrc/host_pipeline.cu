@@ -94,6 +94,10 @@ GDN_API gdn_status gdn_chunk_prefill_host(
     const size_t v_row = (size_t)p.num_v_heads * p.head_dim_v * el;
     const size_t gb_row = (size_t)p.num_v_heads * 4;
     const size_t state_bytes = (size_t)p.num_v_heads * p.head_dim_v * p.head_dim_k * 4;
+    // The whole sequence's workspace covers every piece: check it before
+    // anything is enqueued.
+    const size_t need = gdn_chunk_prefill_workspace_size(&p);
+    if (need > 0 && (!p.workspace || p.workspace_bytes < need)) return GDN_ERR_WORKSPACE;
     Pipe *ppp = pipe();
     if (!ppp) return GDN_ERR_CUDA;
     Pipe &pp = *ppp;
@@ -122,6 +126,16 @@ GDN_API gdn_status gdn_chunk_prefill_host(
         cudaStreamWaitEvent(pp.down, pp.start, 0) != cudaSuccess)
         return GDN_ERR_CUDA;
 
+    // After an error, the caller's stream still waits for whatever the upload
+    // and download streams already hold, so no copy outlives the call's
+    // ordering (best effort: the first error is the one returned).
+    auto fail = [&](gdn_status st) {
+        if (cudaEventRecord(pp.up_done[0], pp.up) == cudaSuccess)
+            cudaStreamWaitEvent(cs, pp.up_done[0], 0);
+        if (cudaEventRecord(pp.down_done, pp.down) == cudaSuccess)
+            cudaStreamWaitEvent(cs, pp.down_done, 0);
+        return st;
+    };
     auto up = [&](void *dst, const void *src, size_t row, int i) {
         const size_t off = (size_t)bnd[i] * row, n = (size_t)lens.len[i] * row;
         return n == 0 || cudaMemcpyAsync(static_cast<uint8_t *>(dst) + off,
@@ -132,10 +146,10 @@ GDN_API gdn_status gdn_chunk_prefill_host(
         if (!up(q_d, q_h, qk_row, i) || !up(k_d, k_h, qk_row, i) || !up(v_d, v_h, v_row, i) ||
             !up(g_d, g_h, gb_row, i) || !up(beta_d, beta_h, gb_row, i) ||
             cudaEventRecord(pp.up_done[i], pp.up) != cudaSuccess)
-            return GDN_ERR_CUDA;
+            return fail(GDN_ERR_CUDA);
     }
     for (int i = 0; i < pieces; ++i) {
-        if (cudaStreamWaitEvent(cs, pp.up_done[i], 0) != cudaSuccess) return GDN_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, pp.up_done[i], 0) != cudaSuccess) return fail(GDN_ERR_CUDA);
         gdn_problem pi = p;
         pi.total_tokens = lens.len[i];
         const size_t o = (size_t)bnd[i];
@@ -145,19 +159,19 @@ GDN_API gdn_status gdn_chunk_prefill_host(
             static_cast<const uint8_t *>(v_d) + o * v_row, g_d + o * p.num_v_heads,
             beta_d + o * p.num_v_heads, cu_d + 2 * i, state_d,
             static_cast<uint8_t *>(out_d) + o * v_row, state_d, stream);
-        if (st != GDN_OK) return st;
+        if (st != GDN_OK) return fail(st);
         if (cudaEventRecord(pp.comp_done[i], cs) != cudaSuccess ||
             cudaStreamWaitEvent(pp.down, pp.comp_done[i], 0) != cudaSuccess)
-            return GDN_ERR_CUDA;
+            return fail(GDN_ERR_CUDA);
         const size_t n = (size_t)lens.len[i] * v_row;
         if (n && cudaMemcpyAsync(static_cast<uint8_t *>(out_h) + o * v_row,
                                  static_cast<const uint8_t *>(out_d) + o * v_row, n,
                                  cudaMemcpyDeviceToHost, pp.down) != cudaSuccess)
-            return GDN_ERR_CUDA;
+            return fail(GDN_ERR_CUDA);
     }
     if (final_state && cudaMemcpyAsync(final_state, state_d, state_bytes,
                                        cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
-        return GDN_ERR_CUDA;
+        return fail(GDN_ERR_CUDA);
     if (cudaEventRecord(pp.down_done, pp.down) != cudaSuccess ||
         cudaStreamWaitEvent(cs, pp.down_done, 0) != cudaSuccess)
         return GDN_ERR_CUDA;

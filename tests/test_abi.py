@@ -211,10 +211,18 @@ def test_scan_argument_errors(lib):
 
 def test_host_pipeline_argument_errors(lib):
     def call(p, pieces):
+        # problem, pieces, 6 host tensors, no initial/final state, 6 device
+        # staging buffers, cu, state, default stream; every case below is
+        # refused before anything is enqueued
         return lib.gdn_chunk_prefill_host(ctypes.byref(p) if p is not None else None, pieces,
-                                          *([A] * 8), None, None, *([A] * 8), None)
+                                          *([A] * 6), None, None, *([A] * 8), None)
     assert call(None, 4) == INVALID
     assert call(prob(N=2, T=128), 4) == INVALID     # one sequence only
     assert call(prob(N=1, T=128), 0) == INVALID
     assert call(prob(N=1, T=128), 65) == INVALID
     assert call(prob(N=1, T=128, dtype=gdn.GDN_F16), 2) == UNSUPPORTED
+    # the whole sequence's workspace is checked before anything is enqueued
+    need = lib.gdn_chunk_prefill_workspace_size(ctypes.byref(prob(N=1, T=128)))
+    assert need > 0
+    assert call(prob(N=1, T=128), 2) == WORKSPACE
+    assert call(prob(N=1, T=128, ws=A, wsb=need - 1), 2) == WORKSPACE
