@@ -51,3 +51,35 @@ def test_host_pipeline(pieces, T, Hk, Hv, h0):
         # the state products rounds S instead of S / sigma from there on: two
         # equally valid roundings, a few 2^-9 apart.
         assert d_o <= TOL_BF16 and d_f <= TOL_BF16
+
+
+@pytest.mark.parametrize("h0", [True, False])
+def test_host_pipeline_empty_sequence(h0):
+    """T = 0: nothing is copied or computed; the final state is the initial
+    state (or zero) and out stays empty."""
+    p = inputs.prefill_inputs([0], 2, 6, 128, 128, dtype=torch.bfloat16, seed=33,
+                              initial_state_std=0.02 if h0 else None)
+    dev = torch.device("cuda")
+    out = torch.empty((0, 6, 128), dtype=torch.bfloat16)
+    h0_d = p.initial_state.to(dev) if h0 else None
+    fin = torch.full((1, 6, 128, 128), 7.0, device=dev)
+    gdn.gdn_chunk_prefill_host(p.q, p.k, p.v, p.g, p.beta, out, h0_d, fin, pieces=4)
+    torch.cuda.synchronize()
+    if h0:
+        assert torch.equal(fin, h0_d)
+    else:
+        assert torch.count_nonzero(fin) == 0
+
+
+def test_device_prefill_all_sequences_empty_bf16():
+    """The tensor-core path with every sequence empty (T = 0, N = 2): the
+    final states are the initial states, bit for bit."""
+    p = inputs.prefill_inputs([0, 0], 2, 6, 128, 128, dtype=torch.bfloat16, seed=34,
+                              initial_state_std=0.02)
+    dev = torch.device("cuda")
+    out, fin = gdn.gdn_chunk_prefill(*[x.to(dev) for x in (p.q, p.k, p.v, p.g, p.beta,
+                                                            p.cu_seqlens, p.initial_state)],
+                                     output_final_state=True)
+    torch.cuda.synchronize()
+    assert out.numel() == 0
+    assert torch.equal(fin.cpu(), p.initial_state)
