@@ -34,7 +34,55 @@ DECODE = dict(N=64, Hk=16, Hv=48, d=128)
 L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
 WORKLOAD = ("GDN prefill, 1 sequence, T=4000, 16 key / 48 value heads, d_k=d_v=128, "
             "bf16 q/k/v, fp32 g/beta/state, zero initial state")
+L2_NOTE = "flushed before every step (512 MB write)"
 E2E_PIECES = 4                      # pieces of the end-to-end host-input prefill
+# The other two full-size prefill workloads, timed beside the headline one.
+EXTRA_PREFILLS = {
+    "t20480_initial_state": dict(
+        seqlens=[20480], h0=True,
+        workload="GDN prefill, 1 sequence, T=20480, 16 key / 48 value heads, d=128, bf16, "
+                 "initial state ~N(0,0.02), final state returned"),
+    "varlen_8_sequences": dict(
+        seqlens=[512, 1000, 2048, 4000, 6000, 8192, 16384, 32768], h0=True,
+        workload="GDN varlen prefill, 8 packed sequences {512..32768} (T=70904), 16 key / 48 "
+                 "value heads, d=128, bf16, per-sequence initial states, final states returned"),
+}
+
+
+def bench_config(world: int) -> dict:
+    """The config dict of both arms' lines (the same workload either way)."""
+    return {"workload": WORKLOAD, "l2": L2_NOTE,
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def cpu_provenance() -> dict:
+    """Host CPU model, the cores this process may run on, and the OpenMP
+    threads the oracle uses."""
+    import platform
+
+    import oracle
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    affinity = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "affinity_cores": affinity, "omp_threads": oracle.max_threads()}
 # Algorithmic work per token per value head (d = 128, C = 64, G = 3), the
 # triangle-aware chunked count: 6 d^2 + C (dk + dv) + C dv + 2 C dk / G + C^2 / 3.
 FLOPS_PER_TOKEN_HEAD = 6 * 128 ** 2 + 64 * 256 + 64 * 128 + 2 * 64 * 128 // 3 + 64 ** 2 // 3
@@ -221,6 +269,7 @@ def oracle_sample_prefill(tokens: int, num_threads: int = 0, min_seconds: float 
         dt = time.perf_counter() - t0
         if dt >= min_seconds or reps >= 200:
             break
+    # One OpenMP task per (sequence, value head): at most Hv threads work.
     return tokens * reps / dt, dt, min(threads, PREFILL["Hv"]), reps
 
 
@@ -245,10 +294,10 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": f"host cores ({threads} threads)",
-                   "sample_tokens": tokens},
+        "config": bench_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "sample_tokens": tokens,
+                         "timing": f"median over {args.steps} steps", **cpu_provenance()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -298,21 +347,22 @@ def run_ours(args, rank, world, local):
             ends[i].record(stream)
         torch.cuda.synchronize()
         barrier()
-        # Per-kernel times: the same steps again with the library recording
-        # events between its three launches on this stream (kept out of the
-        # headline steps: the extra records cost the call a few us), each
-        # step's times read after it.
-        gdn.gdn_prefill_timing(True)
+        # Per-kernel times: the same steps again through the timed entry
+        # point, which records events between its launches on this stream
+        # (kept out of the headline steps: the launches then go without
+        # programmatic dependent launch and the records cost a few us).
         kernel_ms, fused = [], []
+        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+               for _ in range(args.steps)]
         for i in range(args.steps):
             flush.zero_()
-            prefill()
-            kernel_ms.append(gdn.gdn_prefill_kernel_ms())
-            fused.append(gdn.gdn_prefill_last_fused())
-        gdn.gdn_prefill_timing(False)
+            _, _, f, _ = gdn.gdn_chunk_prefill_timed(dq, dk_, dv, dg, db, dcu, None, out=out,
+                                                     events=tev[i])
+            fused.append(f)
         torch.cuda.synchronize()
+        kernel_ms = [[ev[j].elapsed_time(ev[j + 1]) for j in range(3)] for ev in tev]
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_local = statistics.mean(step_ms)
+    ms_local = statistics.median(step_ms)
     ms = max_over_ranks(ms_local, dev)
     value = job_throughput(T, world, ms / 1e3)
     launches_per_step = gdn.prefill_launches(P["Hv"], P["d"], torch.bfloat16)
@@ -401,6 +451,28 @@ def run_ours(args, rank, world, local):
             "sequential_us": seq_us, "scan_us": scan_us, "speedup": seq_us / scan_us,
             "tokens_per_s_scan": 20480 / (scan_us / 1e6)}
         del ps, sa, sout
+    gdn._workspaces.clear()
+
+    # ---------------- the other full-size prefill workloads ----------------
+    extra = {}
+    for name, cfg in EXTRA_PREFILLS.items():
+        px = inputs.prefill_inputs_on_device(cfg["seqlens"], P["Hk"], P["Hv"], P["d"], P["d"],
+                                             dev, seed=0,
+                                             initial_state_std=0.02 if cfg["h0"] else None)
+        Tx = sum(cfg["seqlens"])
+        xout = torch.empty((Tx, P["Hv"], P["d"]), dtype=torch.bfloat16, device=dev)
+        xfin = torch.empty_like(px.initial_state) if px.initial_state is not None else None
+        xargs = (px.q, px.k, px.v, px.g, px.beta, px.cu_seqlens, px.initial_state)
+        x_us = median_us(lambda: gdn.gdn_chunk_prefill(*xargs, out=xout, final_state=xfin),
+                         n=10)
+        xflops = flops_of(Tx, P["Hv"])
+        extra[name] = {"workload": cfg["workload"], "us_per_call": x_us,
+                       "tokens_per_s_per_layer": Tx / (x_us / 1e6),
+                       "tflops": xflops / (x_us / 1e6) / 1e12,
+                       "frac_of_bf16_peak": xflops / (x_us / 1e6) / 1e12 / peak_tf,
+                       "flops_per_call": xflops,
+                       "inputs": "drawn on the device (torch generator, same recipe)"}
+        del px, xout, xfin, xargs
     gdn._workspaces.clear()
 
     # ---------------- end to end through host buffers ----------------
@@ -509,9 +581,9 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD,
-                   "l2": "flushed before every step (512 MB write)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(world),
+        "timing": {"ms_per_step": "median of the timed steps", "mean_ms": statistics.mean(step_ms),
+                   "min_ms": min(step_ms), "max_ms": max(step_ms)},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": traffic,
@@ -539,6 +611,7 @@ def run_ours(args, rank, world, local):
                              "bytes_per_step": dbytes16, "achieved_gbs": dec16_gbs,
                              "peak_gbs": peaks["hbm_gbs"], "frac": dec16_gbs / peaks["hbm_gbs"],
                              "speedup_vs_fp32_state": dec_us / dec16_us},
+        "prefill_other_workloads": extra,
         "prefill_with_snapshots": snap_res,
         "prefill_scan": scan_res,
         "verify": {"workload": "64 sequences x 8 tokens from one state, a state slot per "
@@ -550,7 +623,8 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = {
             "value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"first {args.ref_tokens} of the 4000 tokens, all 48 value heads, "
-                      f"{reps} repeats (fp64 token recurrence, {s:.1f} s wall)"}
+                      f"{reps} repeats (fp64 token recurrence, {s:.1f} s wall)",
+            **cpu_provenance()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -558,7 +632,7 @@ def run_ours(args, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256)

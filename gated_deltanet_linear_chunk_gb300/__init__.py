@@ -28,8 +28,7 @@ __all__ = [
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
-    "gdn_prefill_timing", "gdn_prefill_kernel_ms", "gdn_prefill_last_fused",
-    "gdn_prefill_fused_mode", "gdn_chunk_prefill_host",
+    "gdn_chunk_prefill_timed", "gdn_prefill_fused_mode", "gdn_chunk_prefill_host",
     "gdn_chunk_prefill_scan",
     "gdn_chunk_prefill_scan_workspace_size", "Problem",
     "GDN_BF16", "GDN_F32",
@@ -115,36 +114,14 @@ def library() -> ctypes.CDLL:
     lib.gdn_chunk_prefill_scan_workspace_size.argtypes = [PP, ctypes.c_int32]
     lib.gdn_chunk_prefill_scan.restype = ctypes.c_int
     lib.gdn_chunk_prefill_scan.argtypes = [PP, ctypes.c_int32] + [P] * 10
-    lib.gdn_prefill_timing.restype = ctypes.c_int
-    lib.gdn_prefill_timing.argtypes = [ctypes.c_int32]
-    lib.gdn_prefill_kernel_ms.restype = ctypes.c_int
-    lib.gdn_prefill_kernel_ms.argtypes = [P]
-    lib.gdn_prefill_last_fused.restype = ctypes.c_int32
-    lib.gdn_prefill_last_fused.argtypes = []
+    lib.gdn_chunk_prefill_timed.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_timed.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.gdn_chunk_prefill_host.restype = ctypes.c_int
     lib.gdn_chunk_prefill_host.argtypes = [PP, ctypes.c_int32] + [P] * 16 + [P]
     lib.gdn_prefill_fused_mode.restype = ctypes.c_int32
     lib.gdn_prefill_fused_mode.argtypes = [ctypes.c_int32]
     _lib = lib
     return lib
-
-
-def gdn_prefill_timing(enable: bool) -> None:
-    """Turns per-kernel event timing of the tensor-core prefill on or off (see
-    ``gdn_prefill_timing`` in include/gdn.h)."""
-    rc = library().gdn_prefill_timing(1 if enable else 0)
-    if rc != 0:
-        raise GDNError(rc, "gdn_prefill_timing")
-
-
-def gdn_prefill_kernel_ms() -> Tuple[float, float, float]:
-    """(chunk table, prep, recurrence) durations in ms of the last prefill
-    recorded while timing was on; waits for its events."""
-    ms = (ctypes.c_float * 3)()
-    rc = library().gdn_prefill_kernel_ms(ctypes.cast(ms, ctypes.c_void_p))
-    if rc != 0:
-        raise GDNError(rc, "gdn_prefill_kernel_ms")
-    return float(ms[0]), float(ms[1]), float(ms[2])
 
 
 _staging = threading.local()  # per host thread: .key, .bufs
@@ -199,16 +176,18 @@ def gdn_chunk_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
         if t is not None:
             _check(t, name, torch.float32, (1, Hv, dv, dk))
+    _same_device(dev, initial_state=initial_state, final_state=final_state)
     lib = library()
     p = make_problem(1, T, Hk, Hv, dk, dv, dt)
     need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
     ws = _workspace(dev, need, cs)
     p = make_problem(1, T, Hk, Hv, dk, dv, dt, ws)
-    rc = lib.gdn_chunk_prefill_host(
-        ctypes.byref(p), int(pieces), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
-        _ptr(initial_state), _ptr(final_state), _ptr(st["q"]), _ptr(st["k"]), _ptr(st["v"]),
-        _ptr(st["g"]), _ptr(st["beta"]), _ptr(st["out"]), _ptr(st["cu"]), _ptr(st["state"]),
-        cs.cuda_stream)
+    with torch.cuda.device(dev):
+        rc = lib.gdn_chunk_prefill_host(
+            ctypes.byref(p), int(pieces), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+            _ptr(initial_state), _ptr(final_state), _ptr(st["q"]), _ptr(st["k"]), _ptr(st["v"]),
+            _ptr(st["g"]), _ptr(st["beta"]), _ptr(st["out"]), _ptr(st["cu"]), _ptr(st["state"]),
+            cs.cuda_stream)
     if rc != 0:
         raise GDNError(rc, "gdn_chunk_prefill_host")
     ev = torch.cuda.Event()
@@ -222,12 +201,6 @@ def gdn_prefill_fused_mode(mode: int = -1) -> int:
     1 whenever possible, 2 when expected faster; default 2) and returns the
     previous mode; -1 only queries."""
     return int(library().gdn_prefill_fused_mode(int(mode)))
-
-
-def gdn_prefill_last_fused() -> bool:
-    """Whether the last prefill recorded with timing on ran prep and the
-    recurrence as one fused launch."""
-    return bool(library().gdn_prefill_last_fused())
 
 
 def gdn_status_string(code: int) -> str:
@@ -260,6 +233,16 @@ def _stream(stream) -> Optional[int]:
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _same_device(dev: torch.device, **tensors) -> None:
+    """Every given tensor must live on `dev` (the device the call runs on):
+    a tensor on another GPU would be read through pointers that mean nothing
+    on this one."""
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, but q is on {dev}: all tensors of a "
+                             "call must be on one device")
 
 
 def _check(t: torch.Tensor, name: str, dtype, shape) -> None:
@@ -335,9 +318,11 @@ def gdn_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 
 def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, output_final_state,
-             workspace, stream, snapshots, snapshot_chunks, scan_group=None):
-    """Checks, workspace and dispatch of both prefill entry points
-    (``snapshots``: _NO_SNAPSHOTS, None to allocate, or a tensor)."""
+             workspace, stream, snapshots, snapshot_chunks, scan_group=None, events=None):
+    """Checks, workspace and dispatch of the prefill entry points
+    (``snapshots``: _NO_SNAPSHOTS, None to allocate, or a tensor; ``events``:
+    four torch.cuda.Event for the timed call).  Every tensor must be on q's
+    device; the call runs with that device current."""
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     N = cu_seqlens.shape[0] - 1
@@ -359,45 +344,88 @@ def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, outp
         final_state = torch.empty((N, Hv, dv, dk), dtype=torch.float32, device=q.device)
     if final_state is not None:
         _check(final_state, "final_state", torch.float32, (N, Hv, dv, dk))
-    lib = library()
-    p = make_problem(N, T, Hk, Hv, dk, dv, dt)
-    if scan_group is not None:
-        need = int(lib.gdn_chunk_prefill_scan_workspace_size(ctypes.byref(p), scan_group))
-        if need == 0 and N > 0:
-            raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_prefill_scan")
-    else:
-        need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
-    if workspace is None:
-        workspace = _workspace(q.device, need, stream)
-    p = make_problem(N, T, Hk, Hv, dk, dv, dt, workspace)
-    if scan_group is not None:
-        rc = lib.gdn_chunk_prefill_scan(ctypes.byref(p), scan_group, _ptr(q), _ptr(k), _ptr(v),
-                                        _ptr(g), _ptr(beta), _ptr(cu_seqlens),
-                                        _ptr(initial_state), _ptr(out), _ptr(final_state),
-                                        _stream(stream))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, cu_seqlens=cu_seqlens,
+                 initial_state=initial_state, out=out, final_state=final_state,
+                 workspace=workspace,
+                 snapshots=None if snapshots is _NO_SNAPSHOTS else snapshots)
+    with torch.cuda.device(q.device):
+        lib = library()
+        p = make_problem(N, T, Hk, Hv, dk, dv, dt)
+        if scan_group is not None:
+            need = int(lib.gdn_chunk_prefill_scan_workspace_size(ctypes.byref(p), scan_group))
+            if need == 0 and N > 0:
+                raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_prefill_scan")
+        else:
+            need = int(lib.gdn_chunk_prefill_workspace_size(ctypes.byref(p)))
+        if workspace is None:
+            workspace = _workspace(q.device, need, stream)
+        p = make_problem(N, T, Hk, Hv, dk, dv, dt, workspace)
+        if scan_group is not None:
+            rc = lib.gdn_chunk_prefill_scan(ctypes.byref(p), scan_group, _ptr(q), _ptr(k),
+                                            _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                            _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                            _stream(stream))
+            if rc != 0:
+                raise GDNError(rc, "gdn_chunk_prefill_scan")
+            return out, final_state
+        if events is not None:
+            st = _stream_obj(stream, q.device)
+            for e in events:
+                e.record(st)  # creates the event (torch creates it lazily)
+            handles = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+            fused = ctypes.c_int32(0)
+            rc = lib.gdn_chunk_prefill_timed(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v),
+                                             _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                             _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                             ctypes.cast(handles, ctypes.c_void_p),
+                                             ctypes.addressof(fused), st.cuda_stream)
+            if rc != 0:
+                raise GDNError(rc, "gdn_chunk_prefill_timed")
+            return out, final_state, bool(fused.value)
+        if snapshots is _NO_SNAPSHOTS:
+            rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                       _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state),
+                                       _ptr(out), _ptr(final_state), _stream(stream))
+            if rc != 0:
+                raise GDNError(rc, "gdn_chunk_prefill")
+            return out, final_state
+        slots = int(lib.gdn_chunk_prefill_snapshot_slots(ctypes.byref(p), snapshot_chunks))
+        if slots == 0:
+            raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_prefill_snapshots")
+        if snapshots is None:
+            snapshots = torch.empty((slots, Hv, dv, dk), dtype=torch.float32, device=q.device)
+        _check(snapshots, "snapshots", torch.float32, (slots, Hv, dv, dk))
+        rc = lib.gdn_chunk_prefill_snapshots(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v),
+                                             _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                             _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                             _ptr(snapshots), snapshot_chunks, _stream(stream))
         if rc != 0:
-            raise GDNError(rc, "gdn_chunk_prefill_scan")
-        return out, final_state
-    if snapshots is _NO_SNAPSHOTS:
-        rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                   _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state), _ptr(out),
-                                   _ptr(final_state), _stream(stream))
-        if rc != 0:
-            raise GDNError(rc, "gdn_chunk_prefill")
-        return out, final_state
-    slots = int(lib.gdn_chunk_prefill_snapshot_slots(ctypes.byref(p), snapshot_chunks))
-    if slots == 0:
-        raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_prefill_snapshots")
-    if snapshots is None:
-        snapshots = torch.empty((slots, Hv, dv, dk), dtype=torch.float32, device=q.device)
-    _check(snapshots, "snapshots", torch.float32, (slots, Hv, dv, dk))
-    rc = lib.gdn_chunk_prefill_snapshots(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                         _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state),
-                                         _ptr(out), _ptr(final_state), _ptr(snapshots),
-                                         snapshot_chunks, _stream(stream))
-    if rc != 0:
-        raise GDNError(rc, "gdn_chunk_prefill_snapshots")
-    return out, final_state, snapshots
+            raise GDNError(rc, "gdn_chunk_prefill_snapshots")
+        return out, final_state, snapshots
+
+
+def gdn_chunk_prefill_timed(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            g: torch.Tensor, beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                            initial_state: Optional[torch.Tensor] = None,
+                            out: Optional[torch.Tensor] = None,
+                            final_state: Optional[torch.Tensor] = None,
+                            output_final_state: bool = False,
+                            events=None, workspace: Optional[torch.Tensor] = None,
+                            stream=None):
+    """``gdn_chunk_prefill`` with per-kernel timing (see
+    ``gdn_chunk_prefill_timed`` in include/gdn.h).  ``events``: four
+    torch.cuda.Event(enable_timing=True) (created if None), recorded before
+    the chunk table, after it, after prep and after the recurrence.  Returns
+    (out, final_state, fused, events); read the kernel times with
+    events[i].elapsed_time(events[i + 1]) after synchronising."""
+    if events is None:
+        events = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    if len(events) != 4:
+        raise ValueError("events must hold four torch.cuda.Event")
+    out, final_state, fused = _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out,
+                                       final_state, output_final_state, workspace, stream,
+                                       _NO_SNAPSHOTS, 0, events=events)
+    return out, final_state, fused, events
 
 
 def gdn_chunk_prefill_snapshots(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -497,10 +525,13 @@ def gdn_chunk_prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
         if t is not None:
             _check(t, name, torch.float32, (N, Hv, dv, dk))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, cu_seqlens=cu_seqlens,
+                 initial_state=initial_state, out=out, final_state=final_state)
     p = make_problem(N, T, Hk, Hv, dk, dv, dt)
-    rc = library().gdn_chunk_prefill_noalloc(
-        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
-        _ptr(initial_state), _ptr(out), _ptr(final_state), _stream(stream))
+    with torch.cuda.device(q.device):  # the built-in scratch of q's device
+        rc = library().gdn_chunk_prefill_noalloc(
+            ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+            _ptr(initial_state), _ptr(out), _ptr(final_state), _stream(stream))
     if rc != 0:
         raise GDNError(rc, "gdn_chunk_prefill_noalloc")
     return out, final_state
@@ -526,9 +557,11 @@ def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if out is None:
         out = torch.empty((N, Hv, dv), dtype=dt, device=q.device)
     _check(out, "out", dt, (N, Hv, dv))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, state=state, out=out)
     p = make_problem(N, N, Hk, Hv, dk, dv, dt)
-    rc = library().gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                   _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = library().gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                       _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
     if rc != 0:
         raise GDNError(rc, "gdn_decode_step")
     return out
@@ -558,10 +591,12 @@ def gdn_decode_step_half_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     if out is None:
         out = torch.empty((N, Hv, dv), dtype=dt, device=q.device)
     _check(out, "out", dt, (N, Hv, dv))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, state=state, out=out)
     p = make_problem(N, N, Hk, Hv, dk, dv, dt)
-    rc = library().gdn_decode_step_half_state(
-        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-        _STATE_DTYPES[state.dtype], _ptr(out), _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = library().gdn_decode_step_half_state(
+            ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+            _STATE_DTYPES[state.dtype], _ptr(out), _stream(stream))
     if rc != 0:
         raise GDNError(rc, "gdn_decode_step_half_state")
     return out
@@ -598,10 +633,12 @@ def gdn_verify_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
     if out is None:
         out = torch.empty((N, K, Hv, dv), dtype=dt, device=q.device)
     _check(out, "out", dt, (N, K, Hv, dv))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, state=state, slots=slots, out=out)
     p = make_problem(N, N * K, Hk, Hv, dk, dv, dt)
-    rc = library().gdn_verify_step(ctypes.byref(p), K, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                   _ptr(beta), _ptr(state), _ALL_STATE_DTYPES[state.dtype],
-                                   _ptr(slots), _ptr(out), _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = library().gdn_verify_step(ctypes.byref(p), K, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                       _ptr(beta), _ptr(state), _ALL_STATE_DTYPES[state.dtype],
+                                       _ptr(slots), _ptr(out), _stream(stream))
     if rc != 0:
         raise GDNError(rc, "gdn_verify_step")
     return out, slots

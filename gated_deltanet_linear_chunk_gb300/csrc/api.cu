@@ -57,7 +57,8 @@ gdn_status prefill_impl(const gdn_problem *problem, const void *q, const void *k
                         const float *g, const float *beta, const int32_t *cu_seqlens,
                         const float *initial_state, void *out, float *final_state, float *snaps,
                         int snap_stride, bool want_snaps, gdn_stream_t stream,
-                        int scan_group = -1) {
+                        int scan_group = -1, void *const *events = nullptr,
+                        int *fused = nullptr) {
     const gdn_status st = check_problem(problem);
     if (st != GDN_OK) return st;
     const gdn_problem &p = *problem;
@@ -84,7 +85,7 @@ gdn_status prefill_impl(const gdn_problem *problem, const void *q, const void *k
                                    final_state, st_);
     if (prefill_tc_supported(p))
         return launch_prefill_tc(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
-                                 snaps, snap_stride, st_);
+                                 snaps, snap_stride, st_, events, fused);
     return launch_prefill_simt(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
                                st_);
 }
@@ -208,14 +209,30 @@ GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace,
     return GDN_ERR_CUDA;
 }
 
-GDN_API gdn_status gdn_prefill_timing(int32_t enable) { return gdn::prefill_timing(enable != 0); }
-
-GDN_API gdn_status gdn_prefill_kernel_ms(float *ms) {
-    if (!ms) return GDN_ERR_INVALID_ARG;
-    return gdn::prefill_kernel_ms(ms);
+GDN_API gdn_status gdn_chunk_prefill_timed(const gdn_problem *problem, const void *q,
+                                           const void *k, const void *v, const float *g,
+                                           const float *beta, const int32_t *cu_seqlens,
+                                           const float *initial_state, void *out,
+                                           float *final_state, gdn_event_t const *events,
+                                           int32_t *fused, gdn_stream_t stream) {
+    if (!events || !events[0] || !events[1] || !events[2] || !events[3])
+        return GDN_ERR_INVALID_ARG;
+    if (fused) *fused = 0;
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    if (!prefill_tc_supported(*problem)) return GDN_ERR_UNSUPPORTED;
+    if (problem->num_seqs == 0 && problem->total_tokens == 0) {
+        // Nothing to launch: the four events mark the same point.
+        const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        for (int i = 0; i < 4; ++i)
+            if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) != cudaSuccess)
+                return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+    void *ev[4] = {events[0], events[1], events[2], events[3]};
+    return prefill_impl(problem, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                        nullptr, 1, false, stream, -1, ev, fused);
 }
-
-GDN_API int32_t gdn_prefill_last_fused(void) { return gdn::prefill_timed_fused() ? 1 : 0; }
 
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode) { return gdn::prefill_fused_mode(mode); }
 

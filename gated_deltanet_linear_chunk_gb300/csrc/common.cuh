@@ -68,16 +68,18 @@ gdn_status launch_prefill_scan(const gdn_problem &p, int chunks_per_group, const
                                const int32_t *cu, const float *h0, void *out, float *hT,
                                cudaStream_t stream);
 
-// Per-kernel timing of the tensor-core prefill (events around its launches).
-gdn_status prefill_timing(bool enable);
-gdn_status prefill_kernel_ms(float *ms);
-bool prefill_timed_fused();
+// Fused prep + recurrence mode: sets it (0, 1, 2) and returns the old one;
+// any other value only queries.
 int prefill_fused_mode(int mode);
 
+// events: null, or four caller-created events recorded on `stream` before
+// the chunk table, after it, after prep and after the recurrence; *fused
+// (if given) is set to whether prep and the recurrence ran as one launch.
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, const int32_t *cu_seqlens,
                              const float *h0, void *out, float *hT, float *snaps,
-                             int snap_stride, cudaStream_t stream);
+                             int snap_stride, cudaStream_t stream, void *const *events = nullptr,
+                             int *fused = nullptr);
 // Snapshot slots of a problem with one snapshot per snap_stride chunks (a
 // bound on the batch's count).
 int64_t prefill_tc_snapshot_slots(const gdn_problem &p, int snap_stride);

@@ -45,6 +45,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -1496,54 +1497,34 @@ cudaLaunchConfig_t pdl_config(dim3 grid, unsigned threads, size_t smem, cudaStre
     return cfg;
 }
 
-// Timing events (see gdn_prefill_timing): before the chunk table, after it,
-// after prep, after the recurrence.
-cudaEvent_t g_tev[4] = {};
-bool g_timing = false, g_timed = false, g_timed_fused = false;
+// Per-call timing (gdn_chunk_prefill_timed): caller-created events recorded
+// on the launching stream before the chunk table, after it, after prep and
+// after the recurrence (or the fused kernel); null when the call is not
+// timed.  Nothing about it outlives the call.
+struct Timing {
+    cudaEvent_t ev[4];
+    int *fused;  // set to 1 when prep and the recurrence ran as one launch
+};
 
-void time_mark(int i, cudaStream_t s) {
-    if (g_timing) cudaEventRecord(g_tev[i], s);
+void time_mark(const Timing *tm, int i, cudaStream_t s) {
+    if (tm) cudaEventRecord(tm->ev[i], s);
+}
+
+void time_fused(const Timing *tm, bool fused) {
+    if (tm && tm->fused) *tm->fused = fused ? 1 : 0;
 }
 
 // Fused path mode (gdn_prefill_fused_mode): 0 off, 1 whenever it can run,
-// 2 when the cost model below expects it to be faster.  The environment
-// variable GDN_PREFILL_FUSED (0, 1 or 2) sets the initial mode.
-int g_fused_mode = -1;
+// 2 when the cost model below expects it to be faster.
+std::atomic<int> g_fused_mode{2};
 
-int fused_mode() {
-    if (g_fused_mode < 0) {
-        const char *env = getenv("GDN_PREFILL_FUSED");
-        g_fused_mode = (env && env[0] >= '0' && env[0] <= '2') ? env[0] - '0' : 2;
-    }
-    return g_fused_mode;
-}
-
+constexpr int kMaxDevices = 64;
 
 }  // namespace
 
-gdn_status prefill_timing(bool enable) {
-    if (enable && !g_tev[0]) {
-        for (auto &e : g_tev)
-            if (cudaEventCreate(&e) != cudaSuccess) return GDN_ERR_CUDA;
-    }
-    g_timing = enable;
-    return GDN_OK;
-}
-
-bool prefill_timed_fused() { return g_timed_fused; }
-
 int prefill_fused_mode(int mode) {
-    const int old = fused_mode();
-    if (mode >= 0 && mode <= 2) g_fused_mode = mode;
-    return old;
-}
-
-gdn_status prefill_kernel_ms(float *ms) {
-    if (!g_timed) return GDN_ERR_INVALID_ARG;
-    if (cudaEventSynchronize(g_tev[3]) != cudaSuccess) return GDN_ERR_CUDA;
-    for (int i = 0; i < 3; ++i)
-        if (cudaEventElapsedTime(&ms[i], g_tev[i], g_tev[i + 1]) != cudaSuccess) return GDN_ERR_CUDA;
-    return GDN_OK;
+    if (mode >= 0 && mode <= 2) return g_fused_mode.exchange(mode);
+    return g_fused_mode.load();
 }
 
 size_t prefill_tc_workspace_size(const gdn_problem &p) { return ws_layout(p).total; }
@@ -1595,20 +1576,22 @@ bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void 
 // The chunk table kernel (with `zero_flags`, it also clears the ready flags of
 // the fused kernel).
 gdn_status launch_table(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
-                        const int32_t *cu, int snap_stride, bool zero_flags, cudaStream_t stream) {
-    time_mark(0, stream);
+                        const int32_t *cu, int snap_stride, bool zero_flags, cudaStream_t stream,
+                        const Timing *tm) {
+    time_mark(tm, 0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(
         cu, p.num_seqs, p.total_tokens, w.max_chunks, snap_stride, t.err, t.chunk_off, t.snap_off,
         t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_k_heads) : 0,
         zero_flags ? t.porder : nullptr);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    time_mark(1, stream);
+    time_mark(tm, 1, stream);
     return GDN_OK;
 }
 
 // Prep (a programmatic dependent of the chunk table kernel).
 gdn_status launch_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, const TcMaps &m,
-                       const float *g, const float *beta, cudaStream_t stream, bool pdl) {
+                       const float *g, const float *beta, cudaStream_t stream, bool pdl,
+                       const Timing *tm) {
     if (p.total_tokens > 0) {
         const size_t smem = sizeof(PrepSmem) + 1024;
         if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1622,15 +1605,16 @@ gdn_status launch_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
                                t.err, p.num_seqs, p.num_k_heads, p.num_v_heads) != cudaSuccess)
             return GDN_ERR_CUDA;
     }
-    time_mark(2, stream);
+    time_mark(tm, 2, stream);
     return GDN_OK;
 }
 
 gdn_status launch_table_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
                              const TcMaps &m, const float *g, const float *beta,
-                             const int32_t *cu, int snap_stride, cudaStream_t stream, bool pdl) {
-    const gdn_status st = launch_table(p, w, t, cu, snap_stride, false, stream);
-    return st != GDN_OK ? st : launch_prep(p, w, t, m, g, beta, stream, pdl);
+                             const int32_t *cu, int snap_stride, cudaStream_t stream, bool pdl,
+                             const Timing *tm = nullptr) {
+    const gdn_status st = launch_table(p, w, t, cu, snap_stride, false, stream, tm);
+    return st != GDN_OK ? st : launch_prep(p, w, t, m, g, beta, stream, pdl, tm);
 }
 
 // The recurrence kernel over the chunk table of `p` (a programmatic
@@ -1656,17 +1640,25 @@ gdn_status launch_chain(const gdn_problem &p, const TcPtrs &t, const TcMaps &m,
     return GDN_OK;
 }
 
-// SMs the fused kernel can run on (one CTA each), or 0 when it cannot be
-// used on this device: no cooperative launch, a register count other than the
-// 96 its warpgroup budgets are split from, or less than one CTA per SM.
+// SMs the fused kernel can run on (one CTA each) on the current device, or 0
+// when it cannot be used there: no cooperative launch, a register count other
+// than the 96 its warpgroup budgets are split from, or less than one CTA per
+// SM.  Looked up once per device (the kernel's shared-memory attribute is set
+// with that device current), under a lock.
 int fused_grid() {
-    static int grid = -1;
-    if (grid >= 0) return grid;
-    grid = 0;
-    int dev = 0, sms = 0, coop = 0, blocks = 0;
+    static std::mutex mu;
+    static int grid_of[kMaxDevices];
+    static bool known[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (known[dev]) return grid_of[dev];
+    int sms = 0, coop = 0, blocks = 0, grid = 0;
     cudaFuncAttributes fa;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
         cudaFuncSetAttribute(gdn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFusedSmemBytes) != cudaSuccess ||
@@ -1674,9 +1666,11 @@ int fused_grid() {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gdn_fused_kernel, kFusedThreads,
                                                       kFusedSmemBytes) != cudaSuccess) {
         cudaGetLastError();
-        return grid;
+    } else if (coop && fa.numRegs == 96 && blocks >= 1) {
+        grid = sms;
     }
-    if (coop && fa.numRegs == 96 && blocks >= 1) grid = sms;
+    grid_of[dev] = grid;
+    known[dev] = true;
     return grid;
 }
 
@@ -1732,42 +1726,48 @@ bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, cons
 gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, const int32_t *cu,
                              const float *h0, void *out, float *hT, float *snaps,
-                             int snap_stride, cudaStream_t stream) {
+                             int snap_stride, cudaStream_t stream, void *const *events,
+                             int *fused) {
+    Timing timing;
+    const Timing *tm = nullptr;
+    if (events) {
+        for (int i = 0; i < 4; ++i) timing.ev[i] = static_cast<cudaEvent_t>(events[i]);
+        timing.fused = fused;
+        tm = &timing;
+    }
+    time_fused(tm, false);
     if (p.num_seqs == 0) return GDN_OK;
     const WsLayout w = ws_layout(p);
     const TcPtrs t = tc_ptrs(w, p.workspace);
     TcMaps m;
     if (!encode_maps(p, q, k, v, out, m)) return GDN_ERR_CUDA;
     // The prep and recurrence launches overlap their predecessor's tail
-    // (programmatic dependent launch), except while per-kernel timing records
-    // events between them.
-    const bool pdl = !g_timing;
+    // (programmatic dependent launch), except in a timed call, whose events
+    // sit between them.
+    const bool pdl = tm == nullptr;
     // (sequence x value head) recurrences that leave SMs for prep: the fused
     // kernel.
     const int grid = (snaps || p.total_tokens == 0) ? 0 : fused_grid();
-    const int mode = fused_mode();
+    const int mode = prefill_fused_mode(-1);
     if (grid > 0 && mode > 0 &&
         (mode == 1 ? (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid : fused_pays(p, grid))) {
-        gdn_status st = launch_table(p, w, t, cu, 0, true, stream);
+        gdn_status st = launch_table(p, w, t, cu, 0, true, stream, tm);
         if (st != GDN_OK) return st;
-        time_mark(2, stream);  // (no separate prep launch)
+        time_mark(tm, 2, stream);  // (no separate prep launch)
         if (launch_fused(p, w, t, m, g, beta, h0, out, hT, grid, stream)) {
-            time_mark(3, stream);
-            if (g_timing) g_timed = g_timed_fused = true;
+            time_mark(tm, 3, stream);
+            time_fused(tm, true);
             return GDN_OK;
         }
-        st = launch_prep(p, w, t, m, g, beta, stream, false);
+        st = launch_prep(p, w, t, m, g, beta, stream, false, tm);
         if (st != GDN_OK) return st;
         st = launch_chain<false, false>(p, t, m, m.to, h0, out, hT, nullptr, 1, stream, false);
         if (st != GDN_OK) return st;
-        time_mark(3, stream);
-        if (g_timing) {
-            g_timed = true;
-            g_timed_fused = false;
-        }
+        time_mark(tm, 3, stream);
         return GDN_OK;
     }
-    gdn_status st = launch_table_prep(p, w, t, m, g, beta, cu, snaps ? snap_stride : 0, stream, pdl);
+    gdn_status st =
+        launch_table_prep(p, w, t, m, g, beta, cu, snaps ? snap_stride : 0, stream, pdl, tm);
     if (st != GDN_OK) return st;
     CUtensorMap ts = m.to;
     if (snaps && !encode_states(&ts, snaps,
@@ -1776,11 +1776,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     st = snaps ? launch_chain<true, false>(p, t, m, ts, h0, out, hT, snaps, snap_stride, stream, pdl)
                : launch_chain<false, false>(p, t, m, ts, h0, out, hT, nullptr, 1, stream, pdl);
     if (st != GDN_OK) return st;
-    time_mark(3, stream);
-    if (g_timing) {
-        g_timed = true;
-        g_timed_fused = false;
-    }
+    time_mark(tm, 3, stream);
     return GDN_OK;
 }
 
@@ -1821,12 +1817,18 @@ size_t prefill_scan_workspace_size(const gdn_problem &p, int chunks_per_group) {
 }
 
 int prefill_scan_auto_group(const gdn_problem &p) {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            sms = 148;
+    // SM count of the current device, looked up once per device.
+    static std::atomic<int> sms_of[kMaxDevices];
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        sms = sms_of[dev].load();
+        if (sms == 0) {
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                sms = 148;
+            sms_of[dev].store(sms);
+        }
+    } else {
+        cudaGetLastError();
     }
     // Enough groups that groups x value heads about fills the SMs once.
     const int64_t chunks = (p.total_tokens + C - 1) / C + p.num_seqs;

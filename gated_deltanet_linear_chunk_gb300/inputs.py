@@ -192,6 +192,37 @@ def prefill_inputs(seqlens, Hk: int, Hv: int, dk: int, dv: int,
     return PrefillInputs(q, k, v, g, beta, torch.from_numpy(cu), h0)
 
 
+def prefill_inputs_on_device(seqlens, Hk: int, Hv: int, dk: int, dv: int, device,
+                             dtype: torch.dtype = torch.bfloat16, seed: int = 0,
+                             initial_state_std: Optional[float] = None) -> PrefillInputs:
+    """The same recipe as prefill_inputs, drawn with torch's seeded generator
+    on `device` (fp32 arithmetic): for timing large workloads, where the
+    host generator would take tens of seconds.  The values differ from
+    prefill_inputs'; the parity tests use prefill_inputs."""
+    seqlens = [int(s) for s in seqlens]
+    T = sum(seqlens)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+
+    def normal_(*shape):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32)
+
+    def unit(x):
+        return (x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)).to(dtype)
+
+    q = unit(normal_(T, Hk, dk))
+    k = unit(normal_(T, Hk, dk))
+    v = normal_(T, Hv, dv).to(dtype)
+    beta = torch.sigmoid(normal_(T, Hv))
+    g = -0.1 * torch.nn.functional.softplus(normal_(T, Hv))
+    h0 = None
+    if initial_state_std is not None:
+        h0 = initial_state_std * normal_(len(seqlens), Hv, dv, dk)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]), dtype=torch.int32, device=dev)
+    return PrefillInputs(q, k, v, g.contiguous(), beta.contiguous(), cu, h0)
+
+
 @dataclass
 class DecodeStepInputs:
     q: torch.Tensor     # [N, Hk, dk]

@@ -27,10 +27,14 @@
  * Ownership and threading: the caller owns every buffer.  The library never
  * allocates device memory, never frees, never synchronises, and launches only
  * on the given stream.  Calls are reentrant.  The process-wide state is:
- *   - device attributes (SM count, whether the fused prefill kernel fits),
- *     cached on first use for the then-current device;
- *   - the opt-in timing events of gdn_prefill_timing;
- *   - per device, the upload and download streams of gdn_chunk_prefill_host.
+ *   - per device, an attribute cache (SM count, whether the fused prefill
+ *     kernel fits and its launch attribute), filled once per device under a
+ *     lock;
+ *   - the fused-path mode of gdn_prefill_fused_mode (an atomic integer);
+ *   - per device, the upload and download streams of gdn_chunk_prefill_host
+ *     (created at its first call on that device);
+ *   - per device, the address of gdn_chunk_prefill_noalloc's built-in
+ *     scratch array.
  *
  * Errors: argument errors are detected on the host before any launch and
  * leave every output untouched.  Launch failures return GDN_ERR_CUDA.  Faults
@@ -359,34 +363,40 @@ GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_problem *problem,
  */
 GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace, gdn_stream_t stream);
 
+/* Same type as cudaEvent_t. */
+typedef struct CUevent_st *gdn_event_t;
+
 /*
- * Per-kernel timing of the tensor-core prefill (bf16, d = 128), for
- * measurement; off by default and free when off.  While on, each such prefill
- * records CUDA events on its stream before and after its three launches
- * (chunk table, prep, recurrence); gdn_prefill_kernel_ms waits for the last
- * recorded call's events and returns the three durations.  The events belong
- * to the device current when timing was first enabled; one caller at a time.
- *   gdn_prefill_timing(enable): nonzero creates the events (once) and turns
- *       recording on, 0 turns it off.  GDN_ERR_CUDA if the events cannot be
- *       created.
- *   gdn_prefill_kernel_ms(ms): ms[0], ms[1], ms[2] = chunk table, prep and
- *       recurrence of the last recorded call, in milliseconds.  When that
- *       call ran prep and the recurrence as one fused launch (see
- *       gdn_chunk_prefill), ms[1] is 0 and ms[2] is the fused kernel.
- *       GDN_ERR_INVALID_ARG if ms is NULL or no call was recorded,
- *       GDN_ERR_CUDA if the events cannot be read.
- *   gdn_prefill_last_fused(): 1 if the last recorded call ran the fused
- *       kernel, else 0.
+ * gdn_chunk_prefill with per-kernel timing, for measurement.  The call
+ * records four caller-created CUDA events on `stream`: events[0] before the
+ * chunk-table kernel, events[1] after it, events[2] after the prep kernel and
+ * events[3] after the recurrence.  The launches are then made without
+ * programmatic dependent launch, so each pair of events brackets one kernel.
+ * When prep and the recurrence run as one fused launch (see
+ * gdn_chunk_prefill), events[1] and events[2] mark the same point and
+ * events[3] follows the fused kernel; *fused (if not NULL) is set to 1 in
+ * that case and 0 otherwise.  With no sequences the four events are recorded
+ * back to back.  Nothing is kept between calls: calls on several streams or
+ * threads time themselves independently.
+ *   events   four valid events (cudaEventCreate), owned by the caller;
+ *            GDN_ERR_INVALID_ARG if the array or an event is NULL
+ * Only for bf16 q/k/v with dk = dv = 128 (otherwise GDN_ERR_UNSUPPORTED).
+ * Everything else as gdn_chunk_prefill.
  */
-GDN_API gdn_status gdn_prefill_timing(int32_t enable);
-GDN_API gdn_status gdn_prefill_kernel_ms(float *ms);
-GDN_API int32_t gdn_prefill_last_fused(void);
+GDN_API gdn_status gdn_chunk_prefill_timed(const gdn_problem *problem,
+                                           const void *q, const void *k, const void *v,
+                                           const float *g, const float *beta,
+                                           const int32_t *cu_seqlens,
+                                           const float *initial_state,
+                                           void *out, float *final_state,
+                                           gdn_event_t const *events, int32_t *fused,
+                                           gdn_stream_t stream);
 
 /*
  * Choice of the fused prep + recurrence kernel for later prefills (process
- * wide): 0 never, 1 whenever it can run, 2 when expected to be faster (the
- * default; the environment variable GDN_PREFILL_FUSED = 0, 1 or 2 sets the
- * initial mode).  Any other value only queries.  Returns the previous mode.
+ * wide, an atomic integer): 0 never, 1 whenever it can run, 2 when expected
+ * to be faster (the default).  Any other value only queries.  Returns the
+ * previous mode.
  */
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode);
 

@@ -27,12 +27,36 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def run_prefill(p: inputs.PrefillInputs, final=True, device="cuda"):
+def poison_workspace(p: inputs.PrefillInputs, dev) -> None:
+    """Fills the binding's cached prefill workspace for this problem (created
+    if needed) with 0xFF bytes, which read as NaN in every float field: a
+    kernel that reads scratch it did not write this call shows up as NaN."""
+    T, Hk, dk = p.q.shape
+    Hv, dv = p.v.shape[1:]
+    need = gdn.gdn_chunk_prefill_workspace_size(p.cu_seqlens.shape[0] - 1, T, Hk, Hv, dk, dv,
+                                                p.q.dtype)
+    ws = gdn._workspace(dev, need)
+    if ws is not None:
+        ws.fill_(0xFF)
+
+
+def run_prefill(p: inputs.PrefillInputs, final=True, device="cuda", poison=True):
+    """The prefill through the binding; with `poison`, out, the final state
+    and the workspace start as NaN, so any element the call fails to write
+    (or any stale scratch it reads) fails the comparison."""
     dev = torch.device(device)
+    T, Hv, dv = p.v.shape
+    N, dk = p.cu_seqlens.shape[0] - 1, p.q.shape[2]
+    out = fin = None
+    if poison:
+        out = torch.full((T, Hv, dv), float("nan"), dtype=p.q.dtype, device=dev)
+        if final:
+            fin = torch.full((N, Hv, dv, dk), float("nan"), dtype=torch.float32, device=dev)
+        poison_workspace(p, dev)
     out, fin = gdn.gdn_chunk_prefill(
         p.q.to(dev), p.k.to(dev), p.v.to(dev), p.g.to(dev), p.beta.to(dev),
         p.cu_seqlens.to(dev), None if p.initial_state is None else p.initial_state.to(dev),
-        output_final_state=final)
+        out=out, final_state=fin, output_final_state=final)
     torch.cuda.synchronize()
     return out, fin
 
@@ -61,6 +85,7 @@ def check_prefill(p: inputs.PrefillInputs, tol: float, key_heads=None):
     e_out = rel(f64(out[:, vh]), o_ref)
     e_fin = rel(f64(fin[:, vh]), f_ref)
     assert np.isfinite(f64(out)).all(), "non-finite output"
+    assert np.isfinite(f64(fin)).all(), "non-finite final state"
     assert e_out <= tol, f"out rel err {e_out:.3e} > {tol:.0e}"
     assert e_fin <= tol, f"final state rel err {e_fin:.3e} > {tol:.0e}"
     print(f"[parity] T={p.q.shape[0]} N={p.cu_seqlens.shape[0] - 1} dtype={p.q.dtype} "

@@ -227,6 +227,31 @@ def check_decode_equals_prefill(lib, seed=8) -> float:
     return max(err, rel(S, fin))
 
 
+def check_decode_gqa_grouping(lib, seed=9) -> float:
+    """Decode with 2 key / 6 value heads: value head h reads key head
+    h // (Hv/Hk), so each value head of one batched step equals a 1-key /
+    1-value step on its own key head (contiguous groups; the same reading as
+    the prefill's).  Three steps, each from the batched call's state."""
+    rng = np.random.default_rng(seed)
+    N, Hk, Hv, d = 3, 2, 6, 4
+    S = rng.standard_normal((N, Hv, d, d))
+    err = 0.0
+    for _ in range(3):
+        q = unit(rng.standard_normal((N, Hk, d)))
+        k = unit(rng.standard_normal((N, Hk, d)))
+        v = rng.standard_normal((N, Hv, d))
+        g = -rng.uniform(0, 0.5, (N, Hv))
+        b = rng.uniform(0, 1, (N, Hv))
+        out, S_new = oracle.decode(q, k, v, g, b, S, lib=lib)
+        for h in range(Hv):
+            hk = h // (Hv // Hk)
+            o1, s1 = oracle.decode(q[:, hk:hk + 1], k[:, hk:hk + 1], v[:, h:h + 1],
+                                   g[:, h:h + 1], b[:, h:h + 1], S[:, h:h + 1].copy(), lib=lib)
+            err = max(err, rel(out[:, h], o1[:, 0]), rel(S_new[:, h], s1[:, 0]))
+        S = S_new
+    return err
+
+
 ALL_CHECKS = {
     "beta_zero_decay": (check_beta_zero_decay, 1e-13),
     "orthonormal_retrieval": (check_orthonormal_retrieval, 1e-13),
@@ -236,4 +261,5 @@ ALL_CHECKS = {
     "exact_rational": (check_exact_rational, 1e-13),
     "gqa_grouping": (check_gqa_grouping, 0.0),
     "decode_equals_prefill": (check_decode_equals_prefill, 0.0),
+    "decode_gqa_grouping": (check_decode_gqa_grouping, 0.0),
 }

@@ -176,12 +176,32 @@ def test_binding_rejects_cpu_tensors(lib):
                             torch.zeros(4, 1, 128, 128))
 
 
-def test_prefill_timing_argument_errors(lib):
-    """Off needs no device; reading times needs a recorded call and a buffer."""
-    assert lib.gdn_prefill_timing(0) == OK
-    assert lib.gdn_prefill_kernel_ms(None) == INVALID
-    buf = (ctypes.c_float * 3)()
-    assert lib.gdn_prefill_kernel_ms(ctypes.cast(buf, ctypes.c_void_p)) == INVALID
+def test_timed_prefill_argument_errors(lib):
+    """Checks that need no device: the events array and each event must be
+    given, and only the tensor-core configuration is timed."""
+    timed = lib.gdn_chunk_prefill_timed
+
+    def call(p, events):
+        return timed(ctypes.byref(p), A, A + 4096, A + 8192, A + 12288, A + 16384, A + 20480,
+                     None, A + 24576, None, events, None, None)
+    p = prob(N=1, T=64)
+    assert call(p, None) == INVALID
+    missing = (ctypes.c_void_p * 4)(A, A, None, A)
+    assert call(p, ctypes.cast(missing, ctypes.c_void_p)) == INVALID
+    fake = (ctypes.c_void_p * 4)(A, A, A, A)
+    assert call(prob(N=1, T=64, dtype=gdn.GDN_F32), ctypes.cast(fake, ctypes.c_void_p)) == \
+        UNSUPPORTED
+    assert call(prob(N=1, T=64, dk=64, dv=64), ctypes.cast(fake, ctypes.c_void_p)) == \
+        UNSUPPORTED
+
+
+def test_fused_mode_needs_no_device(lib):
+    """The mode switch is a plain atomic: set, query, restore."""
+    old = lib.gdn_prefill_fused_mode(-1)
+    assert old in (0, 1, 2)
+    assert lib.gdn_prefill_fused_mode(0) == old
+    assert lib.gdn_prefill_fused_mode(9) == 0
+    assert lib.gdn_prefill_fused_mode(old) == 0
 
 
 def scan(lib, p, L, out=A + 24576):
@@ -226,3 +246,15 @@ def test_host_pipeline_argument_errors(lib):
     assert need > 0
     assert call(prob(N=1, T=128), 2) == WORKSPACE
     assert call(prob(N=1, T=128, ws=A, wsb=need - 1), 2) == WORKSPACE
+
+
+def test_binding_rejects_tensors_on_another_device():
+    """Every tensor of a call must be on q's device: the check runs before
+    any pointer reaches the library (shown here with meta and CPU tensors,
+    which need no GPU)."""
+    q = torch.empty(2, 1, 128, device="meta")
+    with pytest.raises(ValueError, match="one device"):
+        gdn._same_device(torch.device("cuda", 0), k=q)
+    with pytest.raises(ValueError, match="one device"):
+        gdn._same_device(torch.device("cuda", 1), v=torch.empty(1))
+    gdn._same_device(torch.device("cpu"), k=torch.empty(1), out=None)

@@ -27,6 +27,8 @@ MUTANTS = {
     "query_is_key": ("y += row[j] * q[j]", "y += row[j] * k[j]"),
     "gqa_interleaved": ("const int64_t hk = h / group;\n        double *S",
                         "const int64_t hk = h % Hk;\n        double *S"),
+    "decode_gqa_interleaved": ("const int64_t hk = h / group;\n        gdn_token_step",
+                               "const int64_t hk = h % Hk;\n        gdn_token_step"),
     "decay_squared": ("const double a = exp(g);", "const double a = exp(2.0 * g);"),
     "drop_last_token": ("t < cu_seqlens[n + 1]; ++t", "t + 1 < cu_seqlens[n + 1]; ++t"),
     "ignore_initial_state": ("if (initial_state)\n", "if (0)\n"),

@@ -21,17 +21,19 @@ def _built():
 
 
 def run(p, mode):
+    """The timed entry point reports which path ran; its events bracket the
+    kernels in order."""
     gdn.gdn_prefill_fused_mode(mode)
     dev = torch.device("cuda")
-    gdn.gdn_prefill_timing(True)
-    out, fin = gdn.gdn_chunk_prefill(
+    out, fin, fused, ev = gdn.gdn_chunk_prefill_timed(
         p.q.to(dev), p.k.to(dev), p.v.to(dev), p.g.to(dev), p.beta.to(dev),
         p.cu_seqlens.to(dev), None if p.initial_state is None else p.initial_state.to(dev),
         output_final_state=True)
-    gdn.gdn_prefill_kernel_ms()
-    fused = gdn.gdn_prefill_last_fused()
-    gdn.gdn_prefill_timing(False)
     torch.cuda.synchronize()
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(t >= 0.0 for t in ms)
+    if fused:
+        assert ms[1] < 0.01, "no prep launch between events 1 and 2 on the fused path"
     return out, fin, fused
 
 
@@ -66,3 +68,16 @@ def test_fused_mode_query_and_default():
     p = inputs.prefill_inputs([2000, 2000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
     _, _, fused = run(p, 2)
     assert not fused, "two sequences x 48 heads leave too few SMs for prep"
+
+
+def test_timed_call_equals_plain_call():
+    """Timing changes only the launch attributes, never the results."""
+    p = inputs.prefill_inputs([700, 64], 2, 6, 128, 128, dtype=torch.bfloat16, seed=22,
+                              initial_state_std=0.02)
+    dev = torch.device("cuda")
+    args = [x.to(dev) for x in (p.q, p.k, p.v, p.g, p.beta, p.cu_seqlens)]
+    h0 = p.initial_state.to(dev)
+    o1, f1 = gdn.gdn_chunk_prefill(*args, h0, output_final_state=True)
+    o2, f2, _, _ = gdn.gdn_chunk_prefill_timed(*args, h0, output_final_state=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)

@@ -38,26 +38,28 @@ def test_zero_start_without_initial_state():
     check_prefill(p, TOL_BF16)
 
 
-def test_t4000_48_heads_sampled():
+def test_t4000_48_heads():
     """T=4000 (62 full chunks + 32), 16 key / 48 value heads, d=128, bf16,
-    zero start: every token of three key-head groups (9 value heads)."""
+    zero start: every token of every head."""
     p = inputs.prefill_inputs([4000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
-    check_prefill(p, TOL_BF16, key_heads=[0, 7, 15])
+    check_prefill(p, TOL_BF16)
 
 
-def test_t20480_initial_state_sampled():
-    """T=20480 (320 chunks), nonzero initial state ~N(0, 0.02^2), final state."""
+def test_t20480_initial_state():
+    """T=20480 (320 chunks), nonzero initial state ~N(0, 0.02^2), final state;
+    every head."""
     p = inputs.prefill_inputs([20480], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0,
                               initial_state_std=0.02)
-    check_prefill(p, TOL_BF16, key_heads=[3, 12])
+    check_prefill(p, TOL_BF16)
 
 
-def test_varlen_eight_sequences_sampled():
-    """8 packed sequences {512 .. 32768} (T=70904), per-sequence initial states."""
+def test_varlen_eight_sequences():
+    """8 packed sequences {512 .. 32768} (T=70904), per-sequence initial
+    states; every head."""
     lens = [512, 1000, 2048, 4000, 6000, 8192, 16384, 32768]
     p = inputs.prefill_inputs(lens, 16, 48, 128, 128, dtype=torch.bfloat16, seed=0,
                               initial_state_std=0.02)
-    check_prefill(p, TOL_BF16, key_heads=[5])
+    check_prefill(p, TOL_BF16)
 
 
 def test_split_prefill_equals_whole():
@@ -75,13 +77,13 @@ def test_split_prefill_equals_whole():
     o2, f2 = gdn.gdn_chunk_prefill(*[x[T1:].contiguous() for x in a], cu2, f1,
                                    output_final_state=True)
     torch.cuda.synchronize()
-    # Different chunk boundaries round differently: both runs are held to the
-    # oracle's tolerance, and to each other at twice that.
+    # A split at token 100 moves every later chunk boundary, so the two runs
+    # round differently and are not compared with each other; each is held
+    # to the oracle's tolerance on its own.
     o_ref, f_ref, _ = oracle_prefill(p)
+    assert rel(f64(whole), o_ref) <= TOL_BF16 and rel(f64(fin), f_ref) <= TOL_BF16
     assert rel(f64(torch.cat([o1, o2])), o_ref) <= TOL_BF16
     assert rel(f64(f2), f_ref) <= TOL_BF16
-    assert rel(f64(torch.cat([o1, o2])), f64(whole)) <= 2 * TOL_BF16
-    assert rel(f64(f2), f64(fin)) <= 2 * TOL_BF16
 
 
 def test_varlen_equals_separate_runs():
