@@ -234,6 +234,35 @@ GDN_API gdn_status gdn_chunk_prefill_timed(const gdn_problem *problem, const voi
                         nullptr, 1, false, stream, -1, ev, fused);
 }
 
+GDN_API gdn_status gdn_chunk_prefill_prep_only(const gdn_problem *problem, const void *q,
+                                               const void *k, const float *g,
+                                               const float *beta, const int32_t *cu_seqlens,
+                                               gdn_stream_t stream) {
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    const gdn_problem &p = *problem;
+    if (!prefill_tc_supported(p)) return GDN_ERR_UNSUPPORTED;
+    if (p.num_seqs == 0) return p.total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (p.total_tokens > 0 && (!q || !k || !g || !beta)) return GDN_ERR_INVALID_ARG;
+    if (any_misaligned({q, k, g, beta})) return GDN_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return GDN_ERR_MISALIGNED;
+    const size_t need = gdn_chunk_prefill_workspace_size(problem);
+    if (!p.workspace || p.workspace_bytes < need || !aligned16(p.workspace))
+        return GDN_ERR_WORKSPACE;
+    return launch_prefill_tc_prep_only(p, q, k, g, beta, cu_seqlens,
+                                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+GDN_API gdn_status gdn_chunk_prefill_prep_layout(const gdn_problem *problem, int64_t *layout) {
+    const gdn_status st = check_problem(problem);
+    if (st != GDN_OK) return st;
+    if (!layout) return GDN_ERR_INVALID_ARG;
+    if (!prefill_tc_supported(*problem)) return GDN_ERR_UNSUPPORTED;
+    prefill_tc_slot_layout(*problem, layout);
+    return GDN_OK;
+}
+
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode) { return gdn::prefill_fused_mode(mode); }
 
 GDN_API const char *gdn_status_string(gdn_status status) {

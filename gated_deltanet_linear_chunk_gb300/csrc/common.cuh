@@ -80,6 +80,13 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
                              const float *h0, void *out, float *hT, float *snaps,
                              int snap_stride, cudaStream_t stream, void *const *events = nullptr,
                              int *fused = nullptr);
+// Chunk table and prep only (diagnostics), and where prep's products lie in
+// the workspace: {slot array offset, slot bytes, W^T, T diag(b), P,
+// diag(e^gamma) Q, e^gamma, e^{gamma_L - gamma} offsets within a slot}.
+gdn_status launch_prefill_tc_prep_only(const gdn_problem &p, const void *q, const void *k,
+                                      const float *g, const float *beta, const int32_t *cu,
+                                      cudaStream_t stream);
+void prefill_tc_slot_layout(const gdn_problem &p, int64_t *layout);
 // Snapshot slots of a problem with one snapshot per snap_stride chunks (a
 // bound on the batch's count).
 int64_t prefill_tc_snapshot_slots(const gdn_problem &p, int snap_stride);

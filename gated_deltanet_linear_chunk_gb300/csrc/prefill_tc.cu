@@ -59,7 +59,6 @@ using namespace ptx;
 constexpr int C = 64;           // chunk length
 constexpr int D = 128;          // head dim (dk = dv)
 constexpr int kTile = 8192;     // bytes of one 64 x 64 bf16 swizzled tile
-constexpr int kThreads = 320;   // 10 warps: 0 loads, 1 MMAs, 2-9 epilogue
 constexpr int kMaxSortSeqs = 4096;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -91,10 +90,10 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.table = align_up(w.order + 4 * (size_t)p.num_seqs, 256);
     w.gl = align_up(w.table + 16 * (size_t)w.max_chunks, 256);  // e^{gamma_L} per (chunk, value head)
     w.tiles = align_up(w.gl + 4 * (size_t)w.max_chunks * p.num_v_heads, 1024);
-    // Ready flag per (chunk, key head) for the fused prep + recurrence kernel.
+    // Ready flag per (chunk, value head) for the fused prep + recurrence kernel.
     w.flags = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
     // and the order in which its prep units take the chunks.
-    w.porder = align_up(w.flags + 4 * (size_t)w.max_chunks * p.num_k_heads, 256);
+    w.porder = align_up(w.flags + 4 * (size_t)w.max_chunks * p.num_v_heads, 256);
     w.total = align_up(w.porder + 4 * (size_t)w.max_chunks, 256);
     return w;
 }
@@ -242,37 +241,44 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
 }
 
 // ------------------------------------------------------------------ kernel 2
-constexpr int kPrepHeads = 3;  // value heads handled per round
+// Intra-chunk prep, one (chunk, value head) item per unit of 128 threads
+// (four warps, one per TMEM lane quadrant).  Small units keep many items in
+// flight on an SM (five per CTA of the fused kernel, five CTAs per SM of the
+// separate kernel): an item is a chain of dependent steps (tile loads, four
+// MMA round trips, CUDA-core epilogues between barriers), and independent
+// items fill each other's waits.  The K K^T and Q K^T product is recomputed
+// for each value head of a key head; it is one small MMA.
+constexpr int kPrepThreads = 128;
+constexpr int kPrepUnits = 5;              // units per CTA of the fused kernel
+constexpr uint32_t kPrepTmemCols = 64;     // [K; Q] K^T, then N, Y and W^T in turn
 
-struct PrepSmem {
-    uint8_t kq[4 * kTile];                // atom 0: K rows 0-63 | Q rows 64-127; atom 1 likewise
-    uint8_t e[kPrepHeads][kTile];         // E (lower-left block of A), then T diag(b)
-    uint8_t dp[kPrepHeads][kTile];        // D' = blockdiag((I + A_bb)^-1)
-    uint8_t n[kPrepHeads][kTile];         // diagonal blocks of A (fp32), then N = D' E,
-                                          // then T diag(b e^gamma)
-    float gam[kPrepHeads][C];
-    float beta[kPrepHeads][C];
-    float eg[kPrepHeads][C];
-    float dec[kPrepHeads][C];
+struct alignas(1024) PrepSmem {
+    // K atom 0 | Q atom 0 | K atom 1 | Q atom 1 (two 64-column 128-byte-swizzled
+    // atoms each; stacked so that one M = 128 MMA gives K K^T and Q K^T).  Once
+    // diag(e^gamma) Q has been stored and the product is done, the Q atoms are
+    // reused: Q atom 0 holds A's two diagonal 32 x 32 blocks (fp32), then
+    // N = D' E (bf16); Q atom 1 holds D' (bf16).
+    uint8_t kq[4 * kTile];
+    uint8_t e[kTile];  // E (lower-left 32 x 32 block of A, bf16), then T diag(b e^gamma)
+    float gam[C];
+    float beta[C];
+    float eg[C];
+    float dec[C];
     uint64_t tma_bar;
     uint64_t mma_bar;
     uint32_t tmem;
 };
 
-// TMEM columns of the prep kernel.
-constexpr uint32_t kPColKQ = 0;    // [K K^T; Q K^T], M = 128, 64 columns
-constexpr uint32_t kPColProd = 64; // + 64 j: N then Y = N D' of head j (M = 64 layout)
-constexpr uint32_t kPColW = 64;    // + 64 j: W^T of head j (M = 128), after the products
-constexpr uint32_t kPrepTmemCols = 256;
-
-// The two fp32 diagonal 32 x 32 blocks of A live in a head's n buffer before
-// N is computed: row t of block b at float offset (32 b + t) * 32, its float4
-// group f stored at group f ^ (t % 8) (conflict-free row stores, broadcast
-// reads in the forward substitution).
+// The two fp32 diagonal 32 x 32 blocks of A live in Q atom 0: row t of block
+// b at float offset (32 b + t) * 32, its float4 group f stored at group
+// f ^ (t % 8) (conflict-free row stores, broadcast row reads).
 __device__ __forceinline__ float *ad_row(uint8_t *buf, int blk, int t) {
     return reinterpret_cast<float *>(buf) + (32 * blk + t) * 32;
 }
 __device__ __forceinline__ int ad_f4(int f, int t) { return (f ^ (t & 7)) * 4; }
+__device__ __forceinline__ float &ad_at(uint8_t *buf, int blk, int t, int i) {
+    return ad_row(buf, blk, t)[ad_f4(i >> 2, t) + (i & 3)];
+}
 
 // Writes 8 floats as one 16-byte bf16 chunk.
 __device__ __forceinline__ uint4 pack8(const float *x) {
@@ -299,12 +305,50 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
     for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
 }
 
-// One prep unit: kThreads threads with local index `ltid`, its own PrepSmem
-// and named barrier `bar`; it works through items item0, item0 + stride, ...
-// below n_items (item = chunk * Hk + key head, chunk-major).  With `flags`,
-// each finished item publishes `epoch` into flags[item] (release, device
-// scope) once its workspace slot writes are visible.  kLoop = false: exactly
-// one item (the per-chunk kernel), compiled without the loop.
+// L2 prefetch of what item (ch, h) will load: its K and Q tiles and its
+// g and beta values (64 tokens, one value head: strided, so every line is
+// fetched separately).  Called by one full warp.
+__device__ __forceinline__ void prep_prefetch(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                              const float *g, const float *beta, int tok0, int L,
+                                              int Hv, int h, int hk) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        tma_prefetch_3d(tm_k, 0, hk, tok0);
+        tma_prefetch_3d(tm_k, 64, hk, tok0);
+        tma_prefetch_3d(tm_q, 0, hk, tok0);
+        tma_prefetch_3d(tm_q, 64, hk, tok0);
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int t = 2 * lane + s;
+        if (t < L) {
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(g + (size_t)(tok0 + t) * Hv + h));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + (size_t)(tok0 + t) * Hv + h));
+        }
+    }
+}
+
+// One prep unit: kPrepThreads threads with local index `ltid` (the unit's
+// first warp is a multiple of 4, so warp w of the unit reads TMEM lane
+// quadrant w), its own PrepSmem, TMEM columns and named barrier `bar`.  It
+// works through items item0, item0 + stride, ... below n_items (item =
+// chunk * Hv + value head, chunk-major).  With `flags`, each finished item
+// publishes `epoch` into flags[chunk * Hv + h] (release, device scope) once
+// its workspace slot writes are visible.  kLoop = false: exactly one item
+// (blockIdx.x = chunk, blockIdx.y = value head), compiled without the loop.
+//
+// Per item:
+//   gamma = cumsum(g), b, e^gamma, e^{gamma_L - gamma};  [K; Q] K^T (M = 128);
+//   diag(e^gamma) Q to the slot;
+//   A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i), i < t: its diagonal 32 x 32
+//     blocks in fp32, its lower-left block E in bf16;
+//   P = M o Q K^T, M_ri = e^{gamma_r - gamma_i} (i <= r), to the slot;
+//   D' = blockdiag((I + A_bb)^-1), each 32 x 32 block from its two 16 x 16
+//     diagonal blocks (fp32 forward substitution) and the merge
+//     [[X1, 0], [-X2 C X1, X2]] (C the lower-left 16 x 16 block, fp32);
+//   T = (I + A)^-1 = D' - (D' E) D' (two M = 64 MMAs: with two blocks
+//     (D' E)^2 = 0, so the series stops there);
+//   T diag(b) to the slot, W^T = K^T (T diag(b e^gamma))^T (M = 128) to the slot.
 template <bool kLoop>
 __device__ __forceinline__ void prep_unit(
     PrepSmem &sm, const CUtensorMap *tm_q, const CUtensorMap *tm_k, const float *__restrict__ g,
@@ -314,11 +358,10 @@ __device__ __forceinline__ void prep_unit(
     int n_items, unsigned *flags, unsigned epoch, const int *__restrict__ porder = nullptr) {
     const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
-    // Epilogue warps 2-9: TMEM quadrant q (of the physical warp: lanes
-    // 32q..32q+31), column half.
-    const int q = (threadIdx.x >> 5) & 3, half = (warp - 2) >> 2;
-    const int c0 = 32 * half;
-    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const int q4 = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of the physical warp
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    uint8_t *const bufA = sm.kq + kTile;      // Q atom 0: A's diagonal blocks, then N
+    uint8_t *const bufD = sm.kq + 3 * kTile;  // Q atom 1: D'
 
     if (tid == 0) {
         prefetch_tensormap(tm_q);
@@ -329,12 +372,12 @@ __device__ __forceinline__ void prep_unit(
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, kPrepTmemCols);
-        // The permit is the CTA's: with two units in one CTA (kLoop) the
-        // other unit may still have to allocate.
+        // The permit is the CTA's: with several units in one CTA (kLoop) the
+        // others may still have to allocate.
         if (!kLoop) tmem_relinquish();
     }
     tc_fence_before();
-    named_barrier(bar, kThreads);
+    named_barrier(bar, kPrepThreads);
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
     bool bad = false;
@@ -342,15 +385,16 @@ __device__ __forceinline__ void prep_unit(
     const int n_ch = chunk_off[N];
 #pragma unroll 1
     for (int item = item0; item < n_items && !bad; item += stride) {
-    // (blockIdx when there is one item: registers the compiler can re-read)
-    const int ci = kLoop ? item / Hk : (int)blockIdx.x;
-    if (ci >= n_ch) break;  // chunk-major: every later item is past the table
-    const int ch = (kLoop && porder) ? porder[ci] : ci;
-    const int hk = kLoop ? item % Hk : (int)blockIdx.y;
-    const int4 e = table[ch];
-    const int tok0 = e.y, L = e.z;
+        const int ci = kLoop ? item / Hv : (int)blockIdx.x;
+        if (ci >= n_ch) break;  // chunk-major: every later item is past the table
+        const int ch = (kLoop && porder) ? porder[ci] : ci;
+        const int h = kLoop ? item % Hv : (int)blockIdx.y;
+        const int hk = h / G;
+        const int4 e = table[ch];
+        const int tok0 = e.y, L = e.z;
+        uint8_t *const slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
         if (tid == 0) {
-            // The previous item's generic reads of these tiles are ordered
+            // The previous item's generic accesses of these tiles are ordered
             // before the TMA writes (unit barrier, then this fence).
             if (kLoop) fence_proxy_async_smem();
             mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
@@ -359,291 +403,339 @@ __device__ __forceinline__ void prep_unit(
             tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, hk, tok0, &sm.tma_bar);
         }
-        // gamma, b and the decay factors of the first round of value heads,
-        // while the K and Q tiles are in flight.
-        auto head_gamma = [&](int j0, int nh) {
-            if (warp >= 1 && warp <= nh) {
-                const int j = warp - 1, h = hk * G + j0 + j;
-                chunk_gamma(g, tok0, L, Hv, h, sm.gam[j], sm.beta[j], beta, sm.eg[j], sm.dec[j]);
-                float *slot_f = reinterpret_cast<float *>(slots + ((size_t)ch * Hv + h) * kSlotBytes);
-                slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[j][2 * lane];
-                slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[j][2 * lane + 1];
-                slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[j][2 * lane];
-                slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[j][2 * lane + 1];
-                if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[j][C - 1];
+        if (warp == 1) {
+            // gamma, b and the decay factors while the tiles are in flight.
+            chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec);
+            float *slot_f = reinterpret_cast<float *>(slot);
+            slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[2 * lane];
+            slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[2 * lane + 1];
+            slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[2 * lane];
+            slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[2 * lane + 1];
+            if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[C - 1];
+        } else if (kLoop && warp == 2 && item + stride < n_items) {
+            // The next item's inputs into L2 while this one runs.
+            const int cn = (item + stride) / Hv;
+            if (cn < n_ch) {
+                const int chn = porder ? porder[cn] : cn;
+                const int hn = (item + stride) % Hv;
+                const int4 en = table[chn];
+                prep_prefetch(tm_q, tm_k, g, beta, en.y, en.z, Hv, hn, hn / G);
             }
-        };
-        head_gamma(0, min(kPrepHeads, G));
-        bad = !warp_wait(&sm.tma_bar, kLoop ? tph : 0, nullptr);
+        }
+        bad = !warp_wait(&sm.tma_bar, tph, nullptr);
         tph ^= 1;
+        named_barrier(bar, kPrepThreads);  // gamma & co. visible to the unit
         if (tid == 0 && !bad) {
             tc_fence_after();
             const uint32_t base = smem_u32(sm.kq);
             constexpr uint32_t id = idesc_bf16(128, 64, false, false);
-    #pragma unroll
+#pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = (k / 4) * (2 * kTile) + (k % 4) * 32;
-                mma_bf16(tmem + kPColKQ, smem_desc(base + off, 16, 1024),
-                         smem_desc(base + off, 16, 1024), id, k > 0);
+                mma_bf16(tmem, smem_desc(base + off, 16, 1024), smem_desc(base + off, 16, 1024),
+                         id, k > 0);
             }
             mma_commit(&sm.mma_bar);
         }
-        for (int j0 = 0; j0 < G; j0 += kPrepHeads) {
-            const int nh = min(kPrepHeads, G - j0);
-            if (j0 > 0) head_gamma(j0, nh);
-            if (j0 == 0) {
-                bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-                mph ^= 1;
-            }
-            tc_fence_after();
-            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
-            // ---- A blocks, E and P from the rows of [K K^T; Q K^T].
-            if (warp >= 2) {
-                const int row = 32 * q + lane;
-                float x[32];
-                tmem_ld32f(tmem + lane_base + kPColKQ + c0, x);
-                if (q < 2) {
-                    const int t = row;
-                    for (int j = 0; j < nh; ++j) {
-                        // Decay factors first (shared loads), then the stores.
-                        const float gt = sm.gam[j][t], bt = sm.beta[j][t];
-                        float av[32];
-    #pragma unroll
-                        for (int u = 0; u < 32; u += 4) {
-                            const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
-                            const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
-    #pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                const int i = c0 + u + w;
-                                av[u + w] = i < t ? bt * ex2_approx((gt - gi[w]) * kLog2e) * x[u + w] : 0.f;
-                            }
+        // ---- diag(e^gamma) Q to the slot (the same swizzled image as the Q
+        // atoms, scaled row by row), while the MMA runs.
+#pragma unroll 2
+        for (int idx = tid; idx < 2 * C * 8; idx += kPrepThreads) {
+            const int a = idx / (C * 8), r = (idx >> 3) & (C - 1), cc = idx & 7;
+            const uint32_t off = swz(r, cc);
+            float x[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm.kq + (2 * a + 1) * kTile + off), x);
+            const float sc = sm.eg[r];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] *= sc;
+            *reinterpret_cast<uint4 *>(slot + kSlotQ + a * kTile + off) = pack8(x);
+        }
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        mph ^= 1;
+        tc_fence_after();
+        // (every Q read is done: the Q atoms become bufA and bufD)
+        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
+        // ---- A's diagonal blocks (fp32) and E (bf16) from K K^T (lanes
+        // 0-63), P from Q K^T (lanes 64-127).  Warp-uniform branches: each
+        // warp holds one quadrant of rows.
+        {
+            const int row = 32 * q4 + lane;
+            float x[32];
+            if (q4 < 2) {
+                const int t = row, blk = q4;
+                const float gt = sm.gam[t], bt = sm.beta[t];
+                // Columns of this row's block half: the diagonal block.
+                tmem_ld32f(tmem + lane_base + 32 * blk, x);
+                {
+                    float *dst = ad_row(bufA, blk, t & 31);
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4) {
+                        float av[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int i = 32 * blk + u + w;
+                            av[w] = i < t ? bt * ex2_approx((gt - sm.gam[i]) * kLog2e) * x[u + w]
+                                          : 0.f;
                         }
-    #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            float ev[8];
-    #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const int i = c0 + 8 * cc + u;
-                                ev[u] = (t >= 32 && i < 32) ? av[8 * cc + u] : 0.f;
-                            }
-                            *reinterpret_cast<uint4 *>(sm.e[j] + swz(t, (c0 >> 3) + cc)) = pack8(ev);
-                        }
-                        if ((t >> 5) == half) {  // diagonal block: this thread's columns are in it
-                            float *dst = ad_row(sm.n[j], half, t & 31);
-    #pragma unroll
-                            for (int u = 0; u < 32; u += 4)
-                                *reinterpret_cast<float4 *>(dst + ad_f4(u >> 2, t)) =
-                                    make_float4(av[u], av[u + 1], av[u + 2], av[u + 3]);
-                        }
+                        *reinterpret_cast<float4 *>(dst + ad_f4(u >> 2, t)) =
+                            make_float4(av[0], av[1], av[2], av[3]);
+                    }
+                }
+                // E row t: columns 0-31 of rows 32-63 hold A, everything else 0.
+                const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+                if (blk == 1) {
+                    tmem_ld32f(tmem + lane_base, x);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float ev[8];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+                            ev[w] = bt * ex2_approx((gt - sm.gam[8 * cc + w]) * kLog2e) * x[8 * cc + w];
+                        *reinterpret_cast<uint4 *>(sm.e + swz(t, cc)) = pack8(ev);
                     }
                 } else {
-                    const int r = row - 64;
-                    for (int j = 0; j < nh; ++j) {
-                        const int h = hk * G + j0 + j;
-                        const float gr = sm.gam[j][r];
-                        float pv[32];
-    #pragma unroll
-                        for (int u = 0; u < 32; u += 4) {
-                            const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gam[j][c0 + u]);
-                            const float gi[4] = {g4.x, g4.y, g4.z, g4.w};
-    #pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                const int i = c0 + u + w;
-                                pv[u + w] = i <= r ? ex2_approx((gr - gi[w]) * kLog2e) * x[u + w] : 0.f;
-                            }
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4 *>(sm.e + swz(t, cc)) = z4;
+                }
+#pragma unroll
+                for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4 *>(sm.e + swz(t, cc)) = z4;
+            } else {
+                const int r = row - 64;
+                const float gr = sm.gam[r];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    // Rows 0-31 have nothing at columns 32-63 (i > r).
+                    if (hf == 1 && q4 == 2) {
+#pragma unroll
+                        for (int cc = 4; cc < 8; ++cc)
+                            *reinterpret_cast<uint4 *>(slot + kSlotP + swz(r, cc)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
+                    tmem_ld32f(tmem + lane_base + 32 * hf, x);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float pv[8];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const int i = 32 * hf + 8 * cc + w;
+                            pv[w] = i <= r ? ex2_approx((gr - sm.gam[i]) * kLog2e) * x[8 * cc + w]
+                                           : 0.f;
                         }
-                        uint8_t *pdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotP;
-    #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            *reinterpret_cast<uint4 *>(pdst + swz(r, (c0 >> 3) + cc)) = pack8(pv + 8 * cc);
+                        *reinterpret_cast<uint4 *>(slot + kSlotP + swz(r, 4 * hf + cc)) = pack8(pv);
                     }
                 }
             }
-            fence_proxy_async_smem();
-            named_barrier(bar, kThreads);
-            // ---- D' = blockdiag((I + A_bb)^-1): one column of one block per thread.
-            if (tid >= 64 && tid < 64 + 64 * nh) {
-                const int idx = tid - 64, j = idx >> 6, blk = (idx >> 5) & 1, col = idx & 31;
-                float xc[32];
-    #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    float a0 = (t == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                    const float *Ar = ad_row(sm.n[j], blk, t);
-    #pragma unroll
-                    for (int i = 0; i < (t & ~3); i += 4) {
-                        const float4 av = *reinterpret_cast<const float4 *>(Ar + ad_f4(i >> 2, t));
-                        a0 = fmaf(-av.x, xc[i], a0);
-                        a1 = fmaf(-av.y, xc[i + 1], a1);
-                        a2 = fmaf(-av.z, xc[i + 2], a2);
-                        a3 = fmaf(-av.w, xc[i + 3], a3);
-                    }
-    #pragma unroll
-                    for (int i = (t & ~3); i < t; ++i)
-                        a0 = fmaf(-Ar[ad_f4(i >> 2, t) + (i & 3)], xc[i], a0);
-                    xc[t] = (a0 + a1) + (a2 + a3);
-                }
-                const int ccol = 32 * blk + col;
-                uint8_t *dp = sm.dp[j];
-    #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    const float val = ((t >> 5) == blk) ? xc[t & 31] : 0.f;
-                    *reinterpret_cast<__nv_bfloat16 *>(dp + swz(t, ccol >> 3) + 2 * (ccol & 7)) =
-                        __float2bfloat16_rn(val);
-                }
-            } else if (tid < 64 || tid >= 256) {
-                // Meanwhile the other four warps write diag(e^gamma) Q of every
-                // value head of the round: the same swizzled image as Q's tiles,
-                // scaled row by row.
-                const int w = tid < 64 ? tid : tid - 192;  // 0 .. 127
-    #pragma unroll 8
-                for (int idx = w; idx < nh * 2 * C * 8; idx += 128) {
-                    const int j = idx / (2 * C * 8), a = (idx / (C * 8)) & 1;
-                    const int r = (idx >> 3) & (C - 1), cc = idx & 7;
-                    const uint32_t off = swz(r, cc);
-                    float x[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(sm.kq + (2 * a + 1) * kTile + off), x);
-                    const float sc = sm.eg[j][r];
-    #pragma unroll
-                    for (int u = 0; u < 8; ++u) x[u] *= sc;
-                    const int h = hk * G + j0 + j;
-                    *reinterpret_cast<uint4 *>(slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotQ +
-                                               a * kTile + off) = pack8(x);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_barrier(bar, kThreads);
-            // ---- N = D' E  (M = 64, N = 64, K = 64)
-            if (tid == 0) {
-                tc_fence_after();
-                constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-                for (int j = 0; j < nh; ++j) {
-                    const uint32_t a = smem_u32(sm.dp[j]), b = smem_u32(sm.e[j]);
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
-                                 smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
-                }
-                mma_commit(&sm.mma_bar);
-            }
-            bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-            mph ^= 1;
-            tc_fence_after();
-            if (warp >= 2) {
-                for (int j = 0; j < nh; ++j) {
-                    float x[32];
-                    tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, x);
-                    if (lane < 16) {
-                        const int r = 16 * q + lane;
-    #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            *reinterpret_cast<uint4 *>(sm.n[j] + swz(r, (c0 >> 3) + cc)) =
-                                pack8(x + 8 * cc);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
-            // ---- Y = N D'  (M = 64, N = 64, K = 64), into the same columns
-            if (tid == 0) {
-                tc_fence_after();
-                constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-                for (int j = 0; j < nh; ++j) {
-                    const uint32_t a = smem_u32(sm.n[j]), b = smem_u32(sm.dp[j]);
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(tmem + kPColProd + 64 * j, smem_desc(a + 32 * k, 16, 1024),
-                                 smem_desc(b + 2048 * k, kTile, 1024), id, k > 0);
-                }
-                mma_commit(&sm.mma_bar);
-            }
-            bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-            mph ^= 1;
-            tc_fence_after();
-            // ---- T = D' - Y;  T diag(b) -> e (and the workspace), T diag(b e^gamma) -> n
-            if (warp >= 2) {
-                for (int j = 0; j < nh; ++j) {
-                    float y[32];
-                    tmem_ld32f(tmem + lane_base + kPColProd + 64 * j + c0, y);
-                    if (lane < 16) {
-                        const int r = 16 * q + lane, h = hk * G + j0 + j;
-                        uint8_t *tdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotTB;
-    #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const uint32_t off = swz(r, (c0 >> 3) + cc);
-                            float dv[8], tb[8], tbg[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(sm.dp[j] + off), dv);
-    #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const int i = c0 + 8 * cc + u;
-                                tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[j][i];
-                                tbg[u] = tb[u] * sm.eg[j][i];
-                            }
-                            const uint4 wtb = pack8(tb);
-                            *reinterpret_cast<uint4 *>(sm.e[j] + off) = wtb;
-                            *reinterpret_cast<uint4 *>(sm.n[j] + off) = pack8(tbg);
-                            *reinterpret_cast<uint4 *>(tdst + off) = wtb;
-                        }
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
-            // ---- W^T = K^T (T diag(b e^gamma))^T  (M = 128 dk, N = 64, K = 64 tokens)
-            if (tid == 0) {
-                tc_fence_after();
-                constexpr uint32_t id = idesc_bf16(128, 64, true, false);
-                const uint32_t a = smem_u32(sm.kq);
-                for (int j = 0; j < nh; ++j) {
-                    const uint32_t b = smem_u32(sm.n[j]);
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(tmem + kPColW + 64 * j, smem_desc(a + 2048 * k, 2 * kTile, 1024),
-                                 smem_desc(b + 32 * k, 16, 1024), id, k > 0);
-                }
-                mma_commit(&sm.mma_bar);
-            }
-            bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-            mph ^= 1;
-            tc_fence_after();
-            if (warp >= 2) {
-                const int row = 32 * q + lane;  // key dimension
-                for (int j = 0; j < nh; ++j) {
-                    const int h = hk * G + j0 + j;
-                    float x[32];
-                    tmem_ld32f(tmem + lane_base + kPColW + 64 * j + c0, x);
-                    uint8_t *wdst = slots + ((size_t)ch * Hv + h) * kSlotBytes + kSlotWT;
-    #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        *reinterpret_cast<uint4 *>(wdst + swz(row, (c0 >> 3) + cc)) = pack8(x + 8 * cc);
-                }
-            }
-            tc_fence_before();
-            if ((bad = named_barrier_or(bar, kThreads, bad))) break;
         }
-    if (kLoop && flags && !bad) {
-        // Every thread's slot writes are ordered before the barrier; one
-        // thread that is not needed until the next item's epilogue makes them
-        // visible device-wide and publishes the flag, and the others go on.
-        named_barrier(bar, kThreads);
-        if (tid == 128) {
+        tc_fence_before();  // the TMEM reads above precede the next MMA's writes
+        fence_proxy_async_smem();
+        named_barrier(bar, kPrepThreads);
+        // ---- D': the four 16 x 16 diagonal blocks of I + A inverted by
+        // forward substitution, one column per thread (threads 0-63).
+        float xc[16];
+        const int fb = tid >> 4, fcol = tid & 15;  // 16-block (0..3) and column
+        const int fb32 = fb >> 1, foff = 16 * (fb & 1);
+        if (tid < 64) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                float a0 = (t == fcol) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                const int tr = foff + t;
+#pragma unroll
+                for (int i = 0; i < (t & ~3); i += 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(
+                        ad_row(bufA, fb32, tr) + ad_f4((foff + i) >> 2, tr));
+                    a0 = fmaf(-av.x, xc[i], a0);
+                    a1 = fmaf(-av.y, xc[i + 1], a1);
+                    a2 = fmaf(-av.z, xc[i + 2], a2);
+                    a3 = fmaf(-av.w, xc[i + 3], a3);
+                }
+#pragma unroll
+                for (int i = (t & ~3); i < t; ++i)
+                    a0 = fmaf(-ad_at(bufA, fb32, tr, foff + i), xc[i], a0);
+                xc[t] = (a0 + a1) + (a2 + a3);
+            }
+        }
+        named_barrier(bar, kPrepThreads);
+        // X1, X2 over A's diagonal 16 x 16 blocks (read by nobody any more).
+        if (tid < 64) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) ad_at(bufA, fb32, foff + t, foff + fcol) = xc[t];
+        }
+        named_barrier(bar, kPrepThreads);
+        // Y = C X1 per 32-block (C = rows 16-31, columns 0-15), into the
+        // block's unused upper-right 16 x 16 corner (nothing this step reads);
+        // each thread 4 columns.
+        const int mb = tid >> 6, mr = (tid >> 2) & 15, mc = 4 * (tid & 3);
+        {
+            float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float c = ad_at(bufA, mb, 16 + mr, j);
+                const float4 x1 = *reinterpret_cast<const float4 *>(ad_row(bufA, mb, j) +
+                                                                    ad_f4(mc >> 2, j));
+                y0 = fmaf(c, x1.x, y0);
+                y1 = fmaf(c, x1.y, y1);
+                y2 = fmaf(c, x1.z, y2);
+                y3 = fmaf(c, x1.w, y3);
+            }
+            *reinterpret_cast<float4 *>(ad_row(bufA, mb, mr) + ad_f4((16 + mc) >> 2, mr)) =
+                make_float4(y0, y1, y2, y3);
+        }
+        named_barrier(bar, kPrepThreads);
+        // -X2 Y into C's place (the block's lower-left corner, which this
+        // step does not read).
+        {
+            float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float x2 = ad_at(bufA, mb, 16 + mr, 16 + k);
+                const float4 y = *reinterpret_cast<const float4 *>(ad_row(bufA, mb, k) +
+                                                                   ad_f4((16 + mc) >> 2, k));
+                m0 = fmaf(-x2, y.x, m0);
+                m1 = fmaf(-x2, y.y, m1);
+                m2 = fmaf(-x2, y.z, m2);
+                m3 = fmaf(-x2, y.w, m3);
+            }
+            *reinterpret_cast<float4 *>(ad_row(bufA, mb, 16 + mr) + ad_f4(mc >> 2, 16 + mr)) =
+                make_float4(m0, m1, m2, m3);
+        }
+        named_barrier(bar, kPrepThreads);
+        // D' as a bf16 K-major image: row t = tid / 2, 32 columns per thread.
+        {
+            const int t = tid >> 1, hc = tid & 1, b = t >> 5, rr = t & 31;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float dv[8];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const int i = 32 * hc + 8 * cc + w;  // column in the 64-wide row
+                    const int ii = i & 31;
+                    const bool in = (i >> 5) == b && !(rr < 16 && ii >= 16);
+                    dv[w] = in ? ad_at(bufA, b, rr, ii) : 0.f;
+                }
+                *reinterpret_cast<uint4 *>(bufD + swz(t, 4 * hc + cc)) = pack8(dv);
+            }
+        }
+        fence_proxy_async_smem();
+        named_barrier(bar, kPrepThreads);
+        // ---- N = D' E  (M = 64, N = 64, K = 64)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+            const uint32_t a = smem_u32(bufD), b = smem_u32(sm.e);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, smem_desc(a + 32 * k, 16, 1024), smem_desc(b + 2048 * k, kTile, 1024),
+                         id, k > 0);
+            mma_commit(&sm.mma_bar);
+        }
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        mph ^= 1;
+        tc_fence_after();
+        // N to bufA (M = 64 layout: row 16 q + lane in lanes 0-15 of quadrant q).
+        {
+            float x[32];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                tmem_ld32f(tmem + lane_base + 32 * hf, x);
+                if (lane < 16) {
+                    const int r = 16 * q4 + lane;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        *reinterpret_cast<uint4 *>(bufA + swz(r, 4 * hf + cc)) = pack8(x + 8 * cc);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
+        // ---- Y = N D'  (M = 64, N = 64, K = 64)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+            const uint32_t a = smem_u32(bufA), b = smem_u32(bufD);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, smem_desc(a + 32 * k, 16, 1024), smem_desc(b + 2048 * k, kTile, 1024),
+                         id, k > 0);
+            mma_commit(&sm.mma_bar);
+        }
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        mph ^= 1;
+        tc_fence_after();
+        // ---- T = D' - Y;  T diag(b) to the slot, T diag(b e^gamma) to e.
+        {
+            float y[32];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                tmem_ld32f(tmem + lane_base + 32 * hf, y);
+                if (lane < 16) {
+                    const int r = 16 * q4 + lane;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t off = swz(r, 4 * hf + cc);
+                        float dv[8], tb[8], tbg[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(bufD + off), dv);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = 32 * hf + 8 * cc + u;
+                            tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[i];
+                            tbg[u] = tb[u] * sm.eg[i];
+                        }
+                        *reinterpret_cast<uint4 *>(slot + kSlotTB + off) = pack8(tb);
+                        *reinterpret_cast<uint4 *>(sm.e + off) = pack8(tbg);
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
+        // ---- W^T = K^T (T diag(b e^gamma))^T  (M = 128 dk, N = 64, K = 64 tokens)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(128, 64, true, false);
+            const uint32_t a = smem_u32(sm.kq), b = smem_u32(sm.e);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, smem_desc(a + 2048 * k, 2 * kTile, 1024),
+                         smem_desc(b + 32 * k, 16, 1024), id, k > 0);
+            mma_commit(&sm.mma_bar);
+        }
+        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        mph ^= 1;
+        tc_fence_after();
+        {
+            const int row = 32 * q4 + lane;  // key dimension
+            float x[32];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                tmem_ld32f(tmem + lane_base + 32 * hf, x);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(slot + kSlotWT + swz(row, 4 * hf + cc)) =
+                        pack8(x + 8 * cc);
+            }
+        }
+        tc_fence_before();
+        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
+        if (kLoop && flags && tid == 0) {
+            // Every thread's slot writes are ordered before the barrier; this
+            // thread makes them visible device-wide and publishes the flag.
             __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)ch * Hk + hk),
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)ch * Hv + h),
                          "r"(epoch)
                          : "memory");
         }
-    }
-    if (!kLoop) break;
+        if (!kLoop) break;
     }
     if (bad && tid == 0) atomicExch(err, kErrTimeout);
     tc_fence_before();
-    named_barrier(bar, kThreads);
+    named_barrier(bar, kPrepThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 5)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float *__restrict__ g, const float *__restrict__ beta,
                 const int *__restrict__ chunk_off, const int4 *__restrict__ table,
@@ -658,7 +750,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     griddep_launch_dependents();
     griddep_wait();
     if ((int)blockIdx.x >= chunk_off[N]) return;
-    const int item = blockIdx.x * Hk + blockIdx.y;
+    const int item = blockIdx.x * Hv + blockIdx.y;
     prep_unit<false>(sm, &tm_q, &tm_k, g, beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                      threadIdx.x, 1, item, 1, item + 1, nullptr, 0u);
 }
@@ -889,7 +981,7 @@ __device__ __forceinline__ void chain_role(
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
-                if (kFused && !wait_ready(flags + (size_t)(c_begin + c) * Hk + hk, &sm.abort))
+                if (kFused && !wait_ready(flags + (size_t)(c_begin + c) * Hv + h, &sm.abort))
                     break;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
@@ -1246,10 +1338,13 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // waits for the recurrence and all CTAs are resident (cooperative launch), so
 // every wait ends.  Prep runs on the SMs the recurrence leaves idle, during
 // the recurrence instead of before it.
-constexpr int kFusedThreads = 2 * kThreads;
-constexpr size_t kPrepUnitBytes = (sizeof(PrepSmem) + 1023) / 1024 * 1024;
+constexpr int kFusedThreads = kPrepUnits * kPrepThreads;
+constexpr size_t kPrepUnitBytes = sizeof(PrepSmem);  // a multiple of 1024 (alignas)
 constexpr size_t kFusedSmemBytes =
-    (sizeof(ChainSmem) > 2 * kPrepUnitBytes ? sizeof(ChainSmem) : 2 * kPrepUnitBytes) + 1024;
+    (sizeof(ChainSmem) > kPrepUnits * kPrepUnitBytes ? sizeof(ChainSmem)
+                                                     : kPrepUnits * kPrepUnitBytes) + 1024;
+static_assert(kFusedSmemBytes <= 232448, "fused kernel shared memory");
+static_assert(kPrepUnits * kPrepTmemCols <= 512, "prep units' TMEM");
 // The register budgets of the recurrence role (72 x 128 + 128 x 384 + 24 x 128
 // threads) are the launch allocation of 640 threads at 96 registers.
 static_assert(72 * 128 + 128 * 384 + 24 * 128 == kFusedThreads * 96, "register split");
@@ -1273,12 +1368,12 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             chunk_off, order, table, slots, gl, h0, out, hT, nullptr, 1, nullptr, err, N, Hk, Hv,
             flags);
     } else {
-        const int u = threadIdx.x / kThreads;
+        const int u = threadIdx.x / kPrepThreads;
         const int pcta = blockIdx.x - n_chain, ncta = gridDim.x - n_chain;
         prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
-                        threadIdx.x - u * kThreads, 1 + u, 2 * pcta + u, 2 * ncta, n_items, flags,
-                        1u, porder);
+                        threadIdx.x - u * kPrepThreads, 1 + u, kPrepUnits * pcta + u,
+                        kPrepUnits * ncta, n_items, flags, 1u, porder);
     }
 }
 
@@ -1581,7 +1676,7 @@ gdn_status launch_table(const gdn_problem &p, const WsLayout &w, const TcPtrs &t
     time_mark(tm, 0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(
         cu, p.num_seqs, p.total_tokens, w.max_chunks, snap_stride, t.err, t.chunk_off, t.snap_off,
-        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_k_heads) : 0,
+        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_v_heads) : 0,
         zero_flags ? t.porder : nullptr);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     time_mark(tm, 1, stream);
@@ -1598,8 +1693,8 @@ gdn_status launch_prep(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
                                  (int)smem) != cudaSuccess)
             return GDN_ERR_CUDA;
         cudaLaunchAttribute attr;
-        const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)w.max_chunks, p.num_k_heads),
-                                                  kThreads, smem, stream, pdl, &attr);
+        const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)w.max_chunks, p.num_v_heads),
+                                                  kPrepThreads, smem, stream, pdl, &attr);
         if (cudaLaunchKernelEx(&cfg, gdn_prep_kernel, m.tq, m.tk, g, beta,
                                (const int *)t.chunk_off, (const int4 *)t.table, t.slots, t.gl,
                                t.err, p.num_seqs, p.num_k_heads, p.num_v_heads) != cudaSuccess)
@@ -1675,21 +1770,23 @@ int fused_grid() {
 }
 
 // Whether the fused kernel should beat the separate ones, from measured rates
-// on this GPU: a persistent prep unit takes ~27 us per (chunk, key head)
-// item, a wave of the separate prep kernel (two items per SM) ~21 us, a
-// recurrence chunk step ~1.3 us.  Fused: prep on the SMs the recurrences
-// leave, the recurrence following (it cannot finish before its last chunk is
-// prepped).  Separate: prep on every SM, then the recurrence.  The longest
-// sequence is estimated as T / N tokens (as long as T for one sequence).
+// on this GPU: a prep item (chunk, value head) takes kPrepItemUs on one of the
+// kPrepUnits units of a CTA in either kernel, a recurrence chunk step
+// kChainStepUs.  Fused: prep on the SMs the recurrences leave, the
+// recurrence following (it cannot finish before its last chunk is prepped).
+// Separate: prep on every SM, then the recurrence.  The longest sequence is
+// estimated as T / N tokens (as long as T for one sequence).
+constexpr double kPrepItemUs = 8.0, kChainStepUs = 1.3;
 bool fused_pays(const gdn_problem &p, int grid) {
     const int64_t n_chain = (int64_t)p.num_seqs * p.num_v_heads;
     if (n_chain + 16 > grid) return false;
     const int64_t chunks = (p.total_tokens + C - 1) / C + p.num_seqs - 1;
-    const int64_t items = chunks * p.num_k_heads;
-    const double chain = 1.3 * (double)((p.total_tokens / p.num_seqs + C - 1) / C);
-    const double prep_f = 27.0 * (double)((items + 2 * (grid - n_chain) - 1) / (2 * (grid - n_chain)));
-    const double prep_s = 21.0 * (double)((items + 2 * grid - 1) / (2 * grid));
-    return std::max(prep_f, chain + 27.0) < prep_s + chain + 5.0;
+    const int64_t items = chunks * p.num_v_heads;
+    const double chain = kChainStepUs * (double)((p.total_tokens / p.num_seqs + C - 1) / C);
+    const int64_t units_f = kPrepUnits * (grid - n_chain), units_s = kPrepUnits * (int64_t)grid;
+    const double prep_f = kPrepItemUs * (double)((items + units_f - 1) / units_f);
+    const double prep_s = kPrepItemUs * (double)((items + units_s - 1) / units_s);
+    return std::max(prep_f, chain + kPrepItemUs) < prep_s + chain + 5.0;
 }
 
 // Chunk table, then the fused kernel: prep and the recurrence in one launch.
@@ -1709,7 +1806,7 @@ bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, cons
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     const int n_chain = p.num_seqs * p.num_v_heads;
-    const int n_items = (int)(w.max_chunks * p.num_k_heads);
+    const int n_items = (int)(w.max_chunks * p.num_v_heads);
     if (cudaLaunchKernelEx(&cfg, gdn_fused_kernel, m.tq, m.tk, m.tv, m.to, g, beta,
                            (const int *)t.chunk_off, (const int *)t.order, (const int4 *)t.table,
                            t.slots, t.gl, h0, static_cast<__nv_bfloat16 *>(out), hT, t.err,
@@ -1778,6 +1875,31 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     if (st != GDN_OK) return st;
     time_mark(tm, 3, stream);
     return GDN_OK;
+}
+
+gdn_status launch_prefill_tc_prep_only(const gdn_problem &p, const void *q, const void *k,
+                                      const float *g, const float *beta, const int32_t *cu,
+                                      cudaStream_t stream) {
+    if (p.num_seqs == 0) return GDN_OK;
+    const WsLayout w = ws_layout(p);
+    const TcPtrs t = tc_ptrs(w, p.workspace);
+    TcMaps m;
+    // (v and out are not touched by the table and prep kernels: their maps
+    // are built over q)
+    if (!encode_maps(p, q, k, q, const_cast<void *>(q), m)) return GDN_ERR_CUDA;
+    return launch_table_prep(p, w, t, m, g, beta, cu, 0, stream, false);
+}
+
+void prefill_tc_slot_layout(const gdn_problem &p, int64_t *layout) {
+    const WsLayout w = ws_layout(p);
+    layout[0] = (int64_t)w.tiles;
+    layout[1] = kSlotBytes;
+    layout[2] = kSlotWT;
+    layout[3] = kSlotTB;
+    layout[4] = kSlotP;
+    layout[5] = kSlotQ;
+    layout[6] = kSlotEG;
+    layout[7] = kSlotDEC;
 }
 
 namespace {

@@ -400,6 +400,41 @@ GDN_API gdn_status gdn_chunk_prefill_timed(const gdn_problem *problem,
  */
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode);
 
+/*
+ * Diagnostics for tests of the intra-chunk prep on its own (the pages compare
+ * every kernel of the chunked layer with a reference separately: page
+ * "cf-1.com", section "精度").  Only for bf16 q/k/v with dk = dv = 128
+ * (otherwise GDN_ERR_UNSUPPORTED).
+ *
+ * gdn_chunk_prefill_prep_only runs the first two kernels of
+ * gdn_chunk_prefill -- the chunk table and the prep -- on `stream` and leaves
+ * their results in problem->workspace (argument checks and errors as
+ * gdn_chunk_prefill; v, out and the states are not needed).
+ *
+ * gdn_chunk_prefill_prep_layout fills layout[0..7]:
+ *   [0] byte offset of the slot array in the workspace; [1] bytes per slot.
+ *   Slot (c, h) -- chunk c of the batch (chunks numbered sequence by
+ *   sequence, 64 tokens each, the last of a sequence possibly shorter) and
+ *   value head h -- starts at layout[0] + (c * Hv + h) * layout[1].  Within a
+ *   slot, byte offsets of:
+ *   [2] W^T = (T diag(b e^gamma) K)^T   128 rows (dk) x 64 columns (tokens)
+ *   [3] T diag(b)                       64 x 64
+ *   [4] P = M o Q K^T                   64 x 64
+ *   [5] diag(e^gamma) Q                 two 64 x 64 images: dk 0-63, 64-127
+ *   [6] e^{gamma_t}                     fp32 [64]
+ *   [7] e^{gamma_L - gamma_t}           fp32 [64]
+ *   (T = (I + A)^-1, A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i) for i < t,
+ *   M_ri = e^{gamma_r - gamma_i} for i <= r, gamma = cumsum(g) in the chunk;
+ *   tokens past a sequence's end count as b = 0, g = 0.)  The matrices are
+ *   bf16 images of rows of 128 bytes (64 elements): element (r, c) is at byte
+ *   128 r + 16 ((c / 8) xor (r mod 8)) + 2 (c mod 8).
+ */
+GDN_API gdn_status gdn_chunk_prefill_prep_only(const gdn_problem *problem,
+                                               const void *q, const void *k,
+                                               const float *g, const float *beta,
+                                               const int32_t *cu_seqlens, gdn_stream_t stream);
+GDN_API gdn_status gdn_chunk_prefill_prep_layout(const gdn_problem *problem, int64_t *layout);
+
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);
 

@@ -37,13 +37,20 @@ def chunk_prep(Kc, Vc, gc, bc):
     return gam, T, W, U
 
 
+def chunk_output_factors(Qc, Kc, gam):
+    """The state-independent factors of the chunk's output and state update:
+    (Qtil = diag(e^gamma) Q, P = M o Q K^T, dec = e^{gamma_L - gamma})."""
+    M = np.tril(np.exp(gam[:, None] - gam[None, :]))
+    return np.exp(gam)[:, None] * Qc, M * (Qc @ Kc.T), np.exp(gam[-1] - gam)
+
+
 def chunk_step(S, Qc, Kc, Vc, gc, bc):
     """One chunk: returns (O [L, dv], S_end) from the start state S [dv, dk]."""
     gam, T, W, U = chunk_prep(Kc, Vc, gc, bc)
     Delta = U - W @ S.T
-    M = np.tril(np.exp(gam[:, None] - gam[None, :]))
-    O = np.exp(gam)[:, None] * (Qc @ S.T) + (M * (Qc @ Kc.T)) @ Delta
-    Ktil = np.exp(gam[-1] - gam)[:, None] * Kc
+    Qtil, P, dec = chunk_output_factors(Qc, Kc, gam)
+    O = Qtil @ S.T + P @ Delta
+    Ktil = dec[:, None] * Kc
     S_end = np.exp(gam[-1]) * S + Delta.T @ Ktil
     return O, S_end
 
