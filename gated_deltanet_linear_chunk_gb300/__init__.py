@@ -116,6 +116,10 @@ def library() -> ctypes.CDLL:
     lib.gdn_chunk_prefill_scan.argtypes = [PP, ctypes.c_int32] + [P] * 10
     lib.gdn_chunk_prefill_timed.restype = ctypes.c_int
     lib.gdn_chunk_prefill_timed.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.gdn_chunk_prefill_prep_only.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_prep_only.argtypes = [PP, P, P, P, P, P, P]
+    lib.gdn_chunk_prefill_prep_layout.restype = ctypes.c_int
+    lib.gdn_chunk_prefill_prep_layout.argtypes = [PP, P]
     lib.gdn_chunk_prefill_host.restype = ctypes.c_int
     lib.gdn_chunk_prefill_host.argtypes = [PP, ctypes.c_int32] + [P] * 16 + [P]
     lib.gdn_prefill_fused_mode.restype = ctypes.c_int32

@@ -209,11 +209,12 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
 
 // Inclusive prefix sum of g over one chunk (lane holds tokens 2l, 2l+1),
 // with g = 0 past the end of the sequence.  Optionally also b (0 past the
-// end), e^{gamma_t} and e^{gamma_L - gamma_t}.  Called by one full warp.
+// end), e^{gamma_t}, e^{gamma_L - gamma_t} and e^{-gamma_t}.  Called by one
+// full warp.
 __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok0, int L, int Hv,
                                             int h, float *gam, float *beta_out,
                                             const float *__restrict__ beta, float *eg = nullptr,
-                                            float *dec = nullptr) {
+                                            float *dec = nullptr, float *einv = nullptr) {
     const int lane = threadIdx.x & 31;
     const int t0 = 2 * lane, t1 = 2 * lane + 1;
     const float g0 = t0 < L ? g[(size_t)(tok0 + t0) * Hv + h] : 0.f;
@@ -238,6 +239,10 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
         dec[t0] = expf(gL - ga);
         dec[t1] = expf(gL - gb);
     }
+    if (einv) {
+        einv[t0] = expf(-ga);
+        einv[t1] = expf(-gb);
+    }
 }
 
 // ------------------------------------------------------------------ kernel 2
@@ -246,38 +251,58 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
 // flight on an SM (five per CTA of the fused kernel, five CTAs per SM of the
 // separate kernel): an item is a chain of dependent steps (tile loads, four
 // MMA round trips, CUDA-core epilogues between barriers), and independent
-// items fill each other's waits.  The K K^T and Q K^T product is recomputed
-// for each value head of a key head; it is one small MMA.
+// items fill each other's waits.  Within an item one warp polls each
+// mbarrier while the others block at the unit's named barrier (no issue
+// slots spent waiting), TMEM rows are read eight columns at a time in rolled
+// loops (little code for the instruction cache), and the slot's large
+// images leave through shared memory by bulk copies.  The K K^T and Q K^T
+// product is recomputed for each value head of a key head; it is one small
+// MMA.
 constexpr int kPrepThreads = 128;
 constexpr int kPrepUnits = 5;              // units per CTA of the fused kernel
 constexpr uint32_t kPrepTmemCols = 64;     // [K; Q] K^T, then N, Y and W^T in turn
+// Below this gamma_L the factors e^{gamma_t} and e^{-gamma_i} of A and P could
+// overflow fp32 (e^{-gamma_i} <= e^{-gamma_L}): such chunks take one
+// exponential per element instead.
+constexpr float kFactorGammaMin = -80.f;
 
 struct alignas(1024) PrepSmem {
     // K atom 0 | Q atom 0 | K atom 1 | Q atom 1 (two 64-column 128-byte-swizzled
-    // atoms each; stacked so that one M = 128 MMA gives K K^T and Q K^T).  Once
-    // diag(e^gamma) Q has been stored and the product is done, the Q atoms are
-    // reused: Q atom 0 holds A's two diagonal 32 x 32 blocks (fp32), then
-    // N = D' E (bf16); Q atom 1 holds D' (bf16).
+    // atoms each, stacked so that one M = 128 MMA gives K K^T and Q K^T).  The
+    // Q atoms are scaled in place to diag(e^gamma) Q and copied to the slot;
+    // then Q atom 0 holds E (bf16), then N = D' E, and Q atom 1 holds D'
+    // (bf16), then T diag(b) (copied to the slot).  K atom 0 + Q atom 0 finally
+    // stage W^T (copied to the slot).
     uint8_t kq[4 * kTile];
-    uint8_t e[kTile];  // E (lower-left 32 x 32 block of A, bf16), then T diag(b e^gamma)
+    // A's two diagonal 32 x 32 blocks (fp32), the inverse's scratch; then
+    // T diag(b e^gamma) (bf16, the W^T MMA's operand).
+    uint8_t ab[kTile];
     float gam[C];
     float beta[C];
-    float eg[C];
-    float dec[C];
+    float eg[C];    // e^{gamma_t}
+    float einv[C];  // e^{-gamma_t}
+    float dec[C];   // e^{gamma_L - gamma_t}
+    int4 nxt[2];    // chunk-table entries of this and the next item: {chunk, head, token, length}
     uint64_t tma_bar;
     uint64_t mma_bar;
     uint32_t tmem;
+    int fact;       // the chunk's A and P factorise (gamma_L >= kFactorGammaMin)
 };
 
-// The two fp32 diagonal 32 x 32 blocks of A live in Q atom 0: row t of block
-// b at float offset (32 b + t) * 32, its float4 group f stored at group
-// f ^ (t % 8) (conflict-free row stores, broadcast row reads).
+// The two fp32 diagonal 32 x 32 blocks of A: row t of block b at float
+// offset (32 b + t) * 32, its float4 group f stored at group f ^ (t % 8)
+// (conflict-free row stores, broadcast row reads).
 __device__ __forceinline__ float *ad_row(uint8_t *buf, int blk, int t) {
     return reinterpret_cast<float *>(buf) + (32 * blk + t) * 32;
 }
 __device__ __forceinline__ int ad_f4(int f, int t) { return (f ^ (t & 7)) * 4; }
 __device__ __forceinline__ float &ad_at(uint8_t *buf, int blk, int t, int i) {
     return ad_row(buf, blk, t)[ad_f4(i >> 2, t) + (i & 3)];
+}
+
+// Element (r, c) of a bf16 image with 128-byte swizzled rows.
+__device__ __forceinline__ __nv_bfloat16 *img_at(uint8_t *img, int r, int c) {
+    return reinterpret_cast<__nv_bfloat16 *>(img + swz(r, c >> 3) + 2 * (c & 7));
 }
 
 // Writes 8 floats as one 16-byte bf16 chunk.
@@ -305,9 +330,26 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
     for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
 }
 
-// L2 prefetch of what item (ch, h) will load: its K and Q tiles and its
-// g and beta values (64 tokens, one value head: strided, so every line is
-// fetched separately).  Called by one full warp.
+// Eight elements s e^{gamma_r - gamma_i} x_i of a row r of A (with b_r in s)
+// or P, columns i0 .. i0 + 7 read from TMEM; entries past `last` are 0.
+// With `fact`, e^{gamma_r - gamma_i} = e^{gamma_r} e^{-gamma_i} (rs = s e^{gamma_r}).
+__device__ __forceinline__ void decayed8(const PrepSmem &sm, uint32_t taddr, int i0, int last,
+                                         bool fact, float s, float rs, float gr, float (&a)[8]) {
+    uint32_t r[8];
+    tmem_ld8(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u;
+        const float x = __uint_as_float(r[u]);
+        const float v = fact ? rs * sm.einv[i] * x : s * ex2_approx((gr - sm.gam[i]) * kLog2e) * x;
+        a[u] = i <= last ? v : 0.f;
+    }
+}
+
+// L2 prefetch of what an item will load: its K and Q tiles and its g and
+// beta values (64 tokens, one value head: strided, so every line is fetched
+// separately).  Called by one full warp.
 __device__ __forceinline__ void prep_prefetch(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                               const float *g, const float *beta, int tok0, int L,
                                               int Hv, int h, int hk) {
@@ -328,14 +370,34 @@ __device__ __forceinline__ void prep_prefetch(const CUtensorMap *tm_q, const CUt
     }
 }
 
+// The unit's wait for an mbarrier phase: warp 0 polls (bounded), then the
+// whole unit meets at its named barrier, which also ORs the failure flags.
+// True when the unit must stop.
+__device__ __forceinline__ bool unit_wait(uint64_t *bar, uint32_t parity, int warp, int nbar,
+                                          bool bad) {
+    if (warp == 0 && !bad) bad = !warp_wait_poll(bar, parity);
+    return named_barrier_or(nbar, kPrepThreads, bad);
+}
+
+// Makes an item's slot visible device-wide and publishes its ready flag
+// (one thread; every other thread's slot writes are ordered before a unit
+// barrier this thread has passed since).
+__device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
+    bulk_wait_group<0>();
+    fence_proxy_async_global();
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(epoch) : "memory");
+}
+
 // One prep unit: kPrepThreads threads with local index `ltid` (the unit's
 // first warp is a multiple of 4, so warp w of the unit reads TMEM lane
-// quadrant w), its own PrepSmem, TMEM columns and named barrier `bar`.  It
-// works through items item0, item0 + stride, ... below n_items (item =
-// chunk * Hv + value head, chunk-major).  With `flags`, each finished item
-// publishes `epoch` into flags[chunk * Hv + h] (release, device scope) once
-// its workspace slot writes are visible.  kLoop = false: exactly one item
-// (blockIdx.x = chunk, blockIdx.y = value head), compiled without the loop.
+// quadrant w), its own PrepSmem, TMEM columns and named barriers `bar` (the
+// unit) and `bar2` (its warps 2 and 3).  It works through items item0,
+// item0 + stride, ... below n_items (item = chunk * Hv + value head,
+// chunk-major).  With `flags`, each finished item publishes `epoch` into
+// flags[chunk * Hv + h] (release, device scope) once its workspace slot is
+// written.  kLoop = false: exactly one item (blockIdx.x = chunk, blockIdx.y =
+// value head), compiled without the loop.
 //
 // Per item:
 //   gamma = cumsum(g), b, e^gamma, e^{gamma_L - gamma};  [K; Q] K^T (M = 128);
@@ -354,14 +416,25 @@ __device__ __forceinline__ void prep_unit(
     PrepSmem &sm, const CUtensorMap *tm_q, const CUtensorMap *tm_k, const float *__restrict__ g,
     const float *__restrict__ beta, const int *__restrict__ chunk_off,
     const int4 *__restrict__ table, uint8_t *__restrict__ slots, float *__restrict__ gl,
-    int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int item0, int stride,
-    int n_items, unsigned *flags, unsigned epoch, const int *__restrict__ porder = nullptr) {
+    int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int bar2, int item0,
+    int stride, int n_items, unsigned *flags, unsigned epoch,
+    const int *__restrict__ porder = nullptr) {
     const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
     const int q4 = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of the physical warp
+    const int row = 32 * q4 + lane;         // this thread's TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    uint8_t *const bufA = sm.kq + kTile;      // Q atom 0: A's diagonal blocks, then N
-    uint8_t *const bufD = sm.kq + 3 * kTile;  // Q atom 1: D'
+    uint8_t *const bufE = sm.kq + kTile;      // Q atom 0
+    uint8_t *const bufD = sm.kq + 3 * kTile;  // Q atom 1
+    const int n_ch = chunk_off[N];
+    auto chunk_of = [&](int item) { return kLoop ? item / Hv : (int)blockIdx.x; };
+    // Chunk-table entry of an item: {chunk, value head, first token, length}.
+    auto locate = [&](int item) {
+        const int ci = chunk_of(item);
+        const int ch = (kLoop && porder) ? porder[ci] : ci;
+        const int4 e = table[ch];
+        return make_int4(ch, kLoop ? item % Hv : (int)blockIdx.y, e.y, e.z);
+    };
 
     if (tid == 0) {
         prefetch_tensormap(tm_q);
@@ -369,6 +442,7 @@ __device__ __forceinline__ void prep_unit(
         mbar_init(&sm.tma_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
+        if (item0 < n_items && chunk_of(item0) < n_ch) sm.nxt[0] = locate(item0);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, kPrepTmemCols);
@@ -382,50 +456,53 @@ __device__ __forceinline__ void prep_unit(
     const uint32_t tmem = sm.tmem;
     bool bad = false;
     uint32_t mph = 0, tph = 0;
-    const int n_ch = chunk_off[N];
+    int it = 0;
+    int4 pend = make_int4(-1, 0, 0, 0);  // (thread 0) item whose flag is still to publish
 #pragma unroll 1
-    for (int item = item0; item < n_items && !bad; item += stride) {
-        const int ci = kLoop ? item / Hv : (int)blockIdx.x;
-        if (ci >= n_ch) break;  // chunk-major: every later item is past the table
-        const int ch = (kLoop && porder) ? porder[ci] : ci;
-        const int h = kLoop ? item % Hv : (int)blockIdx.y;
-        const int hk = h / G;
-        const int4 e = table[ch];
-        const int tok0 = e.y, L = e.z;
+    for (int item = item0; item < n_items && !bad; item += stride, ++it) {
+        if (chunk_of(item) >= n_ch) break;  // chunk-major: every later item is past the table
+        const int4 cur = sm.nxt[it & 1];
+        const int ch = cur.x, h = cur.y, tok0 = cur.z, L = cur.w, hk = h / G;
         uint8_t *const slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
+        const bool more = kLoop && item + stride < n_items && chunk_of(item + stride) < n_ch;
         if (tid == 0) {
-            // The previous item's generic accesses of these tiles are ordered
-            // before the TMA writes (unit barrier, then this fence).
-            if (kLoop) fence_proxy_async_smem();
+            if (kLoop) {
+                // The previous item's bulk copies have read the tiles, and
+                // its generic accesses are ordered before the TMA writes.
+                bulk_wait_group_read<0>();
+                fence_proxy_async_smem();
+            }
             mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
             tma_load_3d(sm.kq + 0 * kTile, tm_k, 0, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 1 * kTile, tm_q, 0, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, hk, tok0, &sm.tma_bar);
+            if (kLoop && flags && pend.x >= 0) {
+                publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
+                pend.x = -1;
+            }
         }
         if (warp == 1) {
             // gamma, b and the decay factors while the tiles are in flight.
-            chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec);
+            chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec, sm.einv);
             float *slot_f = reinterpret_cast<float *>(slot);
             slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[2 * lane];
             slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[2 * lane + 1];
             slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[2 * lane];
             slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[2 * lane + 1];
-            if (lane == 31) gl[(size_t)ch * Hv + h] = sm.eg[C - 1];
-        } else if (kLoop && warp == 2 && item + stride < n_items) {
-            // The next item's inputs into L2 while this one runs.
-            const int cn = (item + stride) / Hv;
-            if (cn < n_ch) {
-                const int chn = porder ? porder[cn] : cn;
-                const int hn = (item + stride) % Hv;
-                const int4 en = table[chn];
-                prep_prefetch(tm_q, tm_k, g, beta, en.y, en.z, Hv, hn, hn / G);
+            if (lane == 31) {
+                gl[(size_t)ch * Hv + h] = sm.eg[C - 1];
+                sm.fact = sm.gam[C - 1] >= kFactorGammaMin;
             }
+        } else if (warp == 2 && more) {
+            // The next item: its table entry, and its inputs into L2.
+            const int4 nx = locate(item + stride);
+            if (lane == 0) sm.nxt[(it + 1) & 1] = nx;
+            prep_prefetch(tm_q, tm_k, g, beta, nx.z, nx.w, Hv, nx.y, nx.y / G);
         }
-        bad = !warp_wait(&sm.tma_bar, tph, nullptr);
+        if ((bad = unit_wait(&sm.tma_bar, tph, warp, bar, bad))) break;
         tph ^= 1;
-        named_barrier(bar, kPrepThreads);  // gamma & co. visible to the unit
-        if (tid == 0 && !bad) {
+        if (tid == 0) {
             tc_fence_after();
             const uint32_t base = smem_u32(sm.kq);
             constexpr uint32_t id = idesc_bf16(128, 64, false, false);
@@ -437,105 +514,67 @@ __device__ __forceinline__ void prep_unit(
             }
             mma_commit(&sm.mma_bar);
         }
-        // ---- diag(e^gamma) Q to the slot (the same swizzled image as the Q
-        // atoms, scaled row by row), while the MMA runs.
+        if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
+        mph ^= 1;
+        tc_fence_after();
+        // ---- diag(e^gamma) Q in place in the Q atoms, then copied to the slot.
 #pragma unroll 2
         for (int idx = tid; idx < 2 * C * 8; idx += kPrepThreads) {
             const int a = idx / (C * 8), r = (idx >> 3) & (C - 1), cc = idx & 7;
-            const uint32_t off = swz(r, cc);
-            float x[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm.kq + (2 * a + 1) * kTile + off), x);
+            uint4 *p = reinterpret_cast<uint4 *>(sm.kq + (2 * a + 1) * kTile + swz(r, cc));
+            float v[8];
+            unpack8(*p, v);
             const float sc = sm.eg[r];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] *= sc;
-            *reinterpret_cast<uint4 *>(slot + kSlotQ + a * kTile + off) = pack8(x);
+            for (int u = 0; u < 8; ++u) v[u] *= sc;
+            *p = pack8(v);
         }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
-        mph ^= 1;
-        tc_fence_after();
-        // (every Q read is done: the Q atoms become bufA and bufD)
-        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
-        // ---- A's diagonal blocks (fp32) and E (bf16) from K K^T (lanes
-        // 0-63), P from Q K^T (lanes 64-127).  Warp-uniform branches: each
-        // warp holds one quadrant of rows.
-        {
-            const int row = 32 * q4 + lane;
-            float x[32];
-            if (q4 < 2) {
-                const int t = row, blk = q4;
-                const float gt = sm.gam[t], bt = sm.beta[t];
-                // Columns of this row's block half: the diagonal block.
-                tmem_ld32f(tmem + lane_base + 32 * blk, x);
-                {
-                    float *dst = ad_row(bufA, blk, t & 31);
-#pragma unroll
-                    for (int u = 0; u < 32; u += 4) {
-                        float av[4];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int i = 32 * blk + u + w;
-                            av[w] = i < t ? bt * ex2_approx((gt - sm.gam[i]) * kLog2e) * x[u + w]
-                                          : 0.f;
-                        }
-                        *reinterpret_cast<float4 *>(dst + ad_f4(u >> 2, t)) =
-                            make_float4(av[0], av[1], av[2], av[3]);
-                    }
-                }
-                // E row t: columns 0-31 of rows 32-63 hold A, everything else 0.
-                const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-                if (blk == 1) {
-                    tmem_ld32f(tmem + lane_base, x);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float ev[8];
-#pragma unroll
-                        for (int w = 0; w < 8; ++w)
-                            ev[w] = bt * ex2_approx((gt - sm.gam[8 * cc + w]) * kLog2e) * x[8 * cc + w];
-                        *reinterpret_cast<uint4 *>(sm.e + swz(t, cc)) = pack8(ev);
-                    }
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4 *>(sm.e + swz(t, cc)) = z4;
-                }
-#pragma unroll
-                for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4 *>(sm.e + swz(t, cc)) = z4;
-            } else {
-                const int r = row - 64;
-                const float gr = sm.gam[r];
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    // Rows 0-31 have nothing at columns 32-63 (i > r).
-                    if (hf == 1 && q4 == 2) {
-#pragma unroll
-                        for (int cc = 4; cc < 8; ++cc)
-                            *reinterpret_cast<uint4 *>(slot + kSlotP + swz(r, cc)) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        continue;
-                    }
-                    tmem_ld32f(tmem + lane_base + 32 * hf, x);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float pv[8];
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            const int i = 32 * hf + 8 * cc + w;
-                            pv[w] = i <= r ? ex2_approx((gr - sm.gam[i]) * kLog2e) * x[8 * cc + w]
-                                           : 0.f;
-                        }
-                        *reinterpret_cast<uint4 *>(slot + kSlotP + swz(r, 4 * hf + cc)) = pack8(pv);
-                    }
-                }
-            }
-        }
-        tc_fence_before();  // the TMEM reads above precede the next MMA's writes
         fence_proxy_async_smem();
         named_barrier(bar, kPrepThreads);
-        // ---- D': the four 16 x 16 diagonal blocks of I + A inverted by
-        // forward substitution, one column per thread (threads 0-63).
-        float xc[16];
-        const int fb = tid >> 4, fcol = tid & 15;  // 16-block (0..3) and column
-        const int fb32 = fb >> 1, foff = 16 * (fb & 1);
-        if (tid < 64) {
+        if (tid == 0) {
+            bulk_store(slot + kSlotQ, sm.kq + kTile, kTile);
+            bulk_store(slot + kSlotQ + kTile, sm.kq + 3 * kTile, kTile);
+            bulk_commit_group();
+        }
+        // ---- A's diagonal blocks (fp32, into ab) from K K^T (lanes 0-63),
+        // P from Q K^T (lanes 64-127, to the slot).  Warp-uniform branches.
+        const bool fact = sm.fact;
+        if (q4 < 2) {
+            const int t = row, blk = q4;
+            const float gt = sm.gam[t], bt = sm.beta[t], rs = bt * sm.eg[t];
+            float *dst = ad_row(sm.ab, blk, t & 31);
+#pragma unroll 1
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float a[8];
+                decayed8(sm, tmem + lane_base + 32 * blk + 8 * c8, 32 * blk + 8 * c8, t - 1, fact,
+                         bt, rs, gt, a);
+                *reinterpret_cast<float4 *>(dst + ad_f4(2 * c8, t)) = make_float4(a[0], a[1], a[2], a[3]);
+                *reinterpret_cast<float4 *>(dst + ad_f4(2 * c8 + 1, t)) = make_float4(a[4], a[5], a[6], a[7]);
+            }
+        } else {
+            const int r = row - 64;
+            const float gr = sm.gam[r], rs = sm.eg[r];
+#pragma unroll 1
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float a[8];
+                if (c8 < 4 || q4 == 3) {  // (rows 0-31 have nothing at columns 32-63)
+                    decayed8(sm, tmem + lane_base + 8 * c8, 8 * c8, r, fact, 1.f, rs, gr, a);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) a[u] = 0.f;
+                }
+                *reinterpret_cast<uint4 *>(slot + kSlotP + swz(r, c8)) = pack8(a);
+            }
+        }
+        if (tid == 0) bulk_wait_group_read<0>();  // the Q atoms are free
+        named_barrier(bar, kPrepThreads);
+        // ---- D': warps 2-3 invert the four 16 x 16 diagonal blocks of I + A
+        // by forward substitution (one column per thread); warps 0-1 write E
+        // and clear D' outside those blocks and the merged ones.
+        if (q4 >= 2) {
+            const int ft = tid - 64, fb = ft >> 4, fcol = ft & 15;  // 16-block, column
+            const int fb32 = fb >> 1, foff = 16 * (fb & 1);
+            float xc[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 float a0 = (t == fcol) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -543,7 +582,7 @@ __device__ __forceinline__ void prep_unit(
 #pragma unroll
                 for (int i = 0; i < (t & ~3); i += 4) {
                     const float4 av = *reinterpret_cast<const float4 *>(
-                        ad_row(bufA, fb32, tr) + ad_f4((foff + i) >> 2, tr));
+                        ad_row(sm.ab, fb32, tr) + ad_f4((foff + i) >> 2, tr));
                     a0 = fmaf(-av.x, xc[i], a0);
                     a1 = fmaf(-av.y, xc[i + 1], a1);
                     a2 = fmaf(-av.z, xc[i + 2], a2);
@@ -551,16 +590,54 @@ __device__ __forceinline__ void prep_unit(
                 }
 #pragma unroll
                 for (int i = (t & ~3); i < t; ++i)
-                    a0 = fmaf(-ad_at(bufA, fb32, tr, foff + i), xc[i], a0);
+                    a0 = fmaf(-ad_at(sm.ab, fb32, tr, foff + i), xc[i], a0);
                 xc[t] = (a0 + a1) + (a2 + a3);
             }
-        }
-        named_barrier(bar, kPrepThreads);
-        // X1, X2 over A's diagonal 16 x 16 blocks (read by nobody any more).
-        if (tid < 64) {
+            named_barrier(bar2, 64);  // the substitution's reads of A are done
+            // X1, X2: fp32 over A's diagonal 16 x 16 blocks for the merge,
+            // bf16 into D'.
 #pragma unroll
-            for (int t = 0; t < 16; ++t) ad_at(bufA, fb32, foff + t, foff + fcol) = xc[t];
+            for (int t = 0; t < 16; ++t) {
+                ad_at(sm.ab, fb32, foff + t, foff + fcol) = xc[t];
+                *img_at(bufD, 32 * fb32 + foff + t, 32 * fb32 + foff + fcol) =
+                    __float2bfloat16_rn(xc[t]);
+            }
+        } else {
+            const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+            // E row t: columns 0-31 of rows 32-63 hold A, everything else 0.
+            const int t = row;
+            if (q4 == 1) {
+                const float gt = sm.gam[t], bt = sm.beta[t], rs = bt * sm.eg[t];
+#pragma unroll 1
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float a[8];
+                    decayed8(sm, tmem + lane_base + 8 * c8, 8 * c8, t - 1, fact, bt, rs, gt, a);
+                    *reinterpret_cast<uint4 *>(bufE + swz(t, c8)) = pack8(a);
+                }
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4 *>(bufE + swz(t, cc)) = z4;
+            }
+#pragma unroll
+            for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4 *>(bufE + swz(t, cc)) = z4;
+            // D' zeros, as 16-byte chunks: rows 0-31 x columns 32-63 and rows
+            // 32-63 x columns 0-31 (4 chunks a row), and each diagonal 32-block's
+            // upper-right 16 x 16 corner (2 chunks a row): 320 chunks.
+#pragma unroll 1
+            for (int j = tid; j < 320; j += 64) {
+                int r, cc;
+                if (j < 256) {
+                    r = j >> 2;
+                    cc = (r < 32 ? 4 : 0) + (j & 3);
+                } else {
+                    const int k = j - 256;  // block k / 32, row (k / 2) % 16 of it
+                    r = 32 * (k >> 5) + ((k >> 1) & 15);
+                    cc = 4 * (k >> 5) + 2 + (k & 1);
+                }
+                *reinterpret_cast<uint4 *>(bufD + swz(r, cc)) = z4;
+            }
         }
+        tc_fence_before();  // this item's last reads of [K K^T; Q K^T]
         named_barrier(bar, kPrepThreads);
         // Y = C X1 per 32-block (C = rows 16-31, columns 0-15), into the
         // block's unused upper-right 16 x 16 corner (nothing this step reads);
@@ -570,51 +647,33 @@ __device__ __forceinline__ void prep_unit(
             float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float c = ad_at(bufA, mb, 16 + mr, j);
-                const float4 x1 = *reinterpret_cast<const float4 *>(ad_row(bufA, mb, j) +
+                const float c = ad_at(sm.ab, mb, 16 + mr, j);
+                const float4 x1 = *reinterpret_cast<const float4 *>(ad_row(sm.ab, mb, j) +
                                                                     ad_f4(mc >> 2, j));
                 y0 = fmaf(c, x1.x, y0);
                 y1 = fmaf(c, x1.y, y1);
                 y2 = fmaf(c, x1.z, y2);
                 y3 = fmaf(c, x1.w, y3);
             }
-            *reinterpret_cast<float4 *>(ad_row(bufA, mb, mr) + ad_f4((16 + mc) >> 2, mr)) =
+            *reinterpret_cast<float4 *>(ad_row(sm.ab, mb, mr) + ad_f4((16 + mc) >> 2, mr)) =
                 make_float4(y0, y1, y2, y3);
         }
         named_barrier(bar, kPrepThreads);
-        // -X2 Y into C's place (the block's lower-left corner, which this
-        // step does not read).
+        // -X2 Y: D's lower-left 16 x 16 corner of each 32-block, in bf16.
         {
             float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const float x2 = ad_at(bufA, mb, 16 + mr, 16 + k);
-                const float4 y = *reinterpret_cast<const float4 *>(ad_row(bufA, mb, k) +
+                const float x2 = ad_at(sm.ab, mb, 16 + mr, 16 + k);
+                const float4 y = *reinterpret_cast<const float4 *>(ad_row(sm.ab, mb, k) +
                                                                    ad_f4((16 + mc) >> 2, k));
                 m0 = fmaf(-x2, y.x, m0);
                 m1 = fmaf(-x2, y.y, m1);
                 m2 = fmaf(-x2, y.z, m2);
                 m3 = fmaf(-x2, y.w, m3);
             }
-            *reinterpret_cast<float4 *>(ad_row(bufA, mb, 16 + mr) + ad_f4(mc >> 2, 16 + mr)) =
-                make_float4(m0, m1, m2, m3);
-        }
-        named_barrier(bar, kPrepThreads);
-        // D' as a bf16 K-major image: row t = tid / 2, 32 columns per thread.
-        {
-            const int t = tid >> 1, hc = tid & 1, b = t >> 5, rr = t & 31;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float dv[8];
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const int i = 32 * hc + 8 * cc + w;  // column in the 64-wide row
-                    const int ii = i & 31;
-                    const bool in = (i >> 5) == b && !(rr < 16 && ii >= 16);
-                    dv[w] = in ? ad_at(bufA, b, rr, ii) : 0.f;
-                }
-                *reinterpret_cast<uint4 *>(bufD + swz(t, 4 * hc + cc)) = pack8(dv);
-            }
+            *reinterpret_cast<uint2 *>(img_at(bufD, 32 * mb + 16 + mr, 32 * mb + mc)) =
+                make_uint2(pack_bf16(m0, m1), pack_bf16(m2, m3));
         }
         fence_proxy_async_smem();
         named_barrier(bar, kPrepThreads);
@@ -622,48 +681,49 @@ __device__ __forceinline__ void prep_unit(
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-            const uint32_t a = smem_u32(bufD), b = smem_u32(sm.e);
+            const uint32_t a = smem_u32(bufD), b = smem_u32(bufE);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16(tmem, smem_desc(a + 32 * k, 16, 1024), smem_desc(b + 2048 * k, kTile, 1024),
                          id, k > 0);
             mma_commit(&sm.mma_bar);
         }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
         mph ^= 1;
         tc_fence_after();
-        // N to bufA (M = 64 layout: row 16 q + lane in lanes 0-15 of quadrant q).
+        // N over E (M = 64 layout: row 16 q + lane in lanes 0-15 of quadrant q).
         {
-            float x[32];
+            float y[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                tmem_ld32f(tmem + lane_base + 32 * hf, x);
+                tmem_ld32f(tmem + lane_base + 32 * hf, y);
                 if (lane < 16) {
                     const int r = 16 * q4 + lane;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
-                        *reinterpret_cast<uint4 *>(bufA + swz(r, 4 * hf + cc)) = pack8(x + 8 * cc);
+                        *reinterpret_cast<uint4 *>(bufE + swz(r, 4 * hf + cc)) = pack8(y + 8 * cc);
                 }
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
+        named_barrier(bar, kPrepThreads);
         // ---- Y = N D'  (M = 64, N = 64, K = 64)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-            const uint32_t a = smem_u32(bufA), b = smem_u32(bufD);
+            const uint32_t a = smem_u32(bufE), b = smem_u32(bufD);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16(tmem, smem_desc(a + 32 * k, 16, 1024), smem_desc(b + 2048 * k, kTile, 1024),
                          id, k > 0);
             mma_commit(&sm.mma_bar);
         }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
         mph ^= 1;
         tc_fence_after();
-        // ---- T = D' - Y;  T diag(b) to the slot, T diag(b e^gamma) to e.
+        // ---- T = D' - Y;  T diag(b) in place of D' (then copied to the
+        // slot), T diag(b e^gamma) into ab.
         {
             float y[32];
 #pragma unroll
@@ -682,54 +742,57 @@ __device__ __forceinline__ void prep_unit(
                             tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[i];
                             tbg[u] = tb[u] * sm.eg[i];
                         }
-                        *reinterpret_cast<uint4 *>(slot + kSlotTB + off) = pack8(tb);
-                        *reinterpret_cast<uint4 *>(sm.e + off) = pack8(tbg);
+                        *reinterpret_cast<uint4 *>(bufD + off) = pack8(tb);
+                        *reinterpret_cast<uint4 *>(sm.ab + off) = pack8(tbg);
                     }
                 }
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
+        named_barrier(bar, kPrepThreads);
         // ---- W^T = K^T (T diag(b e^gamma))^T  (M = 128 dk, N = 64, K = 64 tokens)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16(128, 64, true, false);
-            const uint32_t a = smem_u32(sm.kq), b = smem_u32(sm.e);
+            const uint32_t a = smem_u32(sm.kq), b = smem_u32(sm.ab);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16(tmem, smem_desc(a + 2048 * k, 2 * kTile, 1024),
                          smem_desc(b + 32 * k, 16, 1024), id, k > 0);
             mma_commit(&sm.mma_bar);
+            bulk_store(slot + kSlotTB, bufD, kTile);
+            bulk_commit_group();
         }
-        bad |= !warp_wait(&sm.mma_bar, mph, nullptr);
+        if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
         mph ^= 1;
         tc_fence_after();
+        // W^T staged in K atom 0 + Q atom 0 (16 KB, both dead), then copied.
         {
-            const int row = 32 * q4 + lane;  // key dimension
-            float x[32];
+            float y[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                tmem_ld32f(tmem + lane_base + 32 * hf, x);
+                tmem_ld32f(tmem + lane_base + 32 * hf, y);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(slot + kSlotWT + swz(row, 4 * hf + cc)) =
-                        pack8(x + 8 * cc);
+                    *reinterpret_cast<uint4 *>(sm.kq + swz(row, 4 * hf + cc)) = pack8(y + 8 * cc);
             }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
-        if ((bad = named_barrier_or(bar, kPrepThreads, bad))) break;
-        if (kLoop && flags && tid == 0) {
-            // Every thread's slot writes are ordered before the barrier; this
-            // thread makes them visible device-wide and publishes the flag.
-            __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)ch * Hv + h),
-                         "r"(epoch)
-                         : "memory");
+        named_barrier(bar, kPrepThreads);
+        if (tid == 0) {
+            bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
+            bulk_commit_group();
+            pend = make_int4(ch, h, 0, 0);  // published once the copies are done
         }
         if (!kLoop) break;
     }
-    if (bad && tid == 0) atomicExch(err, kErrTimeout);
+    if (tid == 0) {
+        if (kLoop && flags && pend.x >= 0 && !bad) publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
+        if (bad) atomicExch(err, kErrTimeout);
+        bulk_wait_group<0>();  // shared memory must outlive the copies
+    }
     tc_fence_before();
     named_barrier(bar, kPrepThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
@@ -752,7 +815,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if ((int)blockIdx.x >= chunk_off[N]) return;
     const int item = blockIdx.x * Hv + blockIdx.y;
     prep_unit<false>(sm, &tm_q, &tm_k, g, beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
-                     threadIdx.x, 1, item, 1, item + 1, nullptr, 0u);
+                     threadIdx.x, 1, 2, item, 1, item + 1, nullptr, 0u);
 }
 
 // ------------------------------------------------------------------ kernel 3
@@ -1345,6 +1408,7 @@ constexpr size_t kFusedSmemBytes =
                                                      : kPrepUnits * kPrepUnitBytes) + 1024;
 static_assert(kFusedSmemBytes <= 232448, "fused kernel shared memory");
 static_assert(kPrepUnits * kPrepTmemCols <= 512, "prep units' TMEM");
+static_assert(1 + 2 * kPrepUnits <= 16, "prep units' named barriers");
 // The register budgets of the recurrence role (72 x 128 + 128 x 384 + 24 x 128
 // threads) are the launch allocation of 640 threads at 96 registers.
 static_assert(72 * 128 + 128 * 384 + 24 * 128 == kFusedThreads * 96, "register split");
@@ -1372,8 +1436,8 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int pcta = blockIdx.x - n_chain, ncta = gridDim.x - n_chain;
         prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
-                        threadIdx.x - u * kPrepThreads, 1 + u, kPrepUnits * pcta + u,
-                        kPrepUnits * ncta, n_items, flags, 1u, porder);
+                        threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u,
+                        kPrepUnits * pcta + u, kPrepUnits * ncta, n_items, flags, 1u, porder);
     }
 }
 

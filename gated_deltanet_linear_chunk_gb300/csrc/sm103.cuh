@@ -131,6 +131,21 @@ __device__ __forceinline__ bool warp_wait_spin(uint64_t *bar, uint32_t parity, v
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Bounded wait of a whole warp, every lane polling try_wait without a
+// suspend-time hint (the hinted form wakes up late: thousands of cycles after
+// a short MMA completes).  For warps that all need the phase: no shuffle, no
+// branch on the lane.  Returns false after about `limit` clock cycles.
+__device__ __forceinline__ bool warp_wait_poll(uint64_t *bar, uint32_t parity,
+                                               long long limit = 4000000000ll) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+#pragma unroll 1
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel of
 // the stream (launched with programmatic stream serialization) be scheduled
 // once every CTA of this grid has called it or exited; wait blocks until the
@@ -301,6 +316,21 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int 
             reinterpret_cast<uint64_t>(map)),
         "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
         : "memory");
+}
+
+// Plain bulk copy shared -> global (both 16-byte aligned, bytes % 16 == 0),
+// completion tracked by bulk async-groups.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
+// Orders this thread's completed async-proxy global writes (bulk stores)
+// with its later generic-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_commit_group() {
@@ -518,6 +548,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
         : "memory");
+}
+
+// Each thread of the warp reads 8 consecutive 32-bit columns of its own TMEM
+// lane (shape 32x32b, 8 repetitions).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

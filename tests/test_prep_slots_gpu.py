@@ -69,6 +69,7 @@ def check_slots(lib, p, heads=None):
     q, k = (x.double().numpy() for x in (p.q, p.k))
     g, b = (x.double().numpy() for x in (p.g, p.beta))
     worst = {}
+    tol_worst = 0.0
     chunk = 0
     for n in range(len(cu) - 1):
         for s in range(cu[n], cu[n + 1], C):
@@ -86,6 +87,11 @@ def check_slots(lib, p, heads=None):
                 qt = np.concatenate([image(slot[o_q:], 64), image(slot[o_q + 8192:], 64)], 1)
                 eg = slot[o_eg:o_eg + 256].view(np.float32).astype(np.float64)
                 dc = slot[o_dec:o_dec + 256].view(np.float32).astype(np.float64)
+                # The decay factors come from an fp32 prefix sum of g: a few
+                # roundings of partial sums as large as sum |g| (scan depth
+                # 6), i.e. an error of about 2^-24 * 8 * sum |g| in the exponent.
+                tol_exp = max(1e-5, 8 * 2.0 ** -24 * float(np.sum(np.abs(g[s:e, h]))))
+                tol_worst = max(tol_worst, tol_exp)
                 errs = {
                     "W^T": rel(wt[:, :L], W.T),
                     "T diag(b)": rel(tb[:L, :L], T * b[s:e, h][None, :]),
@@ -95,15 +101,21 @@ def check_slots(lib, p, heads=None):
                     "e^{gamma_L - gamma}": rel(dc[:L], dec),
                 }
                 # Tokens past the end: no contribution to W or U, decay held.
-                assert np.all(wt[:, L:] == 0) and np.all(tb[L:] == 0) and np.all(tb[:, L:] == 0)
-                assert np.all(eg[L:] == eg[L - 1])
-                assert np.all(dc[L:] == 1.0)
+                where = f"sequence {n}, chunk at token {s} (L = {L}), head {h}"
+                assert np.all(wt[:, L:] == 0), f"W^T past the end, {where}"
+                assert np.all(tb[L:] == 0) and np.all(tb[:, L:] == 0), f"T diag(b), {where}"
+                # (the prefix sum over the chunk adds in a different order for
+                # each pair of tokens, so these agree to fp32 rounding)
+                assert np.allclose(eg[L:], eg[L - 1], rtol=tol_exp, atol=0), \
+                    f"e^gamma past the end {eg[L - 1:]}, {where}"
+                assert np.allclose(dc[L:], 1.0, rtol=tol_exp, atol=0), \
+                    f"decay past the end {dc[L:]}, {where}"
                 for name, err in errs.items():
                     worst[name] = max(worst.get(name, 0.0), err)
             chunk += 1
     print("[prep parity] " + ", ".join(f"{k} {v:.2e}" for k, v in worst.items()))
     for name in ("e^gamma", "e^{gamma_L - gamma}"):
-        assert worst[name] <= 1e-5, f"{name}: {worst[name]:.2e}"
+        assert worst[name] <= tol_worst, f"{name}: {worst[name]:.2e} > {tol_worst:.1e}"
     for name, err in worst.items():
         assert err <= TOL_BF16, f"{name}: rel err {err:.2e} > {TOL_BF16:.0e}"
     return worst
