@@ -265,6 +265,9 @@ constexpr uint32_t kPrepTmemCols = 64;     // [K; Q] K^T, then N, Y and W^T in t
 // overflow fp32 (e^{-gamma_i} <= e^{-gamma_L}): such chunks take one
 // exponential per element instead.
 constexpr float kFactorGammaMin = -80.f;
+// The unit's thread that issues its TMA loads and bulk copies and publishes
+// its items (thread 0 issues the MMAs and its warp polls the mbarriers).
+constexpr int kCopier = 96;
 
 struct alignas(1024) PrepSmem {
     // K atom 0 | Q atom 0 | K atom 1 | Q atom 1 (two 64-column 128-byte-swizzled
@@ -282,6 +285,7 @@ struct alignas(1024) PrepSmem {
     float eg[C];    // e^{gamma_t}
     float einv[C];  // e^{-gamma_t}
     float dec[C];   // e^{gamma_L - gamma_t}
+    float bg[C];    // b_t e^{gamma_t}
     int4 nxt[2];    // chunk-table entries of this and the next item: {chunk, head, token, length}
     uint64_t tma_bar;
     uint64_t mma_bar;
@@ -337,12 +341,15 @@ __device__ __forceinline__ void decayed8(const PrepSmem &sm, uint32_t taddr, int
                                          bool fact, float s, float rs, float gr, float (&a)[8]) {
     uint32_t r[8];
     tmem_ld8(taddr, r);
+    const float4 *src4 = reinterpret_cast<const float4 *>(fact ? sm.einv + i0 : sm.gam + i0);
+    const float4 f0 = src4[0], f1 = src4[1];
+    const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
     tmem_ld_wait();
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const int i = i0 + u;
         const float x = __uint_as_float(r[u]);
-        const float v = fact ? rs * sm.einv[i] * x : s * ex2_approx((gr - sm.gam[i]) * kLog2e) * x;
+        const float v = fact ? rs * f[u] * x : s * ex2_approx((gr - f[u]) * kLog2e) * x;
         a[u] = i <= last ? v : 0.f;
     }
 }
@@ -457,7 +464,7 @@ __device__ __forceinline__ void prep_unit(
     bool bad = false;
     uint32_t mph = 0, tph = 0;
     int it = 0;
-    int4 pend = make_int4(-1, 0, 0, 0);  // (thread 0) item whose flag is still to publish
+    int4 pend = make_int4(-1, 0, 0, 0);  // (copier) item whose flag is still to publish
 #pragma unroll 1
     for (int item = item0; item < n_items && !bad; item += stride, ++it) {
         if (chunk_of(item) >= n_ch) break;  // chunk-major: every later item is past the table
@@ -465,7 +472,7 @@ __device__ __forceinline__ void prep_unit(
         const int ch = cur.x, h = cur.y, tok0 = cur.z, L = cur.w, hk = h / G;
         uint8_t *const slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
         const bool more = kLoop && item + stride < n_items && chunk_of(item + stride) < n_ch;
-        if (tid == 0) {
+        if (tid == kCopier) {
             if (kLoop) {
                 // The previous item's bulk copies have read the tiles, and
                 // its generic accesses are ordered before the TMA writes.
@@ -477,7 +484,7 @@ __device__ __forceinline__ void prep_unit(
             tma_load_3d(sm.kq + 1 * kTile, tm_q, 0, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, hk, tok0, &sm.tma_bar);
-            if (kLoop && flags && pend.x >= 0) {
+            if (kLoop && flags && pend.x >= 0) {  // the previous item, behind the loads
                 publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
                 pend.x = -1;
             }
@@ -490,6 +497,8 @@ __device__ __forceinline__ void prep_unit(
             slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[2 * lane + 1];
             slot_f[kSlotDEC / 4 + 2 * lane] = sm.dec[2 * lane];
             slot_f[kSlotDEC / 4 + 2 * lane + 1] = sm.dec[2 * lane + 1];
+            sm.bg[2 * lane] = sm.beta[2 * lane] * sm.eg[2 * lane];
+            sm.bg[2 * lane + 1] = sm.beta[2 * lane + 1] * sm.eg[2 * lane + 1];
             if (lane == 31) {
                 gl[(size_t)ch * Hv + h] = sm.eg[C - 1];
                 sm.fact = sm.gam[C - 1] >= kFactorGammaMin;
@@ -524,14 +533,18 @@ __device__ __forceinline__ void prep_unit(
             uint4 *p = reinterpret_cast<uint4 *>(sm.kq + (2 * a + 1) * kTile + swz(r, cc));
             float v[8];
             unpack8(*p, v);
-            const float sc = sm.eg[r];
+            const float2 sc = make_float2(sm.eg[r], sm.eg[r]);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] *= sc;
+            for (int u = 0; u < 8; u += 2) {
+                const float2 w = mul2(make_float2(v[u], v[u + 1]), sc);
+                v[u] = w.x;
+                v[u + 1] = w.y;
+            }
             *p = pack8(v);
         }
         fence_proxy_async_smem();
         named_barrier(bar, kPrepThreads);
-        if (tid == 0) {
+        if (tid == kCopier) {
             bulk_store(slot + kSlotQ, sm.kq + kTile, kTile);
             bulk_store(slot + kSlotQ + kTile, sm.kq + 3 * kTile, kTile);
             bulk_commit_group();
@@ -566,7 +579,7 @@ __device__ __forceinline__ void prep_unit(
                 *reinterpret_cast<uint4 *>(slot + kSlotP + swz(r, c8)) = pack8(a);
             }
         }
-        if (tid == 0) bulk_wait_group_read<0>();  // the Q atoms are free
+        if (tid == kCopier) bulk_wait_group_read<0>();  // the Q atoms are free
         named_barrier(bar, kPrepThreads);
         // ---- D': warps 2-3 invert the four 16 x 16 diagonal blocks of I + A
         // by forward substitution (one column per thread); warps 0-1 write E
@@ -691,19 +704,22 @@ __device__ __forceinline__ void prep_unit(
         if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
         mph ^= 1;
         tc_fence_after();
-        // N over E (M = 64 layout: row 16 q + lane in lanes 0-15 of quadrant q).
+        // N over E.  M = 64 layout: row 16 q + l in TMEM lane 32 q + l (l < 16);
+        // the 16x256b shape hands every lane two rows' column pairs (the m8n8
+        // fragment layout), which stmatrix writes.  Matrix m of an x4 group is
+        // (row half m & 1, column group n + m / 2), its row k addressed by lane 8 m + k.
+        const int fr = 16 * q4 + 8 * ((lane >> 3) & 1) + (lane & 7), fg = lane >> 4;
         {
-            float y[32];
+            uint32_t y[32];
+            tmem_ld16x256b_x8(tmem + lane_base, y);
+            tmem_ld_wait();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                tmem_ld32f(tmem + lane_base + 32 * hf, y);
-                if (lane < 16) {
-                    const int r = 16 * q4 + lane;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        *reinterpret_cast<uint4 *>(bufE + swz(r, 4 * hf + cc)) = pack8(y + 8 * cc);
-                }
-            }
+            for (int n = 0; n < 8; n += 2)
+                stmatrix_x4(bufE + swz(fr, n + fg),
+                            pack_bf16(__uint_as_float(y[4 * n]), __uint_as_float(y[4 * n + 1])),
+                            pack_bf16(__uint_as_float(y[4 * n + 2]), __uint_as_float(y[4 * n + 3])),
+                            pack_bf16(__uint_as_float(y[4 * n + 4]), __uint_as_float(y[4 * n + 5])),
+                            pack_bf16(__uint_as_float(y[4 * n + 6]), __uint_as_float(y[4 * n + 7])));
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -723,29 +739,30 @@ __device__ __forceinline__ void prep_unit(
         mph ^= 1;
         tc_fence_after();
         // ---- T = D' - Y;  T diag(b) in place of D' (then copied to the
-        // slot), T diag(b e^gamma) into ab.
+        // slot), T diag(b e^gamma) into ab; D' read with ldmatrix in the same
+        // fragment layout as Y.
         {
-            float y[32];
+            uint32_t y[32];
+            tmem_ld16x256b_x8(tmem + lane_base, y);
+            tmem_ld_wait();
+            const int cp = 2 * (lane & 3);  // this lane's column pair within a group
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                tmem_ld32f(tmem + lane_base + 32 * hf, y);
-                if (lane < 16) {
-                    const int r = 16 * q4 + lane;
+            for (int n = 0; n < 8; n += 2) {
+                uint32_t d[4], tb[4], tbg[4];
+                ldmatrix_x4(bufD + swz(fr, n + fg), d[0], d[1], d[2], d[3]);
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint32_t off = swz(r, 4 * hf + cc);
-                        float dv[8], tb[8], tbg[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(bufD + off), dv);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int i = 32 * hf + 8 * cc + u;
-                            tb[u] = (dv[u] - y[8 * cc + u]) * sm.beta[i];
-                            tbg[u] = tb[u] * sm.eg[i];
-                        }
-                        *reinterpret_cast<uint4 *>(bufD + off) = pack8(tb);
-                        *reinterpret_cast<uint4 *>(sm.ab + off) = pack8(tbg);
-                    }
+                for (int m = 0; m < 4; ++m) {
+                    const int c = 8 * (n + (m >> 1)) + cp;
+                    const float2 bb = *reinterpret_cast<const float2 *>(sm.beta + c);
+                    const float2 bgv = *reinterpret_cast<const float2 *>(sm.bg + c);
+                    const float2 dv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&d[m]));
+                    const int yi = 4 * (n + (m >> 1)) + 2 * (m & 1);
+                    const float t0 = dv.x - __uint_as_float(y[yi]), t1 = dv.y - __uint_as_float(y[yi + 1]);
+                    tb[m] = pack_bf16(t0 * bb.x, t1 * bb.y);
+                    tbg[m] = pack_bf16(t0 * bgv.x, t1 * bgv.y);
                 }
+                stmatrix_x4(bufD + swz(fr, n + fg), tb[0], tb[1], tb[2], tb[3]);
+                stmatrix_x4(sm.ab + swz(fr, n + fg), tbg[0], tbg[1], tbg[2], tbg[3]);
             }
         }
         fence_proxy_async_smem();
@@ -761,6 +778,8 @@ __device__ __forceinline__ void prep_unit(
                 mma_bf16(tmem, smem_desc(a + 2048 * k, 2 * kTile, 1024),
                          smem_desc(b + 32 * k, 16, 1024), id, k > 0);
             mma_commit(&sm.mma_bar);
+        }
+        if (tid == kCopier) {
             bulk_store(slot + kSlotTB, bufD, kTile);
             bulk_commit_group();
         }
@@ -781,18 +800,19 @@ __device__ __forceinline__ void prep_unit(
         fence_proxy_async_smem();
         tc_fence_before();
         named_barrier(bar, kPrepThreads);
-        if (tid == 0) {
+        if (tid == kCopier) {
             bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
             bulk_commit_group();
             pend = make_int4(ch, h, 0, 0);  // published once the copies are done
         }
         if (!kLoop) break;
     }
-    if (tid == 0) {
-        if (kLoop && flags && pend.x >= 0 && !bad) publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
-        if (bad) atomicExch(err, kErrTimeout);
+    if (tid == kCopier) {
+        if (kLoop && flags && pend.x >= 0 && !bad)
+            publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
         bulk_wait_group<0>();  // shared memory must outlive the copies
     }
+    if (bad && tid == 0) atomicExch(err, kErrTimeout);
     tc_fence_before();
     named_barrier(bar, kPrepThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);

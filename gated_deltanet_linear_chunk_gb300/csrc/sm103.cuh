@@ -526,6 +526,26 @@ __device__ __forceinline__ void stmatrix_x4_trans(void *row_addr, uint32_t r0, u
                  : "memory");
 }
 
+// Stores four 8 x 8 bf16 matrices (not transposed): thread i holds, per
+// matrix m, the pair (row i / 4, columns 2 (i % 4) + {0, 1}); memory row k of
+// matrix m starts at the address given by thread 8 m + k.
+__device__ __forceinline__ void stmatrix_x4(void *row_addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                     smem_u32(row_addr)),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
+// Loads four 8 x 8 bf16 matrices in the same fragment layout as stmatrix_x4.
+__device__ __forceinline__ void ldmatrix_x4(const void *row_addr, uint32_t &r0, uint32_t &r1,
+                                            uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(row_addr))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
