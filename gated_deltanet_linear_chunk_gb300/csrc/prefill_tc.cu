@@ -248,8 +248,8 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
 // ------------------------------------------------------------------ kernel 2
 // Intra-chunk prep, one (chunk, value head) item per unit of 128 threads
 // (four warps, one per TMEM lane quadrant).  Small units keep many items in
-// flight on an SM (five per CTA of the fused kernel, five CTAs per SM of the
-// separate kernel): an item is a chain of dependent steps (tile loads, four
+// flight on an SM (four per CTA of the fused kernel, five CTAs per SM of the
+// separate kernel): an item is a chain of dependent steps (tile loads, six
 // MMA round trips, CUDA-core epilogues between barriers), and independent
 // items fill each other's waits.  Within an item one warp polls each
 // mbarrier while the others block at the unit's named barrier (no issue
@@ -259,7 +259,8 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
 // product is recomputed for each value head of a key head; it is one small
 // MMA.
 constexpr int kPrepThreads = 128;
-constexpr int kPrepUnits = 5;              // units per CTA of the fused kernel
+constexpr int kPrepUnits = 4;              // units per CTA of the fused kernel
+constexpr int kPrepCtasPerSm = 5;          // one-unit CTAs per SM of the separate kernel
 constexpr uint32_t kPrepTmemCols = 64;     // [K; Q] K^T, then N, Y and W^T in turn
 // Below this gamma_L the factors e^{gamma_t} and e^{-gamma_i} of A and P could
 // overflow fp32 (e^{-gamma_i} <= e^{-gamma_L}): such chunks take one
@@ -273,12 +274,14 @@ struct alignas(1024) PrepSmem {
     // K atom 0 | Q atom 0 | K atom 1 | Q atom 1 (two 64-column 128-byte-swizzled
     // atoms each, stacked so that one M = 128 MMA gives K K^T and Q K^T).  The
     // Q atoms are scaled in place to diag(e^gamma) Q and copied to the slot;
-    // then Q atom 0 holds E (bf16), then N = D' E, and Q atom 1 holds D'
-    // (bf16), then T diag(b) (copied to the slot).  K atom 0 + Q atom 0 finally
-    // stage W^T (copied to the slot).
+    // then Q atom 0 holds A16 (A below its diagonal 16 x 16 blocks, bf16),
+    // which becomes E, then N = D' E; Q atom 1 holds XD (the inverses of the
+    // diagonal 16 x 16 blocks of I + A, bf16), which becomes D', then
+    // T diag(b) (copied to the slot).  K atom 0 + Q atom 0 finally stage W^T
+    // (copied to the slot).
     uint8_t kq[4 * kTile];
-    // A's two diagonal 32 x 32 blocks (fp32), the inverse's scratch; then
-    // T diag(b e^gamma) (bf16, the W^T MMA's operand).
+    // A's four diagonal 16 x 16 blocks (fp32) for the forward substitution;
+    // then T diag(b e^gamma) (bf16, the W^T MMA's operand).
     uint8_t ab[kTile];
     float gam[C];
     float beta[C];
@@ -293,15 +296,11 @@ struct alignas(1024) PrepSmem {
     int fact;       // the chunk's A and P factorise (gamma_L >= kFactorGammaMin)
 };
 
-// The two fp32 diagonal 32 x 32 blocks of A: row t of block b at float
-// offset (32 b + t) * 32, its float4 group f stored at group f ^ (t % 8)
-// (conflict-free row stores, broadcast row reads).
-__device__ __forceinline__ float *ad_row(uint8_t *buf, int blk, int t) {
-    return reinterpret_cast<float *>(buf) + (32 * blk + t) * 32;
-}
-__device__ __forceinline__ int ad_f4(int f, int t) { return (f ^ (t & 7)) * 4; }
-__device__ __forceinline__ float &ad_at(uint8_t *buf, int blk, int t, int i) {
-    return ad_row(buf, blk, t)[ad_f4(i >> 2, t) + (i & 3)];
+// Row r of A's fp32 diagonal 16 x 16 block b in ab: 16 floats; blocks 260
+// floats apart (so that rows of two blocks read at once fall in different
+// banks).
+__device__ __forceinline__ float *adiag(PrepSmem &sm, int b, int r) {
+    return reinterpret_cast<float *>(sm.ab) + 260 * b + 16 * r;
 }
 
 // Element (r, c) of a bf16 image with 128-byte swizzled rows.
@@ -387,10 +386,12 @@ __device__ __forceinline__ bool unit_wait(uint64_t *bar, uint32_t parity, int wa
 }
 
 // Makes an item's slot visible device-wide and publishes its ready flag
-// (one thread; every other thread's slot writes are ordered before a unit
-// barrier this thread has passed since).
+// (the thread that issued the slot's bulk copies, which are all but the
+// kNewer most recent groups; every other thread's slot writes are ordered
+// before a unit barrier this thread has passed since).
+template <int kNewer>
 __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
-    bulk_wait_group<0>();
+    bulk_wait_group<kNewer>();
     fence_proxy_async_global();
     __threadfence();
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(epoch) : "memory");
@@ -414,7 +415,8 @@ __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
 //   P = M o Q K^T, M_ri = e^{gamma_r - gamma_i} (i <= r), to the slot;
 //   D' = blockdiag((I + A_bb)^-1), each 32 x 32 block from its two 16 x 16
 //     diagonal blocks (fp32 forward substitution) and the merge
-//     [[X1, 0], [-X2 C X1, X2]] (C the lower-left 16 x 16 block, fp32);
+//     [[X1, 0], [-X2 C X1, X2]] (C the lower-left 16 x 16 block; two M = 64
+//     MMAs);
 //   T = (I + A)^-1 = D' - (D' E) D' (two M = 64 MMAs: with two blocks
 //     (D' E)^2 = 0, so the series stops there);
 //   T diag(b) to the slot, W^T = K^T (T diag(b e^gamma))^T (M = 128) to the slot.
@@ -484,10 +486,6 @@ __device__ __forceinline__ void prep_unit(
             tma_load_3d(sm.kq + 1 * kTile, tm_q, 0, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, hk, tok0, &sm.tma_bar);
             tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, hk, tok0, &sm.tma_bar);
-            if (kLoop && flags && pend.x >= 0) {  // the previous item, behind the loads
-                publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
-                pend.x = -1;
-            }
         }
         if (warp == 1) {
             // gamma, b and the decay factors while the tiles are in flight.
@@ -548,21 +546,31 @@ __device__ __forceinline__ void prep_unit(
             bulk_store(slot + kSlotQ, sm.kq + kTile, kTile);
             bulk_store(slot + kSlotQ + kTile, sm.kq + 3 * kTile, kTile);
             bulk_commit_group();
+            // The previous item, a few thousand cycles after its last copies
+            // were issued (waiting for them at once would hold up the unit).
+            if (kLoop && flags && pend.x >= 0) {
+                publish_item<1>(flags + (size_t)pend.x * Hv + pend.y, epoch);
+                pend.x = -1;
+            }
         }
-        // ---- A's diagonal blocks (fp32, into ab) from K K^T (lanes 0-63),
-        // P from Q K^T (lanes 64-127, to the slot).  Warp-uniform branches.
+        // ---- A's four diagonal 16 x 16 blocks (fp32, into ab) from K K^T
+        // (lanes 0-63), P from Q K^T (lanes 64-127, to the slot).  A warp's
+        // TMEM loads take the same columns for every lane (warp-uniform); a
+        // lane keeps the 16 of its own block.
         const bool fact = sm.fact;
         if (q4 < 2) {
-            const int t = row, blk = q4;
+            const int t = row;
             const float gt = sm.gam[t], bt = sm.beta[t], rs = bt * sm.eg[t];
-            float *dst = ad_row(sm.ab, blk, t & 31);
 #pragma unroll 1
             for (int c8 = 0; c8 < 4; ++c8) {
                 float a[8];
-                decayed8(sm, tmem + lane_base + 32 * blk + 8 * c8, 32 * blk + 8 * c8, t - 1, fact,
+                decayed8(sm, tmem + lane_base + 32 * q4 + 8 * c8, 32 * q4 + 8 * c8, t - 1, fact,
                          bt, rs, gt, a);
-                *reinterpret_cast<float4 *>(dst + ad_f4(2 * c8, t)) = make_float4(a[0], a[1], a[2], a[3]);
-                *reinterpret_cast<float4 *>(dst + ad_f4(2 * c8 + 1, t)) = make_float4(a[4], a[5], a[6], a[7]);
+                if ((c8 >> 1) == (lane >> 4)) {
+                    float *dst = adiag(sm, t >> 4, t & 15) + 8 * (c8 & 1);
+                    *reinterpret_cast<float4 *>(dst) = make_float4(a[0], a[1], a[2], a[3]);
+                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(a[4], a[5], a[6], a[7]);
+                }
             }
         } else {
             const int r = row - 64;
@@ -581,114 +589,133 @@ __device__ __forceinline__ void prep_unit(
         }
         if (tid == kCopier) bulk_wait_group_read<0>();  // the Q atoms are free
         named_barrier(bar, kPrepThreads);
-        // ---- D': warps 2-3 invert the four 16 x 16 diagonal blocks of I + A
-        // by forward substitution (one column per thread); warps 0-1 write E
-        // and clear D' outside those blocks and the merged ones.
+        // ---- Warps 2-3 invert the four 16 x 16 diagonal blocks of I + A by
+        // forward substitution (one column per thread) into XD, the bf16
+        // image in Q atom 1 that becomes D'.  Meanwhile warps 0-1 write A16,
+        // the part of A below the diagonal 16 x 16 blocks (bf16, Q atom 0),
+        // and clear XD outside its blocks.
         if (q4 >= 2) {
             const int ft = tid - 64, fb = ft >> 4, fcol = ft & 15;  // 16-block, column
-            const int fb32 = fb >> 1, foff = 16 * (fb & 1);
             float xc[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 float a0 = (t == fcol) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                const int tr = foff + t;
+                const float *ar = adiag(sm, fb, t);
 #pragma unroll
                 for (int i = 0; i < (t & ~3); i += 4) {
-                    const float4 av = *reinterpret_cast<const float4 *>(
-                        ad_row(sm.ab, fb32, tr) + ad_f4((foff + i) >> 2, tr));
+                    const float4 av = *reinterpret_cast<const float4 *>(ar + i);
                     a0 = fmaf(-av.x, xc[i], a0);
                     a1 = fmaf(-av.y, xc[i + 1], a1);
                     a2 = fmaf(-av.z, xc[i + 2], a2);
                     a3 = fmaf(-av.w, xc[i + 3], a3);
                 }
 #pragma unroll
-                for (int i = (t & ~3); i < t; ++i)
-                    a0 = fmaf(-ad_at(sm.ab, fb32, tr, foff + i), xc[i], a0);
+                for (int i = (t & ~3); i < t; ++i) a0 = fmaf(-ar[i], xc[i], a0);
                 xc[t] = (a0 + a1) + (a2 + a3);
-            }
-            named_barrier(bar2, 64);  // the substitution's reads of A are done
-            // X1, X2: fp32 over A's diagonal 16 x 16 blocks for the merge,
-            // bf16 into D'.
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                ad_at(sm.ab, fb32, foff + t, foff + fcol) = xc[t];
-                *img_at(bufD, 32 * fb32 + foff + t, 32 * fb32 + foff + fcol) =
-                    __float2bfloat16_rn(xc[t]);
+                *img_at(bufD, 16 * fb + t, 16 * fb + fcol) = __float2bfloat16_rn(xc[t]);
             }
         } else {
             const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-            // E row t: columns 0-31 of rows 32-63 hold A, everything else 0.
-            const int t = row;
-            if (q4 == 1) {
-                const float gt = sm.gam[t], bt = sm.beta[t], rs = bt * sm.eg[t];
+            const int t = row, tb = t >> 4;  // (tb: the row's diagonal block)
+            const float gt = sm.gam[t], bt = sm.beta[t], rs = bt * sm.eg[t];
+            // A16 row t: A at columns below 16 tb, 0 from there on.  The
+            // warp loads the columns its last lane needs (2 or 6 chunks).
 #pragma unroll 1
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float a[8];
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float a[8];
+                if (c8 < 2 + 4 * q4) {
                     decayed8(sm, tmem + lane_base + 8 * c8, 8 * c8, t - 1, fact, bt, rs, gt, a);
-                    *reinterpret_cast<uint4 *>(bufE + swz(t, c8)) = pack8(a);
-                }
-            } else {
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4 *>(bufE + swz(t, cc)) = z4;
-            }
-#pragma unroll
-            for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4 *>(bufE + swz(t, cc)) = z4;
-            // D' zeros, as 16-byte chunks: rows 0-31 x columns 32-63 and rows
-            // 32-63 x columns 0-31 (4 chunks a row), and each diagonal 32-block's
-            // upper-right 16 x 16 corner (2 chunks a row): 320 chunks.
-#pragma unroll 1
-            for (int j = tid; j < 320; j += 64) {
-                int r, cc;
-                if (j < 256) {
-                    r = j >> 2;
-                    cc = (r < 32 ? 4 : 0) + (j & 3);
+                    *reinterpret_cast<uint4 *>(bufE + swz(t, c8)) = c8 < 2 * tb ? pack8(a) : z4;
                 } else {
-                    const int k = j - 256;  // block k / 32, row (k / 2) % 16 of it
-                    r = 32 * (k >> 5) + ((k >> 1) & 15);
-                    cc = 4 * (k >> 5) + 2 + (k & 1);
+                    *reinterpret_cast<uint4 *>(bufE + swz(t, c8)) = z4;
                 }
-                *reinterpret_cast<uint4 *>(bufD + swz(r, cc)) = z4;
             }
-        }
-        tc_fence_before();  // this item's last reads of [K K^T; Q K^T]
-        named_barrier(bar, kPrepThreads);
-        // Y = C X1 per 32-block (C = rows 16-31, columns 0-15), into the
-        // block's unused upper-right 16 x 16 corner (nothing this step reads);
-        // each thread 4 columns.
-        const int mb = tid >> 6, mr = (tid >> 2) & 15, mc = 4 * (tid & 3);
-        {
-            float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+            // XD row t: zero outside chunks 2 tb, 2 tb + 1.
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float c = ad_at(sm.ab, mb, 16 + mr, j);
-                const float4 x1 = *reinterpret_cast<const float4 *>(ad_row(sm.ab, mb, j) +
-                                                                    ad_f4(mc >> 2, j));
-                y0 = fmaf(c, x1.x, y0);
-                y1 = fmaf(c, x1.y, y1);
-                y2 = fmaf(c, x1.z, y2);
-                y3 = fmaf(c, x1.w, y3);
-            }
-            *reinterpret_cast<float4 *>(ad_row(sm.ab, mb, mr) + ad_f4((16 + mc) >> 2, mr)) =
-                make_float4(y0, y1, y2, y3);
-        }
-        named_barrier(bar, kPrepThreads);
-        // -X2 Y: D's lower-left 16 x 16 corner of each 32-block, in bf16.
-        {
-            float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float x2 = ad_at(sm.ab, mb, 16 + mr, 16 + k);
-                const float4 y = *reinterpret_cast<const float4 *>(ad_row(sm.ab, mb, k) +
-                                                                   ad_f4((16 + mc) >> 2, k));
-                m0 = fmaf(-x2, y.x, m0);
-                m1 = fmaf(-x2, y.y, m1);
-                m2 = fmaf(-x2, y.z, m2);
-                m3 = fmaf(-x2, y.w, m3);
-            }
-            *reinterpret_cast<uint2 *>(img_at(bufD, 32 * mb + 16 + mr, 32 * mb + mc)) =
-                make_uint2(pack_bf16(m0, m1), pack_bf16(m2, m3));
+            for (int c8 = 0; c8 < 8; ++c8)
+                if ((c8 >> 1) != tb) *reinterpret_cast<uint4 *>(bufD + swz(t, c8)) = z4;
         }
         fence_proxy_async_smem();
+        tc_fence_before();  // this item's last reads of [K K^T; Q K^T]
+        named_barrier(bar, kPrepThreads);
+        // ---- The 16 -> 32 merge on the tensor pipe.  Y = A16 XD: in its rows
+        // 16-31 x columns 0-15 and 48-63 x columns 32-47 it is C X1 of each
+        // 32 x 32 diagonal block (C = its lower-left 16 x 16 block of A); the
+        // rest of Y (from A's lower-left 32 x 32 block) is not used.
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+            const uint32_t a = smem_u32(bufE), b = smem_u32(bufD);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, smem_desc(a + 32 * k, 16, 1024), smem_desc(b + 2048 * k, kTile, 1024),
+                         id, k > 0);
+            mma_commit(&sm.mma_bar);
+        }
+        if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
+        mph ^= 1;
+        tc_fence_after();
+        // Those two 16 x 16 blocks of Y replace C in A16 (M = 64 layout: row
+        // 16 q + lane in lane 32 q + lane; quadrants 1 and 3 hold them).
+        const int mcol = (q4 & 2) ? 32 : 0;
+        if (q4 & 1) {
+            uint32_t r0[8], r1[8];
+            tmem_ld8(tmem + lane_base + mcol, r0);
+            tmem_ld8(tmem + lane_base + mcol + 8, r1);
+            tmem_ld_wait();
+            if (lane < 16) {
+                const int r = 16 * q4 + lane;
+                float y[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    y[u] = __uint_as_float(r0[u]);
+                    y[8 + u] = __uint_as_float(r1[u]);
+                }
+                *reinterpret_cast<uint4 *>(bufE + swz(r, mcol >> 3)) = pack8(y);
+                *reinterpret_cast<uint4 *>(bufE + swz(r, (mcol >> 3) + 1)) = pack8(y + 8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_barrier(bar, kPrepThreads);
+        // -XD Y: in the same two blocks, -X2 C X1, the lower-left 16 x 16
+        // block of each 32 x 32 block of D' (A negated by the descriptor).
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true, true);
+            const uint32_t a = smem_u32(bufD), b = smem_u32(bufE);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, smem_desc(a + 32 * k, 16, 1024), smem_desc(b + 2048 * k, kTile, 1024),
+                         id, k > 0);
+            mma_commit(&sm.mma_bar);
+        }
+        if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
+        mph ^= 1;
+        tc_fence_after();
+        // Into XD (which becomes D'), and zeros back into A16 (which becomes
+        // E, A's lower-left 32 x 32 block).
+        if (q4 & 1) {
+            uint32_t r0[8], r1[8];
+            tmem_ld8(tmem + lane_base + mcol, r0);
+            tmem_ld8(tmem + lane_base + mcol + 8, r1);
+            tmem_ld_wait();
+            if (lane < 16) {
+                const int r = 16 * q4 + lane;
+                float m[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    m[u] = __uint_as_float(r0[u]);
+                    m[8 + u] = __uint_as_float(r1[u]);
+                }
+                *reinterpret_cast<uint4 *>(bufD + swz(r, mcol >> 3)) = pack8(m);
+                *reinterpret_cast<uint4 *>(bufD + swz(r, (mcol >> 3) + 1)) = pack8(m + 8);
+                *reinterpret_cast<uint4 *>(bufE + swz(r, mcol >> 3)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(bufE + swz(r, (mcol >> 3) + 1)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
         named_barrier(bar, kPrepThreads);
         // ---- N = D' E  (M = 64, N = 64, K = 64)
         if (tid == 0) {
@@ -809,7 +836,7 @@ __device__ __forceinline__ void prep_unit(
     }
     if (tid == kCopier) {
         if (kLoop && flags && pend.x >= 0 && !bad)
-            publish_item(flags + (size_t)pend.x * Hv + pend.y, epoch);
+            publish_item<0>(flags + (size_t)pend.x * Hv + pend.y, epoch);
         bulk_wait_group<0>();  // shared memory must outlive the copies
     }
     if (bad && tid == 0) atomicExch(err, kErrTimeout);
@@ -818,7 +845,7 @@ __device__ __forceinline__ void prep_unit(
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 5)
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float *__restrict__ g, const float *__restrict__ beta,
                 const int *__restrict__ chunk_off, const int4 *__restrict__ table,
@@ -971,9 +998,8 @@ __device__ __noinline__ bool store_state_rows(ChainSmem &sm, const CUtensorMap *
 // The recurrence for (sequence, value head) number `bid` of the sorted order.
 // Warps: 0 loads, 1 MMAs, kS0..kS0+7 state, kS0+8..kS0+11 output, any other
 // idle.  kFused: inside the persistent kernel that also runs prep (below):
-// each warpgroup sets its register budget first (0-3: 72, state and output:
-// 128, the idle fifth: 24), the loads of chunk c wait for its ready flag,
-// and the chunk decay comes from the stage instead of the workspace.
+// the loads of chunk c wait for its ready flag, and the chunk decay comes
+// from the stage instead of the workspace.
 template <bool kSnaps, bool kLinear, bool kNoOut, int kS0, bool kFused>
 __device__ __forceinline__ void chain_role(
     ChainSmem &sm, int bid, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
@@ -1037,8 +1063,7 @@ __device__ __forceinline__ void chain_role(
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
 
-    if (kFused ? warp < 4 : warp < 2) {
-    if (kFused) setmaxnreg_dec<72>();
+    if (warp < 2) {
     if (warp == 0) {
         // ---------------- producer: TMA tiles and the prep kernel's slot;
         // chunks kPrefetch ahead are pulled into L2 so that a stage's loads
@@ -1195,7 +1220,6 @@ if (elect_one_sync()) {
         }
     }
     } else if (warp < kS0 + 8) {  // (warps below kS0 took the branch above)
-        if (kFused) setmaxnreg_inc<128>();
         // ---------------- state warps 2-9: row j, half h2 of the state's
         // columns (and of Delta's 64 tokens).  The state is kept in TMEM as
         // S^ with S = sigma S^: the chunk decay e^{gamma_L} folds into sigma,
@@ -1314,8 +1338,7 @@ if (elect_one_sync()) {
             }
         }
         if (kSnaps && lane == 0) bulk_wait_group<0>();
-    } else if (!kFused || warp < kS0 + 12) {
-        if (kFused) setmaxnreg_inc<128>();
+    } else if (warp < kS0 + 12) {
         // ---------------- output warps: o_t = S0 (e^{gamma_t} q_t) +
         // (Delta^T P^T)_t for this warp's 32 value dims, read from this
         // chunk's output accumulator with the 16x256b TMEM shape (the m8n8
@@ -1374,8 +1397,6 @@ if (elect_one_sync()) {
             }
         }
         if (leader) bulk_wait_group<0>();
-    } else if (kFused) {
-        setmaxnreg_dec<24>();  // the idle warpgroup
     }
     __syncthreads();
     if (sm.abort) {
@@ -1413,15 +1434,17 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 }
 
 // ------------------------------------------------------------------ fused prep + recurrence
-// One persistent cooperative launch, one CTA per SM.  CTAs below n_chain run
-// the recurrence of one (sequence, value head) each (warps 0, 1 and 4-15);
-// the others run two prep units each (warps 0-9 and 10-19) over the (chunk,
-// key head) items in chunk order, publishing a ready flag per item, and the
-// recurrence waits for the flag of each chunk before loading it.  Prep never
-// waits for the recurrence and all CTAs are resident (cooperative launch), so
-// every wait ends.  Prep runs on the SMs the recurrence leaves idle, during
-// the recurrence instead of before it.
+// One persistent cooperative launch, one CTA of 512 threads per SM (up to 128
+// registers a thread: the recurrence's warps compile as in the separate
+// kernel).  CTAs below n_chain run the recurrence of one (sequence, value
+// head) each (warps 0-13, 14-15 idle); the others run four prep units each
+// over the (chunk, value head) items in chunk order, publishing a ready flag
+// per item, and the recurrence waits for the flag of each chunk before
+// loading it.  Prep never waits for the recurrence and all CTAs are resident
+// (cooperative launch), so every wait ends.  Prep runs on the SMs the
+// recurrence leaves idle, during the recurrence instead of before it.
 constexpr int kFusedThreads = kPrepUnits * kPrepThreads;
+static_assert(kFusedThreads >= kChainThreads, "the recurrence's warps fit the fused CTA");
 constexpr size_t kPrepUnitBytes = sizeof(PrepSmem);  // a multiple of 1024 (alignas)
 constexpr size_t kFusedSmemBytes =
     (sizeof(ChainSmem) > kPrepUnits * kPrepUnitBytes ? sizeof(ChainSmem)
@@ -1429,9 +1452,6 @@ constexpr size_t kFusedSmemBytes =
 static_assert(kFusedSmemBytes <= 232448, "fused kernel shared memory");
 static_assert(kPrepUnits * kPrepTmemCols <= 512, "prep units' TMEM");
 static_assert(1 + 2 * kPrepUnits <= 16, "prep units' named barriers");
-// The register budgets of the recurrence role (72 x 128 + 128 x 384 + 24 x 128
-// threads) are the launch allocation of 640 threads at 96 registers.
-static_assert(72 * 128 + 128 * 384 + 24 * 128 == kFusedThreads * 96, "register split");
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
 gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1447,7 +1467,7 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     if ((int)blockIdx.x < n_chain) {
-        chain_role<false, false, false, 4, true>(
+        chain_role<false, false, false, 2, true>(
             *reinterpret_cast<ChainSmem *>(base), blockIdx.x, &tm_k, &tm_v, &tm_o, &tm_o,
             chunk_off, order, table, slots, gl, h0, out, hT, nullptr, 1, nullptr, err, N, Hk, Hv,
             flags);
@@ -1820,9 +1840,8 @@ gdn_status launch_chain(const gdn_problem &p, const TcPtrs &t, const TcMaps &m,
 }
 
 // SMs the fused kernel can run on (one CTA each) on the current device, or 0
-// when it cannot be used there: no cooperative launch, a register count other
-// than the 96 its warpgroup budgets are split from, or less than one CTA per
-// SM.  Looked up once per device (the kernel's shared-memory attribute is set
+// when it cannot be used there: no cooperative launch, or less than one CTA
+// per SM.  Looked up once per device (the kernel's shared-memory attribute is set
 // with that device current), under a lock.
 int fused_grid() {
     static std::mutex mu;
@@ -1845,7 +1864,7 @@ int fused_grid() {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gdn_fused_kernel, kFusedThreads,
                                                       kFusedSmemBytes) != cudaSuccess) {
         cudaGetLastError();
-    } else if (coop && fa.numRegs == 96 && blocks >= 1) {
+    } else if (coop && blocks >= 1) {
         grid = sms;
     }
     grid_of[dev] = grid;
@@ -1867,7 +1886,7 @@ bool fused_pays(const gdn_problem &p, int grid) {
     const int64_t chunks = (p.total_tokens + C - 1) / C + p.num_seqs - 1;
     const int64_t items = chunks * p.num_v_heads;
     const double chain = kChainStepUs * (double)((p.total_tokens / p.num_seqs + C - 1) / C);
-    const int64_t units_f = kPrepUnits * (grid - n_chain), units_s = kPrepUnits * (int64_t)grid;
+    const int64_t units_f = kPrepUnits * (grid - n_chain), units_s = kPrepCtasPerSm * (int64_t)grid;
     const double prep_f = kPrepItemUs * (double)((items + units_f - 1) / units_f);
     const double prep_s = kPrepItemUs * (double)((items + units_s - 1) / units_s);
     return std::max(prep_f, chain + kPrepItemUs) < prep_s + chain + 5.0;
