@@ -335,23 +335,32 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
 
 // Eight elements s e^{gamma_r - gamma_i} x_i of a row r of A (with b_r in s)
 // or P, columns i0 .. i0 + 7 read from TMEM; entries past `last` are 0.
-// With `fact`, e^{gamma_r - gamma_i} = e^{gamma_r} e^{-gamma_i} (rs = s e^{gamma_r}).
+// kFact: e^{gamma_r - gamma_i} = e^{gamma_r} e^{-gamma_i} (rs = s e^{gamma_r});
+// else one exponential per element.
+template <bool kFact>
 __device__ __forceinline__ void decayed8(const PrepSmem &sm, uint32_t taddr, int i0, int last,
-                                         bool fact, float s, float rs, float gr, float (&a)[8]) {
+                                         float s, float rs, float gr, float (&a)[8]) {
     uint32_t r[8];
     tmem_ld8(taddr, r);
-    const float4 *src4 = reinterpret_cast<const float4 *>(fact ? sm.einv + i0 : sm.gam + i0);
+    const float4 *src4 = reinterpret_cast<const float4 *>(kFact ? sm.einv + i0 : sm.gam + i0);
     const float4 f0 = src4[0], f1 = src4[1];
     const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
     tmem_ld_wait();
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u;
         const float x = __uint_as_float(r[u]);
-        const float v = fact ? rs * f[u] * x : s * ex2_approx((gr - f[u]) * kLog2e) * x;
-        a[u] = i <= last ? v : 0.f;
+        const float v = kFact ? rs * f[u] * x : s * ex2_approx((gr - f[u]) * kLog2e) * x;
+        a[u] = i0 + u <= last ? v : 0.f;
     }
 }
+
+// decayed8 with the factorised form chosen once for the chunk (a branch
+// that is the same for the whole unit, outside the loops).
+#define DECAYED8(taddr, i0, last, s, rs, gr, a)                        \
+    do {                                                                \
+        if (fact) decayed8<true>(sm, taddr, i0, last, s, rs, gr, a);   \
+        else decayed8<false>(sm, taddr, i0, last, s, rs, gr, a);       \
+    } while (0)
 
 // L2 prefetch of what an item will load: its K and Q tiles and its g and
 // beta values (64 tokens, one value head: strided, so every line is fetched
@@ -525,20 +534,25 @@ __device__ __forceinline__ void prep_unit(
         mph ^= 1;
         tc_fence_after();
         // ---- diag(e^gamma) Q in place in the Q atoms, then copied to the slot.
-#pragma unroll 2
-        for (int idx = tid; idx < 2 * C * 8; idx += kPrepThreads) {
-            const int a = idx / (C * 8), r = (idx >> 3) & (C - 1), cc = idx & 7;
-            uint4 *p = reinterpret_cast<uint4 *>(sm.kq + (2 * a + 1) * kTile + swz(r, cc));
-            float v[8];
-            unpack8(*p, v);
-            const float2 sc = make_float2(sm.eg[r], sm.eg[r]);
+        // A thread scales 16-byte chunk tid % 8 of rows tid / 8 + 16 j of both
+        // atoms (rows 16 apart share the swizzle, so the address steps by 2 KB).
+        {
+            const int r0 = tid >> 3;
+            uint8_t *p0 = sm.kq + kTile + swz(r0, tid & 7);
 #pragma unroll
-            for (int u = 0; u < 8; u += 2) {
-                const float2 w = mul2(make_float2(v[u], v[u + 1]), sc);
-                v[u] = w.x;
-                v[u + 1] = w.y;
+            for (int j = 0; j < 8; ++j) {
+                uint4 *p = reinterpret_cast<uint4 *>(p0 + (j >> 2) * (2 * kTile) + (j & 3) * 2048);
+                const float e = sm.eg[r0 + 16 * (j & 3)];
+                float v[8];
+                unpack8(*p, v);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    const float2 w = mul2(make_float2(v[u], v[u + 1]), make_float2(e, e));
+                    v[u] = w.x;
+                    v[u + 1] = w.y;
+                }
+                *p = pack8(v);
             }
-            *p = pack8(v);
         }
         fence_proxy_async_smem();
         named_barrier(bar, kPrepThreads);
@@ -564,8 +578,7 @@ __device__ __forceinline__ void prep_unit(
 #pragma unroll 1
             for (int c8 = 0; c8 < 4; ++c8) {
                 float a[8];
-                decayed8(sm, tmem + lane_base + 32 * q4 + 8 * c8, 32 * q4 + 8 * c8, t - 1, fact,
-                         bt, rs, gt, a);
+                DECAYED8(tmem + lane_base + 32 * q4 + 8 * c8, 32 * q4 + 8 * c8, t - 1, bt, rs, gt, a);
                 if ((c8 >> 1) == (lane >> 4)) {
                     float *dst = adiag(sm, t >> 4, t & 15) + 8 * (c8 & 1);
                     *reinterpret_cast<float4 *>(dst) = make_float4(a[0], a[1], a[2], a[3]);
@@ -579,7 +592,7 @@ __device__ __forceinline__ void prep_unit(
             for (int c8 = 0; c8 < 8; ++c8) {
                 float a[8];
                 if (c8 < 4 || q4 == 3) {  // (rows 0-31 have nothing at columns 32-63)
-                    decayed8(sm, tmem + lane_base + 8 * c8, 8 * c8, r, fact, 1.f, rs, gr, a);
+                    DECAYED8(tmem + lane_base + 8 * c8, 8 * c8, r, 1.f, rs, gr, a);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 8; ++u) a[u] = 0.f;
@@ -624,7 +637,7 @@ __device__ __forceinline__ void prep_unit(
             for (int c8 = 0; c8 < 8; ++c8) {
                 float a[8];
                 if (c8 < 2 + 4 * q4) {
-                    decayed8(sm, tmem + lane_base + 8 * c8, 8 * c8, t - 1, fact, bt, rs, gt, a);
+                    DECAYED8(tmem + lane_base + 8 * c8, 8 * c8, t - 1, bt, rs, gt, a);
                     *reinterpret_cast<uint4 *>(bufE + swz(t, c8)) = c8 < 2 * tb ? pack8(a) : z4;
                 } else {
                     *reinterpret_cast<uint4 *>(bufE + swz(t, c8)) = z4;
@@ -830,7 +843,14 @@ __device__ __forceinline__ void prep_unit(
         if (tid == kCopier) {
             bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
             bulk_commit_group();
-            pend = make_int4(ch, h, 0, 0);  // published once the copies are done
+            if (kLoop && flags && it == 0) {
+                // The first items gate the start of every recurrence: publish
+                // at once.  Later ones are published behind the next item's
+                // loads and copies, when their own copies have long finished.
+                publish_item<0>(flags + (size_t)ch * Hv + h, epoch);
+            } else {
+                pend = make_int4(ch, h, 0, 0);
+            }
         }
         if (!kLoop) break;
     }
@@ -1088,9 +1108,11 @@ __device__ __forceinline__ void chain_role(
             #pragma unroll 1
             for (int c = 0; c < nc; ++c) {
                 const int s = c & 1;
-                if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
+                // (in the fused kernel the chunk's ready flag first: its
+                // acquire overlaps the wait for the stage)
                 if (kFused && !wait_ready(flags + (size_t)(c_begin + c) * Hv + h, &sm.abort))
                     break;
+                if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
                 ChainStage &st = sm.st[s];
@@ -1472,6 +1494,7 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             chunk_off, order, table, slots, gl, h0, out, hT, nullptr, 1, nullptr, err, N, Hk, Hv,
             flags);
     } else {
+        griddep_wait();  // (a programmatic dependent of the chunk table kernel)
         const int u = threadIdx.x / kPrepThreads;
         const int pcta = blockIdx.x - n_chain, ncta = gridDim.x - n_chain;
         prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
@@ -1897,28 +1920,37 @@ bool fused_pays(const gdn_problem &p, int grid) {
 // kernels; the chunk table is already in place).
 bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, const TcMaps &m,
                   const float *g, const float *beta, const float *h0, void *out, float *hT,
-                  int grid, cudaStream_t stream) {
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeCooperative;
-    attr.val.cooperative = 1;
+                  int grid, cudaStream_t stream, bool pdl) {
+    // Cooperative (every CTA resident, so the waits on ready flags end) and,
+    // unless the call is timed, a programmatic dependent of the chunk table
+    // kernel (its CTAs are placed and set up while the table is written; they
+    // wait for it before reading it).  Without the second attribute if the
+    // driver refuses the pair.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kFusedThreads);
     cfg.dynamicSmemBytes = kFusedSmemBytes;
     cfg.stream = stream;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cfg.attrs = attr;
     const int n_chain = p.num_seqs * p.num_v_heads;
     const int n_items = (int)(w.max_chunks * p.num_v_heads);
-    if (cudaLaunchKernelEx(&cfg, gdn_fused_kernel, m.tq, m.tk, m.tv, m.to, g, beta,
-                           (const int *)t.chunk_off, (const int *)t.order, (const int4 *)t.table,
-                           t.slots, t.gl, h0, static_cast<__nv_bfloat16 *>(out), hT, t.err,
-                           t.flags, (const int *)t.porder, p.num_seqs, p.num_k_heads,
-                           p.num_v_heads, n_chain, n_items) != cudaSuccess) {
+    for (int na = pdl ? 2 : 1; na >= 1; --na) {
+        cfg.numAttrs = na;
+        if (cudaLaunchKernelEx(&cfg, gdn_fused_kernel, m.tq, m.tk, m.tv, m.to, g, beta,
+                               (const int *)t.chunk_off, (const int *)t.order,
+                               (const int4 *)t.table, t.slots, t.gl, h0,
+                               static_cast<__nv_bfloat16 *>(out), hT, t.err, t.flags,
+                               (const int *)t.porder, p.num_seqs, p.num_k_heads, p.num_v_heads,
+                               n_chain, n_items) == cudaSuccess)
+            return true;
         cudaGetLastError();
-        return false;
     }
-    return true;
+    return false;
 }
 
 }  // namespace
@@ -1954,7 +1986,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         gdn_status st = launch_table(p, w, t, cu, 0, true, stream, tm);
         if (st != GDN_OK) return st;
         time_mark(tm, 2, stream);  // (no separate prep launch)
-        if (launch_fused(p, w, t, m, g, beta, h0, out, hT, grid, stream)) {
+        if (launch_fused(p, w, t, m, g, beta, h0, out, hT, grid, stream, pdl)) {
             time_mark(tm, 3, stream);
             time_fused(tm, true);
             return GDN_OK;
