@@ -413,8 +413,9 @@ __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
 // item0 + stride, ... below n_items (item = chunk * Hv + value head,
 // chunk-major).  With `flags`, each finished item publishes `epoch` into
 // flags[chunk * Hv + h] (release, device scope) once its workspace slot is
-// written.  kLoop = false: exactly one item (blockIdx.x = chunk, blockIdx.y =
-// value head), compiled without the loop.
+// written.  kLoop = false: exactly one item, compiled without the loop.
+// `relinquish`: give up the CTA's TMEM allocation permit after allocating
+// (only when the CTA allocates nothing after this unit).
 //
 // Per item:
 //   gamma = cumsum(g), b, e^gamma, e^{gamma_L - gamma};  [K; Q] K^T (M = 128);
@@ -435,7 +436,7 @@ __device__ __forceinline__ void prep_unit(
     const float *__restrict__ beta, const int *__restrict__ chunk_off,
     const int4 *__restrict__ table, uint8_t *__restrict__ slots, float *__restrict__ gl,
     int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int bar2, int item0,
-    int stride, int n_items, unsigned *flags, unsigned epoch,
+    int stride, int n_items, unsigned *flags, unsigned epoch, bool relinquish,
     const int *__restrict__ porder = nullptr) {
     const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
@@ -445,13 +446,13 @@ __device__ __forceinline__ void prep_unit(
     uint8_t *const bufE = sm.kq + kTile;      // Q atom 0
     uint8_t *const bufD = sm.kq + 3 * kTile;  // Q atom 1
     const int n_ch = chunk_off[N];
-    auto chunk_of = [&](int item) { return kLoop ? item / Hv : (int)blockIdx.x; };
+    auto chunk_of = [&](int item) { return item / Hv; };
     // Chunk-table entry of an item: {chunk, value head, first token, length}.
     auto locate = [&](int item) {
         const int ci = chunk_of(item);
         const int ch = (kLoop && porder) ? porder[ci] : ci;
         const int4 e = table[ch];
-        return make_int4(ch, kLoop ? item % Hv : (int)blockIdx.y, e.y, e.z);
+        return make_int4(ch, item % Hv, e.y, e.z);
     };
 
     if (tid == 0) {
@@ -466,7 +467,7 @@ __device__ __forceinline__ void prep_unit(
         tmem_alloc(&sm.tmem, kPrepTmemCols);
         // The permit is the CTA's: with several units in one CTA (kLoop) the
         // others may still have to allocate.
-        if (!kLoop) tmem_relinquish();
+        if (relinquish) tmem_relinquish();
     }
     tc_fence_before();
     named_barrier(bar, kPrepThreads);
@@ -863,6 +864,10 @@ __device__ __forceinline__ void prep_unit(
     tc_fence_before();
     named_barrier(bar, kPrepThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+    if (tid == 0) {  // (the memory may hold something else next)
+        mbar_inval(&sm.tma_bar);
+        mbar_inval(&sm.mma_bar);
+    }
 }
 
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
@@ -882,7 +887,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if ((int)blockIdx.x >= chunk_off[N]) return;
     const int item = blockIdx.x * Hv + blockIdx.y;
     prep_unit<false>(sm, &tm_q, &tm_k, g, beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
-                     threadIdx.x, 1, 2, item, 1, item + 1, nullptr, 0u);
+                     threadIdx.x, 1, 2, item, 1, item + 1, nullptr, 0u, true);
 }
 
 // ------------------------------------------------------------------ kernel 3
@@ -1028,7 +1033,8 @@ __device__ __forceinline__ void chain_role(
     const uint8_t *__restrict__ slots, const float *__restrict__ gl,
     const float *__restrict__ h0, __nv_bfloat16 *__restrict__ out, float *__restrict__ hT,
     float *__restrict__ snaps, int snap_stride, const int *__restrict__ snap_off,
-    int *__restrict__ err, int N, int Hk, int Hv, const unsigned *__restrict__ flags) {
+    int *__restrict__ err, int N, int Hk, int Hv, const unsigned *__restrict__ flags,
+    int c_flagged = 0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     griddep_wait();  // a programmatic dependent of prep: wait for its slots
     const int n = order[bid / Hv], h = bid % Hv;
@@ -1110,7 +1116,8 @@ __device__ __forceinline__ void chain_role(
                 const int s = c & 1;
                 // (in the fused kernel the chunk's ready flag first: its
                 // acquire overlaps the wait for the stage)
-                if (kFused && !wait_ready(flags + (size_t)(c_begin + c) * Hv + h, &sm.abort))
+                if (kFused && c >= c_flagged &&
+                    !wait_ready(flags + (size_t)(c_begin + c) * Hv + h, &sm.abort))
                     break;
                 if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
@@ -1488,19 +1495,46 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    griddep_wait();  // (a programmatic dependent of the chunk table kernel)
+    const int u = threadIdx.x / kPrepThreads;
     if ((int)blockIdx.x < n_chain) {
+        // The recurrence's first kPrepUnits chunks are prepped here, one per
+        // unit, before it starts (the prep CTAs begin with the chunks after
+        // them): the recurrence then waits for its own first chunks only,
+        // not for the first round of every prep unit of the grid.
+        const int n = order[blockIdx.x / Hv], h = blockIdx.x % Hv;
+        const int c_begin = chunk_off[n];
+        const int n_local = min(chunk_off[n + 1] - c_begin, kPrepUnits);
+        if (u < n_local) {
+            const int item = (c_begin + u) * Hv + h;
+            prep_unit<false>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q,
+                             &tm_k, g, beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
+                             threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u, item, 1,
+                             item + 1, nullptr, 0u, false);
+        }
+        fence_proxy_async_global();  // (this thread's slot writes, before the loads of them)
+        __syncthreads();
         chain_role<false, false, false, 2, true>(
             *reinterpret_cast<ChainSmem *>(base), blockIdx.x, &tm_k, &tm_v, &tm_o, &tm_o,
             chunk_off, order, table, slots, gl, h0, out, hT, nullptr, 1, nullptr, err, N, Hk, Hv,
-            flags);
+            flags, n_local);
     } else {
-        griddep_wait();  // (a programmatic dependent of the chunk table kernel)
-        const int u = threadIdx.x / kPrepThreads;
+        // Skip what the recurrences prep themselves: in the prep order (by
+        // position in the sequence) the first sum_n min(chunks_n, kPrepUnits)
+        // chunks.
+        __shared__ int s_first;
+        if (threadIdx.x == 0) {
+            int s = 0;
+            for (int m = 0; m < N; ++m) s += min(chunk_off[m + 1] - chunk_off[m], kPrepUnits);
+            s_first = s;
+        }
+        __syncthreads();
         const int pcta = blockIdx.x - n_chain, ncta = gridDim.x - n_chain;
         prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                         threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u,
-                        kPrepUnits * pcta + u, kPrepUnits * ncta, n_items, flags, 1u, porder);
+                        s_first * Hv + kPrepUnits * pcta + u, kPrepUnits * ncta, n_items, flags,
+                        1u, false, porder);
     }
 }
 

@@ -34,6 +34,12 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
                  : "memory");
 }
 
+// Invalidates an mbarrier whose phases are all complete, before its shared
+// memory is used for something else.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
