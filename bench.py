@@ -109,19 +109,31 @@ def flops_of(T, Hv):
     return T * Hv * FLOPS_PER_TOKEN_HEAD
 
 
+def code_digest(path):
+    """SHA-256 of a source file's code: `//` comments, surrounding blanks and
+    empty lines dropped, so that a comment edit keeps a recorded profile valid
+    and any code change voids it."""
+    import hashlib
+    lines = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            code = line.split("//", 1)[0].strip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def recorded_traffic(kernel):
     """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
-    summary, or None when the kernel source has changed since it was taken."""
-    import hashlib
+    summary, or None when the kernel's code has changed since it was taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "prefill_traffic.json")) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, "gated_deltanet_linear_chunk_gb300", "csrc",
-                               "prefill_tc.cu"), "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
+        digest = code_digest(os.path.join(ROOT, "gated_deltanet_linear_chunk_gb300", "csrc",
+                                          "prefill_tc.cu"))
     except (OSError, ValueError):
         return None
-    if rec.get("source_sha256") != digest or kernel not in rec.get("bytes_per_launch", {}):
+    if rec.get("code_sha256") != digest or kernel not in rec.get("bytes_per_launch", {}):
         return None
     return rec["bytes_per_launch"][kernel]
 
@@ -315,6 +327,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     gdn.library()
+    gdn.gdn_prefill_fused_mode(args.fused_mode)
     peaks, peak_kind = load_peaks()
     stream = torch.cuda.current_stream()
 
@@ -588,6 +601,7 @@ def run_ours(args, rank, world, local):
         "timing": {"ms_per_step": "median of the timed steps", "mean_ms": statistics.mean(step_ms),
                    "min_ms": min(step_ms), "max_ms": max(step_ms)},
         "gpu_launches": launches_per_step * args.steps,
+        "prefill_fused_mode": args.fused_mode,
         "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": traffic,
                      "kernel": dom, "kernel_us": k_us[dom],
@@ -643,6 +657,10 @@ def main(argv=None):
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--ref-tokens", type=int, default=4000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-mode", type=int, choices=(0, 1, 2), default=2,
+                    help="when the prefill uses its fused prep + recurrence kernel "
+                         "(gdn_prefill_fused_mode: 0 never, 1 whenever it fits, "
+                         "2 by the library's cost model, its default)")
     args = ap.parse_args(argv)
     rank, world, local = dist_setup()
     if args.impl == "reference":

@@ -4,30 +4,39 @@
 //   1. gdn_chunk_table_kernel  one CTA: chunk offsets of every sequence, a
 //      (sequence, first token, length) table of all chunks and the order in
 //      which the recurrence CTAs take sequences (longest first).
-//   2. gdn_prep_kernel         one CTA per (chunk, key head), all chunks at
-//      once: the intra-chunk prep, for every value head of the key head:
+//   2. gdn_prep_kernel         one unit of 128 threads per (chunk, value
+//      head) item, all chunks at once: the intra-chunk prep,
 //        gamma = cumsum(g); [K; Q] K^T in one M = 128 MMA (K K^T and Q K^T);
 //        A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i), i < t;
 //        T = (I + A)^-1 as  T = D' - (D' E) D',  where D' holds the inverses
-//          of the two 32 x 32 diagonal blocks of I + A (fp32 forward
-//          substitution) and E the lower-left block of A (two MMAs; with
-//          only two blocks, (D' E)^2 = 0, so the series stops there);
+//          of the two 32 x 32 diagonal blocks of I + A (each from its two
+//          16 x 16 diagonal blocks, inverted by fp32 forward substitution
+//          and merged by two MMAs) and E the lower-left block of A (two
+//          MMAs; with only two blocks, (D' E)^2 = 0, so the series stops
+//          there);
 //        W^T = K^T (T diag(b e^gamma))^T  (MMA, M = 128);
 //        P = M o Q K^T,  M_ri = e^{gamma_r - gamma_i} for i <= r;
-//      and stores W^T, T diag(b), P (bf16, as swizzled shared-memory tile
-//      images), e^gamma and e^{gamma_L - gamma} in the workspace.
+//      and stores W^T, T diag(b), P, diag(e^gamma) Q (bf16, as swizzled
+//      shared-memory tile images), e^gamma and e^{gamma_L - gamma} in the
+//      workspace.
 //   3. gdn_chain_kernel        one CTA per (sequence, value head): the
 //      inter-chunk recurrence and the output, warp-specialised: one thread
-//      issues TMA loads, one issues MMAs, eight warps run the epilogues.  The
-//      fp32 state S (dv x dk) stays in tensor memory for the whole sequence;
-//      per chunk, with a bf16 copy S0 of the chunk's start state in shared
-//      memory as the MMA operand:
+//      issues TMA loads, one issues MMAs, eight warps run the state
+//      epilogues and four the output.  The fp32 state S (dv x dk) stays in
+//      tensor memory for the whole sequence (as sigma S^, a running scale
+//      times a stored state); per chunk, with a bf16 copy -S0 of the chunk's
+//      start state in tensor memory as the MMA operand:
 //         Delta^T = V^T (T diag b)^T - S0 W^T       (both MMAs into one tile)
 //         S      <- e^{gamma_L} S + (diag(e^{gamma_L - gamma}) Delta)^T K
 //         O^T     = diag(e^gamma)-scaled S0 Q^T + Delta^T P^T
 //      The two MMAs that carry the state from chunk to chunk (S0 W^T, then
 //      the update of S) and their epilogues are the critical path; the output
 //      MMAs and the next chunk's loads run beside them.
+//
+// Instead of 2 and 3, gdn_fused_kernel can run both in one cooperative
+// launch: the recurrences on some SMs, the prep units on the others, each
+// recurrence waiting for a ready flag per (chunk, value head) before it loads
+// the chunk.
 //
 // The algorithm is the chunked (WY/UT) form of the Gated DeltaNet recurrence
 // with chunk length 64, split into intra-chunk prep, inter-chunk state

@@ -28,8 +28,9 @@
  * allocates device memory, never frees, never synchronises, and launches only
  * on the given stream.  Calls are reentrant.  The process-wide state is:
  *   - per device, an attribute cache (SM count, whether the fused prefill
- *     kernel fits and its launch attribute), filled once per device under a
- *     lock;
+ *     kernel fits and its launch attribute, the resident CTAs of the
+ *     persistent decode kernels and their shared-memory attribute), filled
+ *     once per device and kernel under a lock;
  *   - the fused-path mode of gdn_prefill_fused_mode (an atomic integer);
  *   - per device, the upload and download streams of gdn_chunk_prefill_host
  *     (created at its first call on that device);
@@ -125,7 +126,8 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem);
  * For bf16 and dk = dv = 128, when the N x Hv recurrences leave at least 16
  * SMs free, the intra-chunk prep and the recurrence run as one cooperative
  * launch: prep on the free SMs, publishing each chunk as it is done (every
- * sequence's chunk c before any chunk c + 1), and the recurrences following.  Otherwise they are separate
+ * sequence's chunk c before any chunk c + 1), and the recurrences following
+ * (each first preps its own first four chunks).  Otherwise they are separate
  * kernels.  The results are the same either way.  By default the fused
  * kernel is used when a cost model of the two paths expects it to be faster
  * (long sequences with few (sequence, value head) pairs); see

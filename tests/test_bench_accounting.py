@@ -59,18 +59,19 @@ def test_verify_bytes_are_the_tensors_a_call_moves():
         assert bench.verify_bytes(N, K, Hk, Hv, D, state_bytes) == moved
 
 
-def test_traffic_record_is_dropped_when_the_source_changes(tmp_path, monkeypatch):
+def test_traffic_record_is_dropped_when_the_code_changes(tmp_path, monkeypatch):
     src = tmp_path / "gated_deltanet_linear_chunk_gb300" / "csrc" / "prefill_tc.cu"
     src.parent.mkdir(parents=True)
-    src.write_text("// kernel source v1\n")
+    src.write_text("// kernel source\nint x = 1;  // one\n")
     (tmp_path / "profiles").mkdir()
-    rec = {"source_sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
-           "bytes_per_launch": {"fused": 123}}
+    rec = {"code_sha256": bench.code_digest(str(src)), "bytes_per_launch": {"fused": 123}}
     (tmp_path / "profiles" / "prefill_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.recorded_traffic("fused") == 123
     assert bench.recorded_traffic("prep") is None       # not captured
-    src.write_text("// kernel source v2\n")
+    src.write_text("// the same kernel, comments reworded\n\nint x = 1;  // still one\n")
+    assert bench.recorded_traffic("fused") == 123       # comments do not count
+    src.write_text("// kernel source\nint x = 2;  // one\n")
     assert bench.recorded_traffic("fused") is None      # stale record
 
 
@@ -78,7 +79,7 @@ def test_committed_traffic_record_is_well_formed():
     with open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "profiles",
                            "prefill_traffic.json")) as f:
         rec = json.load(f)
-    assert len(rec["source_sha256"]) == 64
+    assert len(rec["code_sha256"]) == 64
     for kernel, total in rec["bytes_per_launch"].items():
         assert total == sum(rec["read_write"][kernel])
         # at least the compulsory bytes of the 4000-token workload it was taken on
