@@ -114,16 +114,33 @@ WsLayout ws_layout(const gdn_problem &p) {
 // when N is large.  Malformed cu_seqlens (not starting at 0, decreasing, not
 // ending at T, or more chunks than the workspace holds) record an error and
 // make the whole call a no-op.
+// Sequences whose chunk offsets the table kernel keeps in shared memory
+// (more than this: it reads them back from the workspace).
+constexpr int kTableSmemSeqs = 4096;
+
+// Inclusive sum over the warp of x (lane order).
+__device__ __forceinline__ int warp_incl_scan(int x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
 __global__ void __launch_bounds__(1024)
 gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t max_chunks,
                        int snap_stride, int *__restrict__ err, int *__restrict__ chunk_off,
                        int *__restrict__ snap_off, int *__restrict__ order,
                        int4 *__restrict__ table, unsigned *__restrict__ flags, int n_flags,
                        int *__restrict__ porder) {
-    __shared__ int s_scan[1024], s_scan2[1024];
+    __shared__ int s_off[kTableSmemSeqs + 1];
+    __shared__ int s_wsum[32], s_wsum2[32];
     __shared__ int s_carry, s_carry2;
     __shared__ int s_bad;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool in_smem = N <= kTableSmemSeqs;
     griddep_launch_dependents();  // prep may be scheduled; it waits for this grid
     for (int i = tid; i < n_flags; i += 1024) flags[i] = 0u;
     if (tid == 0) {
@@ -133,6 +150,8 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
         *err = kErrNone;
     }
     __syncthreads();
+    // Chunk (and snapshot slot) offsets: a scan over the sequences, 1024 at a
+    // time (warp scans, then a scan of the 32 warp sums).
     for (int base = 0; base < N; base += 1024) {
         const int n = base + tid;
         int nch = 0;
@@ -144,25 +163,28 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
         // Snapshot slots of the sequence: one per snap_stride chunks, the
         // last chunk always included.
         const int nsn = (n < N && snap_stride > 0) ? (nch + snap_stride - 1) / snap_stride : 0;
-        s_scan[tid] = nch;
-        s_scan2[tid] = nsn;
-        __syncthreads();
-        for (int off = 1; off < 1024; off <<= 1) {
-            const int x = tid >= off ? s_scan[tid - off] : 0;
-            const int x2 = tid >= off ? s_scan2[tid - off] : 0;
-            __syncthreads();
-            s_scan[tid] += x;
-            s_scan2[tid] += x2;
-            __syncthreads();
+        const int a = warp_incl_scan(nch), a2 = warp_incl_scan(nsn);
+        if (lane == 31) {
+            s_wsum[warp] = a;
+            s_wsum2[warp] = a2;
         }
+        __syncthreads();
+        if (warp == 0) {
+            s_wsum[lane] = warp_incl_scan(s_wsum[lane]);
+            s_wsum2[lane] = warp_incl_scan(s_wsum2[lane]);
+        }
+        __syncthreads();
+        const int pre = s_carry + (warp > 0 ? s_wsum[warp - 1] : 0);
+        const int pre2 = s_carry2 + (warp > 0 ? s_wsum2[warp - 1] : 0);
         if (n < N) {
-            chunk_off[n] = s_carry + s_scan[tid] - nch;
-            snap_off[n] = s_carry2 + s_scan2[tid] - nsn;
+            chunk_off[n] = pre + a - nch;
+            snap_off[n] = pre2 + a2 - nsn;
+            if (in_smem) s_off[n] = pre + a - nch;
         }
         __syncthreads();
-        if (tid == 1023) {
-            s_carry += s_scan[1023];
-            s_carry2 += s_scan2[1023];
+        if (tid == 0) {
+            s_carry += s_wsum[31];
+            s_carry2 += s_wsum2[31];
         }
         __syncthreads();
     }
@@ -171,6 +193,7 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
         if (s_bad) *err = kErrCuSeqlens;
         snap_off[N] = s_carry2;
         chunk_off[N] = s_bad ? 0 : s_carry;
+        if (in_smem) s_off[N] = s_carry;
     }
     __syncthreads();
     if (s_bad) {
@@ -178,14 +201,17 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
         for (int n = tid; n < N; n += 1024) order[n] = n;
         return;
     }
+    // Chunk offsets of this call (block-visible: shared memory, or the
+    // workspace written above).
+    const int *off = in_smem ? s_off : chunk_off;
     const int total = s_carry;
     for (int ch = tid; ch < total; ch += 1024) {
-        int lo = 0, hi = N - 1;  // last n with chunk_off[n] <= ch
+        int lo = 0, hi = N - 1;  // last n with off[n] <= ch
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (chunk_off[mid] <= ch) lo = mid; else hi = mid - 1;
+            if (off[mid] <= ch) lo = mid; else hi = mid - 1;
         }
-        const int c = ch - chunk_off[lo];
+        const int c = ch - off[lo];
         const int tok0 = cu[lo] + c * C;
         table[ch] = make_int4(lo, tok0, min(C, cu[lo + 1] - tok0), c);
         if (porder) {
@@ -194,7 +220,7 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
             // chunk c + 1.
             int rank = 0;
             for (int m = 0; m < N; ++m) {
-                const int nm = chunk_off[m + 1] - chunk_off[m];
+                const int nm = off[m + 1] - off[m];
                 rank += min(c, nm) + ((m < lo && nm > c) ? 1 : 0);
             }
             porder[rank] = ch;
@@ -205,10 +231,10 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
             order[n] = n;
             continue;
         }
-        const int mine = chunk_off[n + 1] - chunk_off[n];
+        const int mine = off[n + 1] - off[n];
         int rank = 0;
         for (int m = 0; m < N; ++m) {
-            const int other = chunk_off[m + 1] - chunk_off[m];
+            const int other = off[m + 1] - off[m];
             rank += (other > mine) || (other == mine && m < n);
         }
         order[rank] = n;
