@@ -18,8 +18,8 @@
 // The step is a read-modify-write of the state, so it is bound by HBM
 // bandwidth: 2 * dv * dk * sizeof(state) bytes per (n, h) against ~6 dv dk
 // flops.  The state is cut into tiles of whole rows (contiguous in memory);
-// a persistent grid of two CTAs per SM walks the tiles with a cp.async
-// pipeline a few tiles deep into shared memory, so that the next tiles
+// a persistent grid of one or two CTAs per SM walks the tiles with a
+// cp.async pipeline a few tiles deep into shared memory, so that the next tiles
 // (with their k, q, v, g and beta) are in flight while the current one is
 // computed and the bytes in flight are bounded by shared memory, not by
 // registers.  The compute reads a tile with L lanes per state row (8 for an
@@ -147,9 +147,10 @@ template <typename TS, int DK, int ROWS> struct Tile {
 
 // Decode pipeline shape per state type (measured on GB300, 64 x 48 heads of
 // 128 x 128): state bytes per tile and tiles in flight per CTA, the current
-// one included; two CTAs per SM either way.
+// one included.  fp32: 4 x 32 KB, one CTA per SM; 16 bits: 6 x 16 KB, two
+// CTAs per SM.
 template <typename TS> constexpr int decode_tile_bytes() { return sizeof(TS) == 4 ? 32768 : 16384; }
-template <typename TS> constexpr int decode_stages() { return sizeof(TS) == 4 ? 3 : 6; }
+template <typename TS> constexpr int decode_stages() { return sizeof(TS) == 4 ? 4 : 6; }
 
 template <typename TS, int DK> constexpr int decode_rows() {
     return decode_tile_bytes<TS>() / (DK * (int)sizeof(TS)) < DK
