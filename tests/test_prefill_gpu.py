@@ -38,6 +38,23 @@ def test_zero_start_without_initial_state():
     check_prefill(p, TOL_BF16)
 
 
+def test_more_sequences_than_the_table_keeps_on_chip():
+    """4200 sequences of 0 to 6 tokens (every chunk ragged, many sequences
+    empty), one key and one value head: more sequences than the chunk table
+    kernel keeps offsets for in shared memory and sorts by length (4096), so
+    it reads the offsets back from the workspace and keeps the given order.
+    Every output token against the oracle."""
+    rng = np.random.default_rng(7)
+    lens = rng.integers(0, 7, size=4200).tolist()
+    p = inputs.prefill_inputs(lens, 1, 1, 128, 128, dtype=torch.bfloat16, seed=7)
+    out, _ = run_prefill(p, final=False)
+    o_ref, _, vh = oracle_prefill(p)
+    e_out = rel(f64(out[:, vh]), o_ref)
+    assert np.isfinite(f64(out)).all(), "non-finite output"
+    assert e_out <= TOL_BF16, f"out rel err {e_out:.3e}"
+    print(f"[parity] N=4200 short sequences, T={p.q.shape[0]}: out {e_out:.3e}")
+
+
 def test_t4000_48_heads():
     """T=4000 (62 full chunks + 32), 16 key / 48 value heads, d=128, bf16,
     zero start: every token of every head."""
