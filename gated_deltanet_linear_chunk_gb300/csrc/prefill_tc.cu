@@ -99,10 +99,11 @@ WsLayout ws_layout(const gdn_problem &p) {
     w.table = align_up(w.order + 4 * (size_t)p.num_seqs, 256);
     w.gl = align_up(w.table + 16 * (size_t)w.max_chunks, 256);  // e^{gamma_L} per (chunk, value head)
     w.tiles = align_up(w.gl + 4 * (size_t)w.max_chunks * p.num_v_heads, 1024);
-    // Ready flag per (chunk, value head) for the fused prep + recurrence kernel.
+    // Ready flag per (chunk, value head) for the fused prep + recurrence kernel,
+    // then the ticket its prep units draw items from,
     w.flags = w.tiles + (size_t)w.max_chunks * p.num_v_heads * kSlotBytes;
     // and the order in which its prep units take the chunks.
-    w.porder = align_up(w.flags + 4 * (size_t)w.max_chunks * p.num_v_heads, 256);
+    w.porder = align_up(w.flags + 4 * ((size_t)w.max_chunks * p.num_v_heads + 1), 256);
     w.total = align_up(w.porder + 4 * (size_t)w.max_chunks, 256);
     return w;
 }
@@ -246,6 +247,32 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
 // with g = 0 past the end of the sequence.  Optionally also b (0 past the
 // end), e^{gamma_t}, e^{gamma_L - gamma_t} and e^{-gamma_t}.  Called by one
 // full warp.
+// The arithmetic of chunk_gamma on the lane's tokens' g (and b) values.
+__device__ __forceinline__ void chunk_gamma_of(float g0, float g1, float b0, float b1, float *gam,
+                                               float *beta_out, float *eg, float *dec,
+                                               float *einv) {
+    const int lane = threadIdx.x & 31;
+    const int t0 = 2 * lane, t1 = 2 * lane + 1;
+    float s = g0 + g1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float x = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += x;
+    }
+    const float ga = s - g1, gb = s;
+    gam[t0] = ga;
+    gam[t1] = gb;
+    beta_out[t0] = b0;
+    beta_out[t1] = b1;
+    const float gL = __shfl_sync(0xffffffffu, s, 31);
+    eg[t0] = expf(ga);
+    eg[t1] = expf(gb);
+    dec[t0] = expf(gL - ga);
+    dec[t1] = expf(gL - gb);
+    einv[t0] = expf(-ga);
+    einv[t1] = expf(-gb);
+}
+
 __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok0, int L, int Hv,
                                             int h, float *gam, float *beta_out,
                                             const float *__restrict__ beta, float *eg = nullptr,
@@ -254,6 +281,12 @@ __device__ __forceinline__ void chunk_gamma(const float *__restrict__ g, int tok
     const int t0 = 2 * lane, t1 = 2 * lane + 1;
     const float g0 = t0 < L ? g[(size_t)(tok0 + t0) * Hv + h] : 0.f;
     const float g1 = t1 < L ? g[(size_t)(tok0 + t1) * Hv + h] : 0.f;
+    if (beta_out && eg && einv) {
+        const float b0 = t0 < L ? beta[(size_t)(tok0 + t0) * Hv + h] : 0.f;
+        const float b1 = t1 < L ? beta[(size_t)(tok0 + t1) * Hv + h] : 0.f;
+        chunk_gamma_of(g0, g1, b0, b1, gam, beta_out, eg, dec, einv);
+        return;
+    }
     float s = g0 + g1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -329,6 +362,21 @@ struct alignas(1024) PrepSmem {
     uint64_t mma_bar;
     uint32_t tmem;
     int fact;       // the chunk's A and P factorise (gamma_L >= kFactorGammaMin)
+};
+
+// What a persistent prep unit keeps beside its PrepSmem so that each item
+// starts without waiting on memory: the second half of W^T's staging (W^T
+// goes to ab and wt_hi, so the K and Q atoms take the next item's tiles as
+// soon as this item's W^T MMA has read them), the next item's g and beta
+// (copied by cp.async during this item, by item parity; 0 past the end), and
+// the items up to two ahead with their chunk-table entries (by the unit's
+// item count mod 4).
+struct alignas(1024) PrepAhead {
+    uint8_t wt_hi[kTile];
+    float gs[2][C];
+    float bs[2][C];
+    int4 loc[4];  // {chunk, value head, first token, length}
+    int idx[4];   // item number, -1 past the last
 };
 
 // Row r of A's fp32 diagonal 16 x 16 block b in ab: 16 floats; blocks 260
@@ -444,19 +492,27 @@ __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
 // One prep unit: kPrepThreads threads with local index `ltid` (the unit's
 // first warp is a multiple of 4, so warp w of the unit reads TMEM lane
 // quadrant w), its own PrepSmem, TMEM columns and named barriers `bar` (the
-// unit) and `bar2` (its warps 2 and 3).  It works through items item0,
-// item0 + stride, ... below n_items (item = chunk * Hv + value head,
-// chunk-major).  With `flags`, each finished item publishes `epoch` into
+// unit) and `bar2` (its warps 2 and 3).  Items are numbered chunk * Hv +
+// value head (chunk-major, chunks in the prep order when `porder` is given),
+// below n_items.  With `flags`, each finished item publishes `epoch` into
 // flags[chunk * Hv + h] (release, device scope) once its workspace slot is
-// written.  kLoop = false: exactly one item, compiled without the loop.
+// written.  kLoop = false: exactly the one item item0, compiled without the
+// loop.
 // `relinquish`: give up the CTA's TMEM allocation permit after allocating
-// (only when the CTA allocates nothing after this unit).
+// (only when the CTA allocates nothing after this unit).  kLoop units also
+// take `ahead` (see PrepAhead) and `ticket`: their first two items are item0
+// and item0 + stride (the grid's first two rounds, in order), the later ones
+// are drawn one at a time from *ticket (item = dyn0 + ticket, in order, while
+// items remain), so that a unit slowed down holds up at most the two items
+// it has drawn.  Each item is drawn two items ahead (the ticket, the prep
+// order and the chunk table read a few phases apart), and its tiles, g and
+// beta are in flight during the item before.
 //
 // Per item:
 //   gamma = cumsum(g), b, e^gamma, e^{gamma_L - gamma};  [K; Q] K^T (M = 128);
 //   diag(e^gamma) Q to the slot;
-//   A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i), i < t: its diagonal 32 x 32
-//     blocks in fp32, its lower-left block E in bf16;
+//   A_ti = b_t e^{gamma_t - gamma_i} (k_t . k_i), i < t: its diagonal 16 x 16
+//     blocks in fp32, the rest below them (E included) in bf16;
 //   P = M o Q K^T, M_ri = e^{gamma_r - gamma_i} (i <= r), to the slot;
 //   D' = blockdiag((I + A_bb)^-1), each 32 x 32 block from its two 16 x 16
 //     diagonal blocks (fp32 forward substitution) and the merge
@@ -472,7 +528,8 @@ __device__ __forceinline__ void prep_unit(
     const int4 *__restrict__ table, uint8_t *__restrict__ slots, float *__restrict__ gl,
     int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int bar2, int item0,
     int stride, int n_items, unsigned *flags, unsigned epoch, bool relinquish,
-    const int *__restrict__ porder = nullptr) {
+    const int *__restrict__ porder = nullptr, PrepAhead *ahead = nullptr,
+    unsigned *ticket = nullptr, int dyn0 = 0) {
     const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
     const int q4 = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of the physical warp
@@ -496,7 +553,17 @@ __device__ __forceinline__ void prep_unit(
         mbar_init(&sm.tma_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        if (item0 < n_items && chunk_of(item0) < n_ch) sm.nxt[0] = locate(item0);
+        if (kLoop) {
+            const int i0 = item0, i1 = item0 + stride;
+            const bool v0 = i0 < n_items && chunk_of(i0) < n_ch;
+            const bool v1 = i1 < n_items && chunk_of(i1) < n_ch;
+            ahead->idx[0] = v0 ? i0 : -1;
+            ahead->idx[1] = v1 ? i1 : -1;
+            if (v0) ahead->loc[0] = locate(i0);
+            if (v1) ahead->loc[1] = locate(i1);
+        } else if (item0 < n_items && chunk_of(item0) < n_ch) {
+            sm.nxt[0] = locate(item0);
+        }
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, kPrepTmemCols);
@@ -512,14 +579,20 @@ __device__ __forceinline__ void prep_unit(
     uint32_t mph = 0, tph = 0;
     int it = 0;
     int4 pend = make_int4(-1, 0, 0, 0);  // (copier) item whose flag is still to publish
+    bool tma_ahead = false;              // (kLoop) this item's tiles were issued by the last one
 #pragma unroll 1
-    for (int item = item0; item < n_items && !bad; item += stride, ++it) {
-        if (chunk_of(item) >= n_ch) break;  // chunk-major: every later item is past the table
-        const int4 cur = sm.nxt[it & 1];
+    for (; !bad; ++it) {
+        if (kLoop ? ahead->idx[it & 3] < 0 : (item0 >= n_items || chunk_of(item0) >= n_ch)) break;
+        const int4 cur = kLoop ? ahead->loc[it & 3] : sm.nxt[0];
         const int ch = cur.x, h = cur.y, tok0 = cur.z, L = cur.w, hk = h / G;
         uint8_t *const slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
-        const bool more = kLoop && item + stride < n_items && chunk_of(item + stride) < n_ch;
-        if (tid == kCopier) {
+        const bool more = kLoop && ahead->idx[(it + 1) & 3] >= 0;
+        // (warp 2, lane 0) the item after next: its number, whether it
+        // exists, its chunk from the prep order and its chunk-table entry
+        int item2 = 0, pch = 0;
+        bool more2 = false;
+        int4 e2 = make_int4(0, 0, 0, 0);
+        if (tid == kCopier && !tma_ahead) {
             if (kLoop) {
                 // The previous item's bulk copies have read the tiles, and
                 // its generic accesses are ordered before the TMA writes.
@@ -533,8 +606,15 @@ __device__ __forceinline__ void prep_unit(
             tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, hk, tok0, &sm.tma_bar);
         }
         if (warp == 1) {
-            // gamma, b and the decay factors while the tiles are in flight.
-            chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec, sm.einv);
+            // gamma, b and the decay factors while the tiles are in flight
+            // (kLoop: from the g and beta copied during the previous item).
+            if (kLoop && it > 0) {
+                const float *gs = ahead->gs[it & 1], *bs = ahead->bs[it & 1];
+                chunk_gamma_of(gs[2 * lane], gs[2 * lane + 1], bs[2 * lane], bs[2 * lane + 1],
+                               sm.gam, sm.beta, sm.eg, sm.dec, sm.einv);
+            } else {
+                chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec, sm.einv);
+            }
             float *slot_f = reinterpret_cast<float *>(slot);
             slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[2 * lane];
             slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[2 * lane + 1];
@@ -547,13 +627,32 @@ __device__ __forceinline__ void prep_unit(
                 sm.fact = sm.gam[C - 1] >= kFactorGammaMin;
             }
         } else if (warp == 2 && more) {
-            // The next item: its table entry, and its inputs into L2.
-            const int4 nx = locate(item + stride);
-            if (lane == 0) sm.nxt[(it + 1) & 1] = nx;
-            prep_prefetch(tm_q, tm_k, g, beta, nx.z, nx.w, Hv, nx.y, nx.y / G);
+            // The next item's g and beta into shared memory; the first load
+            // of the entry of the item after it (used two phases on).
+            const int4 nx = ahead->loc[(it + 1) & 3];
+            float *gs = ahead->gs[(it + 1) & 1], *bs = ahead->bs[(it + 1) & 1];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * lane + u;
+                if (t < nx.w) {
+                    cp_async4(gs + t, g + (size_t)(nx.z + t) * Hv + nx.y);
+                    cp_async4(bs + t, beta + (size_t)(nx.z + t) * Hv + nx.y);
+                } else {
+                    gs[t] = 0.f;
+                    bs[t] = 0.f;
+                }
+            }
+            cp_async_commit();
+            if (it == 0) prep_prefetch(tm_q, tm_k, g, beta, nx.z, nx.w, Hv, nx.y, nx.y / G);
+            if (lane == 0) {
+                item2 = dyn0 + (int)atomicAdd(ticket, 1u);
+                more2 = item2 < n_items && chunk_of(item2) < n_ch;
+            }
         }
         if ((bad = unit_wait(&sm.tma_bar, tph, warp, bar, bad))) break;
         tph ^= 1;
+        tma_ahead = false;
+        if (warp == 2 && lane == 0 && more2) pch = porder ? porder[chunk_of(item2)] : chunk_of(item2);
         if (tid == 0) {
             tc_fence_after();
             const uint32_t base = smem_u32(sm.kq);
@@ -591,6 +690,9 @@ __device__ __forceinline__ void prep_unit(
             }
         }
         fence_proxy_async_smem();
+        // (kLoop: the previous item's W^T copies read ab and wt_hi, which the
+        // next phases write)
+        if (kLoop && tid == kCopier) bulk_wait_group_read<0>();
         named_barrier(bar, kPrepThreads);
         if (tid == kCopier) {
             bulk_store(slot + kSlotQ, sm.kq + kTile, kTile);
@@ -691,6 +793,7 @@ __device__ __forceinline__ void prep_unit(
         // 16-31 x columns 0-15 and 48-63 x columns 32-47 it is C X1 of each
         // 32 x 32 diagonal block (C = its lower-left 16 x 16 block of A); the
         // rest of Y (from A's lower-left 32 x 32 block) is not used.
+        if (warp == 2 && lane == 0 && more2) e2 = table[pch];
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16(64, 64, false, true);
@@ -766,6 +869,19 @@ __device__ __forceinline__ void prep_unit(
         fence_proxy_async_smem();
         tc_fence_before();
         named_barrier(bar, kPrepThreads);
+        if (warp == 2 && more) {
+            // The item after next (or none): recorded, and its inputs into L2.
+            const bool v2 = __shfl_sync(0xffffffffu, more2, 0);
+            const int i2 = __shfl_sync(0xffffffffu, item2, 0);
+            if (v2) {
+                const int4 nx2 = make_int4(__shfl_sync(0xffffffffu, pch, 0), i2 % Hv,
+                                           __shfl_sync(0xffffffffu, e2.y, 0),
+                                           __shfl_sync(0xffffffffu, e2.z, 0));
+                if (lane == 0) ahead->loc[(it + 2) & 3] = nx2;
+                prep_prefetch(tm_q, tm_k, g, beta, nx2.z, nx2.w, Hv, nx2.y, nx2.y / G);
+            }
+            if (lane == 0) ahead->idx[(it + 2) & 3] = v2 ? i2 : -1;
+        }
         // ---- N = D' E  (M = 64, N = 64, K = 64)
         if (tid == 0) {
             tc_fence_after();
@@ -862,22 +978,49 @@ __device__ __forceinline__ void prep_unit(
         if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
         mph ^= 1;
         tc_fence_after();
-        // W^T staged in K atom 0 + Q atom 0 (16 KB, both dead), then copied.
+        if (kLoop && more) {
+            // The W^T MMA has read the K atoms and T diag(b e^gamma); the Q
+            // atoms are dead once T diag(b)'s copy has read Q atom 1: the
+            // next item's tiles go now, beside this item's W^T read-back.
+            if (tid == kCopier) {
+                bulk_wait_group_read<0>();
+                fence_proxy_async_smem();
+                const int4 nx = ahead->loc[(it + 1) & 3];
+                const int nhk = nx.y / G;
+                mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
+                tma_load_3d(sm.kq + 0 * kTile, tm_k, 0, nhk, nx.z, &sm.tma_bar);
+                tma_load_3d(sm.kq + 1 * kTile, tm_q, 0, nhk, nx.z, &sm.tma_bar);
+                tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, nhk, nx.z, &sm.tma_bar);
+                tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, nhk, nx.z, &sm.tma_bar);
+            }
+            tma_ahead = true;
+        }
+        // W^T staged (16 KB), then copied: in K atom 0 + Q atom 0 (both
+        // dead), or (kLoop) in ab (rows 0-63) and wt_hi (rows 64-127).
         {
+            uint8_t *const wt = kLoop ? (row < 64 ? sm.ab : ahead->wt_hi) : sm.kq;
+            const int wr = kLoop ? (row & 63) : row;
             float y[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 tmem_ld32f(tmem + lane_base + 32 * hf, y);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(sm.kq + swz(row, 4 * hf + cc)) = pack8(y + 8 * cc);
+                    *reinterpret_cast<uint4 *>(wt + swz(wr, 4 * hf + cc)) = pack8(y + 8 * cc);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
+        // (the next item's g and beta are in shared memory before it starts)
+        if (kLoop && warp == 2) cp_async_wait_all();
         named_barrier(bar, kPrepThreads);
         if (tid == kCopier) {
-            bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
+            if (kLoop) {
+                bulk_store(slot + kSlotWT, sm.ab, kTile);
+                bulk_store(slot + kSlotWT + kTile, ahead->wt_hi, kTile);
+            } else {
+                bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
+            }
             bulk_commit_group();
             if (kLoop && flags && it == 0) {
                 // The first items gate the start of every recurrence: publish
@@ -896,6 +1039,10 @@ __device__ __forceinline__ void prep_unit(
         bulk_wait_group<0>();  // shared memory must outlive the copies
     }
     if (bad && tid == 0) atomicExch(err, kErrTimeout);
+    // Copies started for an item that will not run (the unit stopped on a
+    // time-out): let them land before the memory is given up.
+    if (kLoop && warp == 2) cp_async_wait_all();
+    if (tma_ahead && warp == 0) warp_wait_poll(&sm.tma_bar, tph, 200000000ll);
     tc_fence_before();
     named_barrier(bar, kPrepThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
@@ -1510,9 +1657,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 constexpr int kFusedThreads = kPrepUnits * kPrepThreads;
 static_assert(kFusedThreads >= kChainThreads, "the recurrence's warps fit the fused CTA");
 constexpr size_t kPrepUnitBytes = sizeof(PrepSmem);  // a multiple of 1024 (alignas)
+// A prep CTA: kPrepUnits PrepSmem, then each unit's PrepAhead.
+constexpr size_t kPrepCtaBytes = kPrepUnits * (kPrepUnitBytes + sizeof(PrepAhead));
 constexpr size_t kFusedSmemBytes =
-    (sizeof(ChainSmem) > kPrepUnits * kPrepUnitBytes ? sizeof(ChainSmem)
-                                                     : kPrepUnits * kPrepUnitBytes) + 1024;
+    (sizeof(ChainSmem) > kPrepCtaBytes ? sizeof(ChainSmem) : kPrepCtaBytes) + 1024;
 static_assert(kFusedSmemBytes <= 232448, "fused kernel shared memory");
 static_assert(kPrepUnits * kPrepTmemCols <= 512, "prep units' TMEM");
 static_assert(1 + 2 * kPrepUnits <= 16, "prep units' named barriers");
@@ -1564,12 +1712,17 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             s_first = s;
         }
         __syncthreads();
-        const int pcta = blockIdx.x - n_chain, ncta = gridDim.x - n_chain;
+        // The units' first two rounds in order, then items drawn from the
+        // ticket after the flags, in the prep order.
+        const int pcta = blockIdx.x - n_chain, n_units = kPrepUnits * (gridDim.x - n_chain);
         prep_unit<true>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q, &tm_k, g,
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                         threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u,
-                        s_first * Hv + kPrepUnits * pcta + u, kPrepUnits * ncta, n_items, flags,
-                        1u, false, porder);
+                        s_first * Hv + kPrepUnits * pcta + u, n_units, n_items, flags, 1u, false,
+                        porder,
+                        reinterpret_cast<PrepAhead *>(base + kPrepUnits * kPrepUnitBytes +
+                                                      u * sizeof(PrepAhead)),
+                        flags + n_items, s_first * Hv + 2 * n_units);
     }
 }
 
@@ -1864,15 +2017,15 @@ bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void 
            encode_thd(&m.to, out, p.total_tokens, p.num_v_heads);
 }
 
-// The chunk table kernel (with `zero_flags`, it also clears the ready flags of
-// the fused kernel).
+// The chunk table kernel (with `zero_flags`, it also clears the ready flags and
+// the prep ticket of the fused kernel).
 gdn_status launch_table(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
                         const int32_t *cu, int snap_stride, bool zero_flags, cudaStream_t stream,
                         const Timing *tm) {
     time_mark(tm, 0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(
         cu, p.num_seqs, p.total_tokens, w.max_chunks, snap_stride, t.err, t.chunk_off, t.snap_off,
-        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_v_heads) : 0,
+        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_v_heads) + 1 : 0,
         zero_flags ? t.porder : nullptr);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     time_mark(tm, 1, stream);
