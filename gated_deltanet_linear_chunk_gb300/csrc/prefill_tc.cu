@@ -542,7 +542,7 @@ __device__ __forceinline__ void prep_unit(
     // Chunk-table entry of an item: {chunk, value head, first token, length}.
     auto locate = [&](int item) {
         const int ci = chunk_of(item);
-        const int ch = (kLoop && porder) ? porder[ci] : ci;
+        const int ch = porder ? porder[ci] : ci;
         const int4 e = table[ch];
         return make_int4(ch, item % Hv, e.y, e.z);
     };
@@ -1022,7 +1022,7 @@ __device__ __forceinline__ void prep_unit(
                 bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
             }
             bulk_commit_group();
-            if (kLoop && flags && it == 0) {
+            if (flags && it == 0) {
                 // The first items gate the start of every recurrence: publish
                 // at once.  Later ones are published behind the next item's
                 // loads and copies, when their own copies have long finished.
@@ -1655,6 +1655,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // (cooperative launch), so every wait ends.  Prep runs on the SMs the
 // recurrence leaves idle, during the recurrence instead of before it.
 constexpr int kFusedThreads = kPrepUnits * kPrepThreads;
+constexpr int kLocalChunks = kPrepUnits;  // chunks each recurrence preps itself (one round)
 static_assert(kFusedThreads >= kChainThreads, "the recurrence's warps fit the fused CTA");
 constexpr size_t kPrepUnitBytes = sizeof(PrepSmem);  // a multiple of 1024 (alignas)
 // A prep CTA: kPrepUnits PrepSmem, then each unit's PrepAhead.
@@ -1681,15 +1682,19 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     griddep_wait();  // (a programmatic dependent of the chunk table kernel)
     const int u = threadIdx.x / kPrepThreads;
     if ((int)blockIdx.x < n_chain) {
-        // The recurrence's first kPrepUnits chunks are prepped here, one per
-        // unit, before it starts (the prep CTAs begin with the chunks after
-        // them): the recurrence then waits for its own first chunks only,
-        // not for the first round of every prep unit of the grid.
+        // The recurrence's first kLocalChunks chunks are prepped here, one
+        // per unit, before it starts (the prep CTAs begin with the chunks
+        // after them): the recurrence then waits for its own first chunks
+        // only, not for the first round of every prep unit of the grid.  (Two
+        // rounds here avoid the wait for that round, whose items run twice as
+        // long as later ones, but start the recurrence later and slow its
+        // steps while more prep runs beside them: slower at 4000 tokens.)
         const int n = order[blockIdx.x / Hv], h = blockIdx.x % Hv;
         const int c_begin = chunk_off[n];
-        const int n_local = min(chunk_off[n + 1] - c_begin, kPrepUnits);
-        if (u < n_local) {
-            const int item = (c_begin + u) * Hv + h;
+        const int n_local = min(chunk_off[n + 1] - c_begin, kLocalChunks);
+#pragma unroll 1
+        for (int c = u; c < n_local; c += kPrepUnits) {
+            const int item = (c_begin + c) * Hv + h;
             prep_unit<false>(*reinterpret_cast<PrepSmem *>(base + u * kPrepUnitBytes), &tm_q,
                              &tm_k, g, beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                              threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u, item, 1,
@@ -1703,12 +1708,12 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             flags, n_local);
     } else {
         // Skip what the recurrences prep themselves: in the prep order (by
-        // position in the sequence) the first sum_n min(chunks_n, kPrepUnits)
+        // position in the sequence) the first sum_n min(chunks_n, kLocalChunks)
         // chunks.
         __shared__ int s_first;
         if (threadIdx.x == 0) {
             int s = 0;
-            for (int m = 0; m < N; ++m) s += min(chunk_off[m + 1] - chunk_off[m], kPrepUnits);
+            for (int m = 0; m < N; ++m) s += min(chunk_off[m + 1] - chunk_off[m], kLocalChunks);
             s_first = s;
         }
         __syncthreads();
