@@ -46,6 +46,7 @@ GDN_ERR_MISALIGNED = 3
 GDN_ERR_WORKSPACE = 4
 GDN_ERR_CUDA = 5
 GDN_ERR_TIMEOUT = 6
+GDN_ERR_INTERNAL = 7  # a device-side index check of a GDN_DEBUG build failed
 _DTYPES = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
 
 
@@ -79,7 +80,25 @@ def library() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.library_path()
+    _lib = _load(_build.library_path())
+    return _lib
+
+
+_debug_lib = None
+
+
+def debug_library() -> ctypes.CDLL:
+    """The GDN_DEBUG variant of the library (the same C ABI; the kernels also
+    check the inputs' preconditions and their own indices on the device and
+    report through gdn_chunk_prefill_device_status).  The wrappers of this
+    module call library(); this one is called through its C ABI directly."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _load(_build.library_path(debug=True))
+    return _debug_lib
+
+
+def _load(path: str) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise RuntimeError(
             f"the CUDA library {path} is missing: build it first "
@@ -124,7 +143,6 @@ def library() -> ctypes.CDLL:
     lib.gdn_chunk_prefill_host.argtypes = [PP, ctypes.c_int32] + [P] * 16 + [P]
     lib.gdn_prefill_fused_mode.restype = ctypes.c_int32
     lib.gdn_prefill_fused_mode.argtypes = [ctypes.c_int32]
-    _lib = lib
     return lib
 
 

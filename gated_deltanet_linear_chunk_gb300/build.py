@@ -2,7 +2,9 @@
 
 Each .cu under csrc/ compiles to an object in parallel; the objects link into
 one shared library with the CUDA runtime linked statically, so the library
-loads on a machine without a GPU (only the C ABI symbols are exported).
+loads on a machine without a GPU (only the C ABI symbols are exported).  A
+second variant, libgdn_debug, is built with GDN_DEBUG: the same kernels plus
+device-side checks of the inputs' preconditions and of the kernels' indices.
 """
 from __future__ import annotations
 
@@ -23,8 +25,11 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibilit
               "-Xptxas", "-warn-spills", "--expt-relaxed-constexpr"]
 
 
-def library_path() -> str:
-    return os.path.join(BUILD, f"libgdn_{platform.machine()}.so")
+def library_path(debug: bool = False) -> str:
+    """The release library, or with `debug` the GDN_DEBUG one (device-side
+    checks of the inputs' preconditions and of the kernels' indices)."""
+    name = "libgdn_debug" if debug else "libgdn"
+    return os.path.join(BUILD, f"{name}_{platform.machine()}.so")
 
 
 def _nvcc() -> str:
@@ -43,38 +48,55 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source and link libgdn; returns the library path."""
-    out = library_path()
-    if not force and os.path.exists(out):
-        newest = max(os.path.getmtime(p) for p in _deps())
-        if os.path.getmtime(out) >= newest:
-            return out
-    os.makedirs(BUILD, exist_ok=True)
-    nvcc = _nvcc()
-    objs = []
+def _stale(out: str) -> bool:
+    if not os.path.exists(out):
+        return True
+    newest = max(os.path.getmtime(p) for p in _deps())
+    return os.path.getmtime(out) < newest
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + f".{platform.machine()}.o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC,
-               "-c", src, "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
-        if verbose and r.stderr:
-            print(r.stderr)
-        return obj
 
-    srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, srcs))
-    tmp = out + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, out)
-    return out
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug=None) -> str:
+    """Compile every CUDA source and link the library: debug=None builds the
+    release and the GDN_DEBUG variants (their sources compiled in one
+    parallel pool), True or False one of them.  Returns the path of the
+    release library (or of the one variant asked for)."""
+    variants = [False, True] if debug is None else [bool(debug)]
+    todo = [v for v in variants if force or _stale(library_path(v))]
+    if todo:
+        nvcc = _nvcc()
+        srcs = _sources()
+
+        def obj_dir(dbg):
+            return os.path.join(BUILD, "debug") if dbg else BUILD
+
+        def compile_one(job):
+            dbg, src = job
+            obj = os.path.join(obj_dir(dbg), os.path.basename(src) + f".{platform.machine()}.o")
+            flags = [*NVCC_FLAGS, *extra_flags] + (["-DGDN_DEBUG"] if dbg else [])
+            cmd = [nvcc, *ARCH, *flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
+            if verbose and r.stderr:
+                print(r.stderr)
+            return obj
+
+        for dbg in todo:
+            os.makedirs(obj_dir(dbg), exist_ok=True)
+        jobs = [(dbg, src) for dbg in todo for src in srcs]
+        with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+            objs = list(ex.map(compile_one, jobs))
+        for dbg in todo:
+            out = library_path(dbg)
+            mine = [o for (d, _), o in zip(jobs, objs) if d == dbg]
+            tmp = out + ".tmp"
+            cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-Xcompiler", "-fPIC", *mine,
+                   "-o", tmp]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stderr}")
+            os.replace(tmp, out)
+    return library_path(False if debug is None else bool(debug))
 
 
 if __name__ == "__main__":

@@ -80,12 +80,22 @@ gdn_status prefill_impl(const gdn_problem *problem, const void *q, const void *k
         if (!aligned16(p.workspace)) return GDN_ERR_WORKSPACE;
     }
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    if (scan_group > 0)
-        return launch_prefill_scan(p, scan_group, q, k, v, g, beta, cu_seqlens, initial_state, out,
-                                   final_state, st_);
-    if (prefill_tc_supported(p))
-        return launch_prefill_tc(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
-                                 snaps, snap_stride, st_, events, fused);
+    if (scan_group > 0) {
+        gdn_status st = launch_prefill_scan(p, scan_group, q, k, v, g, beta, cu_seqlens,
+                                            initial_state, out, final_state, st_);
+        if (kDebug && st == GDN_OK && p.total_tokens > 0)
+            st = launch_debug_input_checks(p, q, k, g, beta, static_cast<int *>(p.workspace), st_);
+        return st;
+    }
+    if (prefill_tc_supported(p)) {
+        gdn_status st = launch_prefill_tc(p, q, k, v, g, beta, cu_seqlens, initial_state, out,
+                                          final_state, snaps, snap_stride, st_, events, fused);
+        // (debug builds: the inputs' preconditions, after the call's kernels
+        // so that its first kernel's reset of the error word comes before)
+        if (kDebug && st == GDN_OK && p.total_tokens > 0)
+            st = launch_debug_input_checks(p, q, k, g, beta, static_cast<int *>(p.workspace), st_);
+        return st;
+    }
     return launch_prefill_simt(p, q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
                                st_);
 }
@@ -205,6 +215,8 @@ GDN_API gdn_status gdn_chunk_prefill_device_status(const void *workspace,
         case gdn::kErrNone: return GDN_OK;
         case gdn::kErrCuSeqlens: return GDN_ERR_INVALID_ARG;
         case gdn::kErrTimeout: return GDN_ERR_TIMEOUT;
+        case gdn::kErrInputs: return GDN_ERR_INVALID_ARG;
+        case gdn::kErrIndex: return GDN_ERR_INTERNAL;
     }
     return GDN_ERR_CUDA;
 }
@@ -274,6 +286,8 @@ GDN_API const char *gdn_status_string(gdn_status status) {
         case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA launch or runtime error";
         case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+        case GDN_ERR_INTERNAL:
+            return "GDN_ERR_INTERNAL: a device-side index check of a debug build failed";
     }
     return "GDN_ERR_UNKNOWN";
 }

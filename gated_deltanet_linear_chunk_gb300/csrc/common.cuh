@@ -29,8 +29,30 @@ __device__ __forceinline__ float warp_sum(float x) {
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Error word at offset 0 of the tensor-core prefill's workspace, written by
-// its kernels (reset by the first kernel of every call).
-enum DeviceError : int { kErrNone = 0, kErrCuSeqlens = 1, kErrTimeout = 2 };
+// its kernels (reset by the first kernel of every call).  The last two only
+// by GDN_DEBUG builds: kErrInputs for inputs outside the documented
+// preconditions, kErrIndex for a failed internal index check (a bug).
+enum DeviceError : int {
+    kErrNone = 0,
+    kErrCuSeqlens = 1,
+    kErrTimeout = 2,
+    kErrInputs = 3,
+    kErrIndex = 4
+};
+
+// GDN_DEBUG builds check, on the device, the inputs' documented
+// preconditions and the kernels' table-derived indices: a failed check
+// records its code in the error word (the first one wins) and the access it
+// guards is skipped; nothing traps.
+#ifdef GDN_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+
+__device__ __forceinline__ void debug_fail(int *err, int code) {
+    if (err) atomicCAS(err, (int)kErrNone, code);
+}
 
 // Launch helpers return a gdn_status for the last launch on this thread.
 inline gdn_status launch_status() {
@@ -51,6 +73,13 @@ gdn_status launch_prefill_simt(const gdn_problem &p, const void *q, const void *
                                const void *v, const float *g, const float *beta,
                                const int32_t *cu_seqlens, const float *h0, void *out,
                                float *hT, cudaStream_t stream);
+
+// GDN_DEBUG builds: checks of a prefill's inputs on `stream` (g <= 0, beta in
+// [0, 1], unit-norm q and k rows; all finite), kErrInputs into *err on a
+// failure.
+gdn_status launch_debug_input_checks(const gdn_problem &p, const void *q, const void *k,
+                                     const float *g, const float *beta, int *err,
+                                     cudaStream_t stream);
 
 // Device address of the no-alloc entry point's built-in scratch on the
 // current device (nullptr if it cannot be looked up).

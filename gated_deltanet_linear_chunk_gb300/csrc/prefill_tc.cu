@@ -585,6 +585,11 @@ __device__ __forceinline__ void prep_unit(
         if (kLoop ? ahead->idx[it & 3] < 0 : (item0 >= n_items || chunk_of(item0) >= n_ch)) break;
         const int4 cur = kLoop ? ahead->loc[it & 3] : sm.nxt[0];
         const int ch = cur.x, h = cur.y, tok0 = cur.z, L = cur.w, hk = h / G;
+        if (kDebug && !(ch >= 0 && ch < n_ch && h >= 0 && h < Hv && tok0 >= 0 && L >= 1 && L <= C)) {
+            if (tid == 0) debug_fail(err, kErrIndex);  // (then the unit stops, as on a time-out)
+            bad = true;
+            break;
+        }
         uint8_t *const slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
         const bool more = kLoop && ahead->idx[(it + 1) & 3] >= 0;
         // (warp 2, lane 0) the item after next: its number, whether it
@@ -1038,7 +1043,7 @@ __device__ __forceinline__ void prep_unit(
             publish_item<0>(flags + (size_t)pend.x * Hv + pend.y, epoch);
         bulk_wait_group<0>();  // shared memory must outlive the copies
     }
-    if (bad && tid == 0) atomicExch(err, kErrTimeout);
+    if (bad && tid == 0) atomicCAS(err, (int)kErrNone, (int)kErrTimeout);  // (the first error stays)
     // Copies started for an item that will not run (the unit stopped on a
     // time-out): let them land before the memory is given up.
     if (kLoop && warp == 2) cp_async_wait_all();
@@ -1304,6 +1309,17 @@ __device__ __forceinline__ void chain_role(
                 if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
                 const int tok0 = seq_tok0 + C * c;
+                if (kDebug) {
+                    // The chunk's table entry agrees with the sequence's.
+                    const int4 te = table[ch];
+                    if (!(ch < chunk_off[N] && te.y == tok0 && te.z >= 1 && te.z <= C)) {
+                        if (lane == 0) {
+                            debug_fail(err, kErrIndex);
+                            sm.abort = 1;
+                        }
+                        break;
+                    }
+                }
                 ChainStage &st = sm.st[s];
                 uint64_t *bar = &sm.full[s];
                 const uint8_t *slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
@@ -1612,7 +1628,7 @@ if (elect_one_sync()) {
     __syncthreads();
     if (sm.abort) {
         if (tid == 0) {
-            atomicExch(err, kErrTimeout);
+            atomicCAS(err, (int)kErrNone, (int)kErrTimeout);  // (the first error stays)
             // Let loads still in flight land before the CTA leaves.
             for (int c = max(0, sm.issued - 2); c < sm.issued; ++c)
                 mbar_wait(&sm.full[c & 1], (c >> 1) & 1, 200000000ll);

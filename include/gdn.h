@@ -68,8 +68,10 @@ typedef enum {
     GDN_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned       */
     GDN_ERR_WORKSPACE = 4,    /* workspace missing, too small or misaligned    */
     GDN_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed          */
-    GDN_ERR_TIMEOUT = 6       /* a bounded wait inside a kernel ran out
+    GDN_ERR_TIMEOUT = 6,      /* a bounded wait inside a kernel ran out
                                  (reported by gdn_chunk_prefill_device_status) */
+    GDN_ERR_INTERNAL = 7      /* a device-side index check of a GDN_DEBUG build
+                                 failed (reported likewise; a library bug) */
 } gdn_status;
 
 typedef enum {
@@ -359,6 +361,13 @@ GDN_API gdn_status gdn_chunk_prefill_noalloc(const gdn_problem *problem,
  *   GDN_ERR_TIMEOUT    a bounded wait inside a kernel ran out (each wait
  *                      gives up after about two seconds); outputs incomplete
  *   GDN_ERR_CUDA       the stream reports an error, or the read failed
+ * Builds with GDN_DEBUG (the libgdn_debug variant) also check on the device,
+ * after the call's kernels, the inputs' documented preconditions (g finite
+ * and <= 0, beta in [0, 1], q and k rows of unit L2 norm within 1e-2) and
+ * report a violation as GDN_ERR_INVALID_ARG (the outputs are computed all
+ * the same), and they check the kernels' table-derived indices: a failure
+ * is GDN_ERR_INTERNAL (a library bug; the access is skipped and the call's
+ * outputs are incomplete).  The first condition recorded is the one reported.
  * workspace: problem->workspace of that gdn_chunk_prefill call, or NULL for
  * the built-in scratch of gdn_chunk_prefill_noalloc on the current device.
  * Meaningless after calls that need no workspace (fp32 inputs, d = 64).

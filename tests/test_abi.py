@@ -43,8 +43,15 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"{name} not exported"
 
 
+def test_debug_library_exports_the_same_entry_points(lib):
+    dbg = gdn.debug_library()
+    assert dbg._name != lib._name
+    for name in declared_symbols():
+        assert hasattr(dbg, name), f"{name} not exported by the debug build"
+
+
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = gdn.gdn_status_string(code)
         assert s.startswith("GDN_")
     assert "UNKNOWN" in gdn.gdn_status_string(99)
