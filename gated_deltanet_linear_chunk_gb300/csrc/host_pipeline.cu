@@ -1,10 +1,10 @@
 // host_pipeline.cu -- gdn_chunk_prefill_host: one sequence's prefill from
 // host memory, with the transfers overlapped with the computation.
 //
-// The sequence is cut into pieces of whole 64-token chunks.  Piece p's
-// inputs go up on an upload stream while piece p - 1 is computed on the
-// caller's stream.  Its output comes back on a download stream while piece
-// p + 1 is computed.  The pieces are chained through a device state buffer
+// The sequence is cut into pieces of whole 64-token chunks, the last two
+// smaller than the others.  Piece p's inputs go up on an upload stream while
+// piece p - 1 is computed on the caller's stream.  Its output comes back on
+// a download stream while piece p + 1 is computed.  The pieces are chained through a device state buffer
 // (each piece's final state is the next one's initial state), which is
 // exactly the whole prefill, because chunks restart at every 64 tokens.
 // Besides the prefill kernels this issues only cudaMemcpyAsync,
@@ -104,12 +104,32 @@ GDN_API gdn_status gdn_chunk_prefill_host(
     std::lock_guard<std::mutex> lock(pp.mu);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
-    // Piece boundaries at whole chunks.
+    // Piece boundaries at whole chunks: equal shares, except that the last
+    // two pieces (of three or more; the last of two) get a half and a
+    // quarter of a share.  What is left after the last upload (that piece's
+    // computation and download) is then short, and the link, which carries
+    // the other pieces' downloads beside the uploads, stays busy.  Every
+    // piece gets at least one chunk.
     const int64_t chunks = (T + 63) / 64;
     if (pieces > chunks) pieces = (int32_t)(chunks > 0 ? chunks : 1);
     int64_t bnd[kMaxPieces + 1];
     PieceLens lens;
-    for (int i = 0; i <= pieces; ++i) bnd[i] = std::min<int64_t>(T, 64 * ((chunks * i) / pieces));
+    {
+        int64_t w[kMaxPieces], total = 0;
+        for (int i = 0; i < pieces; ++i)
+            w[i] = pieces >= 3 ? (i < pieces - 2 ? 4 : i == pieces - 2 ? 2 : 1)
+                               : (pieces == 2 ? (i == 0 ? 2 : 1) : 1);
+        for (int i = 0; i < pieces; ++i) total += w[i];
+        int64_t acc = 0, c_prev = 0;
+        bnd[0] = 0;
+        for (int i = 1; i <= pieces; ++i) {
+            acc += w[i - 1];
+            const int64_t c = std::min<int64_t>(std::max<int64_t>((chunks * acc) / total, c_prev + 1),
+                                                chunks - (pieces - i));
+            bnd[i] = std::min<int64_t>(T, 64 * c);
+            c_prev = c;
+        }
+    }
     for (int i = 0; i < pieces; ++i) lens.len[i] = (int32_t)(bnd[i + 1] - bnd[i]);
 
     // The state chain starts from the initial state (or zero).

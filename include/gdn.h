@@ -149,7 +149,11 @@ GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
  *
  * The sequence is cut into `pieces` pieces of whole 64-token chunks; the
  * output is that of one gdn_chunk_prefill, because chunks restart every 64
- * tokens and each piece starts from the previous piece's state.  Piece p's
+ * tokens and each piece starts from the previous piece's state.  The pieces
+ * take equal shares of the chunks, except the last two (of three or more),
+ * which take a half and a quarter of a share (of two pieces, the second
+ * takes half the first's), so that little computation and download is left
+ * once the last upload ends; every piece has at least one chunk.  Piece p's
  * inputs are copied up on an upload stream while piece p - 1 is computed on
  * `stream`, and its output is copied back on a download stream while piece
  * p + 1 is computed.  Overlapping the link's two directions with the
