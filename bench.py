@@ -35,6 +35,9 @@ L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
 WORKLOAD = ("GDN prefill, 1 sequence, T=4000, 16 key / 48 value heads, d_k=d_v=128, "
             "bf16 q/k/v, fp32 g/beta/state, zero initial state")
 L2_NOTE = "flushed before every step (512 MB write)"
+PREFILL_PATHS = ("separate prep and recurrence kernels",
+                 "fused: one recurrence per (sequence, value head) beside prep",
+                 "fused: one recurrence per value head over all sequences, beside prep")
 E2E_PIECES = 4                      # pieces of the end-to-end host-input prefill
 # The other two full-size prefill workloads, timed beside the headline one.
 EXTRA_PREFILLS = {
@@ -478,8 +481,12 @@ def run_ours(args, rank, world, local):
         xargs = (px.q, px.k, px.v, px.g, px.beta, px.cu_seqlens, px.initial_state)
         x_us = median_us(lambda: gdn.gdn_chunk_prefill(*xargs, out=xout, final_state=xfin),
                          n=10)
+        # which kernels the call runs (the timed entry point reports it)
+        _, _, xf, _ = gdn.gdn_chunk_prefill_timed(*xargs, out=xout, final_state=xfin)
+        torch.cuda.synchronize()
         xflops = flops_of(Tx, P["Hv"])
         extra[name] = {"workload": cfg["workload"], "us_per_call": x_us,
+                       "path": PREFILL_PATHS[int(xf)],
                        "tokens_per_s_per_layer": Tx / (x_us / 1e6),
                        "tflops": xflops / (x_us / 1e6) / 1e12,
                        "frac_of_bf16_peak": xflops / (x_us / 1e6) / 1e12 / peak_tf,
@@ -648,6 +655,46 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """--prefill-case: one packed prefill batch alone (16 key / 48 value heads,
+    d = 128, bf16, initial states, the bench's input recipe drawn on the
+    device), `warmup` calls then `steps` timed calls with the L2 flushed before
+    each.  For profiling a prefill path on a case small enough to capture;
+    prints one JSON line (not the bench's result line)."""
+    import torch
+    import gated_deltanet_linear_chunk_gb300 as gdn
+    from gated_deltanet_linear_chunk_gb300 import inputs
+    dev = torch.device("cuda")
+    lens = [int(x) for x in args.prefill_case.split(",")]
+    gdn.gdn_prefill_fused_mode(args.fused_mode)
+    P = PREFILL
+    p = inputs.prefill_inputs_on_device(lens, P["Hk"], P["Hv"], P["d"], P["d"], dev, seed=0,
+                                        initial_state_std=0.02)
+    T = sum(lens)
+    out = torch.empty((T, P["Hv"], P["d"]), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty_like(p.initial_state)
+    xargs = (p.q, p.k, p.v, p.g, p.beta, p.cu_seqlens, p.initial_state)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        gdn.gdn_chunk_prefill(*xargs, out=out, final_state=fin)
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gdn.gdn_chunk_prefill(*xargs, out=out, final_state=fin)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    _, _, f, _ = gdn.gdn_chunk_prefill_timed(*xargs, out=out, final_state=fin)
+    torch.cuda.synchronize()
+    us = statistics.median(ts)
+    print(json.dumps({"prefill_case": lens, "tokens": T, "us_per_call": us,
+                      "tokens_per_s_per_layer": T / (us / 1e6), "path": PREFILL_PATHS[int(f)],
+                      "steps": args.steps, "warmup": args.warmup}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,7 +708,13 @@ def main(argv=None):
                     help="when the prefill uses its fused prep + recurrence kernel "
                          "(gdn_prefill_fused_mode: 0 never, 1 whenever it fits, "
                          "2 by the library's cost model, its default)")
+    ap.add_argument("--prefill-case", default=None, metavar="LENS",
+                    help="time one packed prefill batch alone (comma-separated sequence "
+                         "lengths, 16/48 heads) instead of the bench, for profiling")
     args = ap.parse_args(argv)
+    if args.prefill_case:
+        run_case(args)
+        return
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank)

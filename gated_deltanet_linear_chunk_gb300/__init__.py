@@ -403,7 +403,7 @@ def _prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, outp
                                              ctypes.addressof(fused), st.cuda_stream)
             if rc != 0:
                 raise GDNError(rc, "gdn_chunk_prefill_timed")
-            return out, final_state, bool(fused.value)
+            return out, final_state, int(fused.value)
         if snapshots is _NO_SNAPSHOTS:
             rc = lib.gdn_chunk_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                        _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state),

@@ -199,7 +199,8 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
     __syncthreads();
     if (s_bad) {
         for (int n = tid; n < N; n += 1024) chunk_off[n] = 0;
-        for (int n = tid; n < N; n += 1024) order[n] = n;
+        if (order)
+            for (int n = tid; n < N; n += 1024) order[n] = n;
         return;
     }
     // Chunk offsets of this call (block-visible: shared memory, or the
@@ -227,7 +228,7 @@ gdn_chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int64_t
             porder[rank] = ch;
         }
     }
-    for (int n = tid; n < N; n += 1024) {
+    for (int n = tid; order && n < N; n += 1024) {
         if (N > kMaxSortSeqs) {
             order[n] = n;
             continue;
@@ -1212,7 +1213,12 @@ __device__ __noinline__ bool store_state_rows(ChainSmem &sm, const CUtensorMap *
 // idle.  kFused: inside the persistent kernel that also runs prep (below):
 // the loads of chunk c wait for its ready flag, and the chunk decay comes
 // from the stage instead of the workspace.
-template <bool kSnaps, bool kLinear, bool kNoOut, int kS0, bool kFused>
+// kMulti (fused kernel only): the CTA runs value head h = bid over every
+// sequence in turn, as one stream of chunks 0 .. chunk_off[N] - 1 (the
+// recurrence restarts from each sequence's initial state at its first chunk
+// and stores its final state after its last).  Otherwise: one (sequence,
+// value head) recurrence, order[bid / Hv] and bid % Hv.
+template <bool kSnaps, bool kLinear, bool kNoOut, int kS0, bool kFused, bool kMulti = false>
 __device__ __forceinline__ void chain_role(
     ChainSmem &sm, int bid, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
     const CUtensorMap *tm_o, const CUtensorMap *tm_s, const int *__restrict__ chunk_off,
@@ -1223,16 +1229,37 @@ __device__ __forceinline__ void chain_role(
     int *__restrict__ err, int N, int Hk, int Hv, const unsigned *__restrict__ flags,
     int c_flagged = 0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    static_assert(!kMulti || (kFused && !kSnaps && !kLinear && !kNoOut), "kMulti: fused only");
     griddep_wait();  // a programmatic dependent of prep: wait for its slots
-    const int n = order[bid / Hv], h = bid % Hv;
+    const int n = kMulti ? 0 : order[bid / Hv], h = kMulti ? bid : bid % Hv;
     const int hk = h / (Hv / Hk);
-    const int c_begin = chunk_off[n], nc = chunk_off[n + 1] - c_begin;
-    const size_t state_off = ((size_t)n * Hv + h) * D * D;
+    const int c_begin = kMulti ? 0 : chunk_off[n];
+    const int nc = kMulti ? chunk_off[N] : chunk_off[n + 1] - c_begin;
+    const size_t state_off = ((size_t)n * Hv + h) * D * D;  // (kMulti: per sequence)
+    const int n_thr = kFused ? (int)blockDim.x : kChainThreads;
+    // kMulti: final state = initial state for every empty sequence of head h
+    // (one warp per sequence).
+    auto copy_empty_states = [&]() {
+        if (!hT || (chunk_off[N] == 0 && *err != kErrNone)) return;
+        for (int m = warp; m < N; m += n_thr / 32) {
+            if (chunk_off[m + 1] != chunk_off[m]) continue;
+            const size_t off = ((size_t)m * Hv + h) * D * D;
+            for (int i = lane; i < D * D / 4; i += 32) {
+                const float4 x = h0 ? reinterpret_cast<const float4 *>(h0 + off)[i]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(hT + off)[i] = x;
+            }
+        }
+    };
     // Epilogue warps: TMEM quadrant q, state or output row j.
     const int q = warp & 3;
     const int j = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 
+    if (kMulti && nc == 0) {
+        copy_empty_states();
+        return;
+    }
     if (nc == 0) {
         // Empty sequence (or a rejected chunk table): final state = initial state.
         if (hT && !(chunk_off[N] == 0 && *err != kErrNone)) {
@@ -1288,7 +1315,7 @@ __device__ __forceinline__ void chain_role(
             auto prefetch = [&](int c) {
                 if (lane != 0) return;
                 const int ch = c_begin + c;
-                const int tok0 = seq_tok0 + C * c;
+                const int tok0 = kMulti ? table[ch].y : seq_tok0 + C * c;
                 tma_prefetch_3d(tm_k, 0, hk, tok0);
                 tma_prefetch_3d(tm_k, 64, hk, tok0);
                 tma_prefetch_3d(tm_v, 0, h, tok0);
@@ -1308,11 +1335,12 @@ __device__ __forceinline__ void chain_role(
                     break;
                 if (c >= 2 && !warp_wait_lean(&sm.empty[s], ((c >> 1) + 1) & 1, &sm.abort)) break;
                 const int ch = c_begin + c;
-                const int tok0 = seq_tok0 + C * c;
+                const int tok0 = kMulti ? table[ch].y : seq_tok0 + C * c;
                 if (kDebug) {
                     // The chunk's table entry agrees with the sequence's.
                     const int4 te = table[ch];
-                    if (!(ch < chunk_off[N] && te.y == tok0 && te.z >= 1 && te.z <= C)) {
+                    if (!(ch < chunk_off[N] && te.y == tok0 && te.z >= 1 && te.z <= C &&
+                          te.x >= 0 && te.x < N && (kMulti || te.x == n))) {
                         if (lane == 0) {
                             debug_fail(err, kErrIndex);
                             sm.abort = 1;
@@ -1460,12 +1488,14 @@ if (elect_one_sync()) {
         bool ok = true;
         // Snapshot countdown and plane (no division in the loop).
         int snap_left = snap_stride, snap_z = kSnaps ? snap_off[n] * Hv + h : 0;
+        // (kMulti) the state's sequence: its initial and final state plane
+        size_t st_off = kMulti ? ((size_t)table[c_begin].x * Hv + h) * D * D : state_off;
         {
             float x[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
                 float4 v4 = h0 ? *reinterpret_cast<const float4 *>(
-                                     h0 + state_off + (size_t)j * D + 64 * h2 + c)
+                                     h0 + st_off + (size_t)j * D + 64 * h2 + c)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
                 if (kLinear) {
                     const int k0 = 64 * h2 + c;
@@ -1480,6 +1510,10 @@ if (elect_one_sync()) {
         }
         #pragma unroll 1
         for (int c = 0; ok && c < nc; ++c) {
+            // (kMulti) the next chunk's entry: a sequence starts there when it
+            // is that sequence's chunk 0 (read now, used after two waits)
+            const int4 te_next = (kMulti && c + 1 < nc) ? table[c_begin + c + 1]
+                                                         : make_int4(0, 0, 0, 1);
             const float *dec = sm.st[c & 1].egdec + C;
             // e^{gamma_L} of chunk c (in the fused kernel from the stage, which
             // holds e^{gamma_t} with gamma constant past the chunk's end)
@@ -1535,14 +1569,32 @@ if (elect_one_sync()) {
             {
                 float x[64];
                 tmem_ld64(t_s, x);
-                if (c == nc - 1) {
+                if (c == nc - 1 || te_next.w == 0) {
                     if (hT) {
-                        float *dst = hT + state_off + (size_t)j * D + 64 * h2;
+                        float *dst = hT + st_off + (size_t)j * D + 64 * h2;
 #pragma unroll
                         for (int i = 0; i < 64; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) =
                                 make_float4(sigma * x[i], sigma * x[i + 1], sigma * x[i + 2],
                                             sigma * x[i + 3]);
+                    }
+                    if (kMulti && c + 1 < nc) {
+                        // The next sequence starts from its own initial state
+                        // (in place of the hand-off; S^ and this parity's -S0
+                        // are free as they are for the hand-off).
+                        st_off = ((size_t)te_next.x * Hv + h) * D * D;
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4) {
+                            const float4 v4 = h0 ? *reinterpret_cast<const float4 *>(
+                                                       h0 + st_off + (size_t)j * D + 64 * h2 + i)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                            x[i] = v4.x; x[i + 1] = v4.y; x[i + 2] = v4.z; x[i + 3] = v4.w;
+                        }
+                        store_state(t_ns + 64 * ((c + 1) & 1), t_s, x, 1.f);
+                        tmem_st_wait();
+                        sigma = 1.f;
+                        tc_fence_before();
+                        mbar_arrive(&sm.s16_ready);
                     }
                 } else {
                     // -S0 of chunk c + 1 for the MMAs (the hand-off).
@@ -1626,6 +1678,7 @@ if (elect_one_sync()) {
         if (leader) bulk_wait_group<0>();
     }
     __syncthreads();
+    if (kMulti && !sm.abort) copy_empty_states();
     if (sm.abort) {
         if (tid == 0) {
             atomicCAS(err, (int)kErrNone, (int)kErrTimeout);  // (the first error stays)
@@ -1682,6 +1735,11 @@ static_assert(kFusedSmemBytes <= 232448, "fused kernel shared memory");
 static_assert(kPrepUnits * kPrepTmemCols <= 512, "prep units' TMEM");
 static_assert(1 + 2 * kPrepUnits <= 16, "prep units' named barriers");
 
+// kMulti: n_chain = Hv recurrences, each over all sequences in turn (value
+// head h = blockIdx.x), and prep in the chunks' own order, which is then the
+// order the recurrences take them in.  For batches whose N x Hv recurrences
+// would not leave SMs for prep.
+template <bool kMulti>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -1705,9 +1763,10 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // rounds here avoid the wait for that round, whose items run twice as
         // long as later ones, but start the recurrence later and slow its
         // steps while more prep runs beside them: slower at 4000 tokens.)
-        const int n = order[blockIdx.x / Hv], h = blockIdx.x % Hv;
-        const int c_begin = chunk_off[n];
-        const int n_local = min(chunk_off[n + 1] - c_begin, kLocalChunks);
+        const int n = kMulti ? 0 : order[blockIdx.x / Hv];
+        const int h = kMulti ? (int)blockIdx.x : (int)blockIdx.x % Hv;
+        const int c_begin = kMulti ? 0 : chunk_off[n];
+        const int n_local = min((kMulti ? chunk_off[N] : chunk_off[n + 1]) - c_begin, kLocalChunks);
 #pragma unroll 1
         for (int c = u; c < n_local; c += kPrepUnits) {
             const int item = (c_begin + c) * Hv + h;
@@ -1718,18 +1777,22 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         fence_proxy_async_global();  // (this thread's slot writes, before the loads of them)
         __syncthreads();
-        chain_role<false, false, false, 2, true>(
+        chain_role<false, false, false, 2, true, kMulti>(
             *reinterpret_cast<ChainSmem *>(base), blockIdx.x, &tm_k, &tm_v, &tm_o, &tm_o,
             chunk_off, order, table, slots, gl, h0, out, hT, nullptr, 1, nullptr, err, N, Hk, Hv,
             flags, n_local);
     } else {
         // Skip what the recurrences prep themselves: in the prep order (by
         // position in the sequence) the first sum_n min(chunks_n, kLocalChunks)
-        // chunks.
+        // chunks; (kMulti) the first kLocalChunks chunks.
         __shared__ int s_first;
         if (threadIdx.x == 0) {
             int s = 0;
-            for (int m = 0; m < N; ++m) s += min(chunk_off[m + 1] - chunk_off[m], kLocalChunks);
+            if (kMulti) {
+                s = min(chunk_off[N], kLocalChunks);
+            } else {
+                for (int m = 0; m < N; ++m) s += min(chunk_off[m + 1] - chunk_off[m], kLocalChunks);
+            }
             s_first = s;
         }
         __syncthreads();
@@ -1740,7 +1803,7 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                         threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u,
                         s_first * Hv + kPrepUnits * pcta + u, n_units, n_items, flags, 1u, false,
-                        porder,
+                        kMulti ? nullptr : porder,
                         reinterpret_cast<PrepAhead *>(base + kPrepUnits * kPrepUnitBytes +
                                                       u * sizeof(PrepAhead)),
                         flags + n_items, s_first * Hv + 2 * n_units);
@@ -1975,8 +2038,9 @@ void time_mark(const Timing *tm, int i, cudaStream_t s) {
     if (tm) cudaEventRecord(tm->ev[i], s);
 }
 
-void time_fused(const Timing *tm, bool fused) {
-    if (tm && tm->fused) *tm->fused = fused ? 1 : 0;
+// (0 separate kernels, 1 fused, 2 fused with one recurrence per value head)
+void time_fused(const Timing *tm, int fused) {
+    if (tm && tm->fused) *tm->fused = fused;
 }
 
 // Fused path mode (gdn_prefill_fused_mode): 0 off, 1 whenever it can run,
@@ -2040,14 +2104,18 @@ bool encode_maps(const gdn_problem &p, const void *q, const void *k, const void 
 
 // The chunk table kernel (with `zero_flags`, it also clears the ready flags and
 // the prep ticket of the fused kernel).
+// zero_flags: also clear the fused kernel's flags and ticket and write its
+// prep order; orders: the recurrences' sequence order and that prep order
+// (the fused kernel with one recurrence per value head reads neither).
 gdn_status launch_table(const gdn_problem &p, const WsLayout &w, const TcPtrs &t,
                         const int32_t *cu, int snap_stride, bool zero_flags, cudaStream_t stream,
-                        const Timing *tm) {
+                        const Timing *tm, bool orders = true) {
     time_mark(tm, 0, stream);
     gdn_chunk_table_kernel<<<1, 1024, 0, stream>>>(
         cu, p.num_seqs, p.total_tokens, w.max_chunks, snap_stride, t.err, t.chunk_off, t.snap_off,
-        t.order, t.table, t.flags, zero_flags ? (int)(w.max_chunks * p.num_v_heads) + 1 : 0,
-        zero_flags ? t.porder : nullptr);
+        orders ? t.order : nullptr, t.table, t.flags,
+        zero_flags ? (int)(w.max_chunks * p.num_v_heads) + 1 : 0,
+        zero_flags && orders ? t.porder : nullptr);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     time_mark(tm, 1, stream);
     return GDN_OK;
@@ -2107,8 +2175,9 @@ gdn_status launch_chain(const gdn_problem &p, const TcPtrs &t, const TcMaps &m,
 
 // SMs the fused kernel can run on (one CTA each) on the current device, or 0
 // when it cannot be used there: no cooperative launch, or less than one CTA
-// per SM.  Looked up once per device (the kernel's shared-memory attribute is set
-// with that device current), under a lock.
+// per SM.  Looked up once per device and variant (the kernel's shared-memory
+// attribute is set with that device current), under a lock.
+template <bool kMulti>
 int fused_grid() {
     static std::mutex mu;
     static int grid_of[kMaxDevices];
@@ -2124,11 +2193,12 @@ int fused_grid() {
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(gdn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gdn_fused_kernel<kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFusedSmemBytes) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, gdn_fused_kernel) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gdn_fused_kernel, kFusedThreads,
-                                                      kFusedSmemBytes) != cudaSuccess) {
+        cudaFuncGetAttributes(&fa, gdn_fused_kernel<kMulti>) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gdn_fused_kernel<kMulti>,
+                                                      kFusedThreads, kFusedSmemBytes) !=
+            cudaSuccess) {
         cudaGetLastError();
     } else if (coop && blocks >= 1) {
         grid = sms;
@@ -2158,12 +2228,25 @@ bool fused_pays(const gdn_problem &p, int grid) {
     return std::max(prep_f, chain + kPrepItemUs) < prep_s + chain + 5.0;
 }
 
+// Whether the kMulti fused kernel should be used for a batch whose N x Hv
+// recurrences do not fit beside prep: whenever its Hv recurrences do.  Its
+// recurrence runs every chunk of the batch in turn, with a restart per
+// sequence, while prep runs on the other SMs; the separate kernels run prep,
+// then the (sequence, value head) recurrences side by side, bound by HBM and
+// by the longest sequence.  Measured on GB300 at 16/48 heads it was the
+// faster of the two for every batch tried: 8 sequences of 512 to 32768
+// tokens (1.51 against 1.86 ms), 4 x 2000, 8 x 1024, 16 x 512, 64 x 128,
+// 512 x 16 and 2000 x 4 tokens, and mixes of long and one-token sequences.
+bool multi_pays(const gdn_problem &p, int grid) {
+    return p.num_v_heads + 16 <= grid && (int64_t)p.num_seqs * p.num_v_heads + 16 > grid;
+}
+
 // Chunk table, then the fused kernel: prep and the recurrence in one launch.
 // False when the launch was refused (the caller then runs the separate
 // kernels; the chunk table is already in place).
 bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, const TcMaps &m,
                   const float *g, const float *beta, const float *h0, void *out, float *hT,
-                  int grid, cudaStream_t stream, bool pdl) {
+                  int grid, bool multi, cudaStream_t stream, bool pdl) {
     // Cooperative (every CTA resident, so the waits on ready flags end) and,
     // unless the call is timed, a programmatic dependent of the chunk table
     // kernel (its CTAs are placed and set up while the table is written; they
@@ -2180,11 +2263,12 @@ bool launch_fused(const gdn_problem &p, const WsLayout &w, const TcPtrs &t, cons
     cfg.dynamicSmemBytes = kFusedSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    const int n_chain = p.num_seqs * p.num_v_heads;
+    const int n_chain = multi ? p.num_v_heads : p.num_seqs * p.num_v_heads;
     const int n_items = (int)(w.max_chunks * p.num_v_heads);
+    auto kernel = multi ? gdn_fused_kernel<true> : gdn_fused_kernel<false>;
     for (int na = pdl ? 2 : 1; na >= 1; --na) {
         cfg.numAttrs = na;
-        if (cudaLaunchKernelEx(&cfg, gdn_fused_kernel, m.tq, m.tk, m.tv, m.to, g, beta,
+        if (cudaLaunchKernelEx(&cfg, kernel, m.tq, m.tk, m.tv, m.to, g, beta,
                                (const int *)t.chunk_off, (const int *)t.order,
                                (const int4 *)t.table, t.slots, t.gl, h0,
                                static_cast<__nv_bfloat16 *>(out), hT, t.err, t.flags,
@@ -2210,7 +2294,7 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
         timing.fused = fused;
         tm = &timing;
     }
-    time_fused(tm, false);
+    time_fused(tm, 0);
     if (p.num_seqs == 0) return GDN_OK;
     const WsLayout w = ws_layout(p);
     const TcPtrs t = tc_ptrs(w, p.workspace);
@@ -2222,18 +2306,29 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     const bool pdl = tm == nullptr;
     // (sequence x value head) recurrences that leave SMs for prep: the fused
     // kernel.
-    const int grid = (snaps || p.total_tokens == 0) ? 0 : fused_grid();
     const int mode = prefill_fused_mode(-1);
-    if (grid > 0 && mode > 0 &&
-        (mode == 1 ? (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid : fused_pays(p, grid))) {
-        gdn_status st = launch_table(p, w, t, cu, 0, true, stream, tm);
+    const bool plain = snaps || p.total_tokens == 0 || mode == 0;
+    const int grid = plain ? 0 : fused_grid<false>();
+    // Fused with one recurrence per (sequence, value head) when they leave SMs
+    // for prep, else (kMulti) one per value head over all sequences.
+    const bool fits = (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid;
+    const bool one = grid > 0 && (mode == 1 ? fits : fused_pays(p, grid));
+    const int grid_m = (plain || one || fits) ? 0 : fused_grid<true>();
+    const bool multi = grid_m > 0 &&
+                       (mode == 1 ? p.num_v_heads + 16 <= grid_m : multi_pays(p, grid_m));
+    if (one || multi) {
+        gdn_status st = launch_table(p, w, t, cu, 0, true, stream, tm, !multi);
         if (st != GDN_OK) return st;
         time_mark(tm, 2, stream);  // (no separate prep launch)
-        if (launch_fused(p, w, t, m, g, beta, h0, out, hT, grid, stream, pdl)) {
+        if (launch_fused(p, w, t, m, g, beta, h0, out, hT, multi ? grid_m : grid, multi, stream,
+                         pdl)) {
             time_mark(tm, 3, stream);
-            time_fused(tm, true);
+            time_fused(tm, multi ? 2 : 1);
             return GDN_OK;
         }
+        // (the launch was refused: the separate kernels, with the sequence
+        // order the chunk table left out for the per-head variant)
+        if (multi && (st = launch_table(p, w, t, cu, 0, false, stream, tm)) != GDN_OK) return st;
         st = launch_prep(p, w, t, m, g, beta, stream, false, tm);
         if (st != GDN_OK) return st;
         st = launch_chain<false, false>(p, t, m, m.to, h0, out, hT, nullptr, 1, stream, false);

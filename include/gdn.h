@@ -129,11 +129,15 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem);
  * SMs free, the intra-chunk prep and the recurrence run as one cooperative
  * launch: prep on the free SMs, publishing each chunk as it is done (every
  * sequence's chunk c before any chunk c + 1), and the recurrences following
- * (each first preps its own first four chunks).  Otherwise they are separate
- * kernels.  The results are the same either way.  By default the fused
- * kernel is used when a cost model of the two paths expects it to be faster
- * (long sequences with few (sequence, value head) pairs); see
- * gdn_prefill_fused_mode.
+ * (each first preps its own first four chunks).  When they do not, the
+ * fused launch can instead run Hv recurrences, each taking one value head
+ * through every sequence in turn (restarting from each sequence's initial
+ * state), with prep publishing the chunks in their packed order.  Otherwise
+ * prep and the recurrence are separate kernels.  The results are the same
+ * every way.  By default the fused kernel is used when a cost model of the
+ * paths expects it to be faster (long sequences with few (sequence, value
+ * head) pairs), and the per-head variant whenever the first does not fit
+ * and it does; see gdn_prefill_fused_mode.
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
                                      const void *q, const void *k, const void *v,
@@ -390,7 +394,8 @@ typedef struct CUevent_st *gdn_event_t;
  * When prep and the recurrence run as one fused launch (see
  * gdn_chunk_prefill), events[1] and events[2] mark the same point and
  * events[3] follows the fused kernel; *fused (if not NULL) is set to 1 in
- * that case and 0 otherwise.  With no sequences the four events are recorded
+ * that case (2 for the fused variant with one recurrence per value head)
+ * and 0 otherwise.  With no sequences the four events are recorded
  * back to back.  Nothing is kept between calls: calls on several streams or
  * threads time themselves independently.
  *   events   four valid events (cudaEventCreate), owned by the caller;

@@ -1,7 +1,10 @@
 """The fused prep + recurrence kernel against the separate kernels and the
 fp64 oracle.  Both paths run the same arithmetic per chunk, so their outputs
 and final states are equal bit for bit; the fused path is forced on for
-batches the cost model would send to the separate kernels."""
+batches the cost model would send to the separate kernels.  Batches whose
+(sequence, value head) recurrences do not fit beside prep take the fused
+variant with one recurrence per value head over all sequences in turn
+(reported as 2 by the timed call)."""
 import pytest
 import torch
 
@@ -55,6 +58,43 @@ def test_fused_equals_separate_and_oracle(lens, Hk, Hv):
     e_o, e_f = rel(f64(o1[:, vh]), o_ref), rel(f64(f1[:, vh]), f_ref)
     print(f"[parity] fused lens={lens} {Hk}/{Hv}: out {e_o:.3e} final {e_f:.3e}")
     assert e_o <= TOL_BF16 and e_f <= TOL_BF16
+
+
+@pytest.mark.parametrize("lens,Hk,Hv,h0", [
+    # 8 x 48 recurrences: one per value head; empty, one-token and ragged
+    # sequences, the first ones shorter than the four chunks each recurrence
+    # preps itself (so its own prep spans sequences)
+    ([64, 1, 0, 100, 130, 2000, 0, 77, 1000, 0], 16, 48, True),
+    ([0, 0, 700, 64, 1500], 16, 48, False),
+    # 40 sequences x 6 value heads (240 recurrences)
+    ([37 * (i % 7) + 64 * (i % 3) for i in range(40)], 2, 6, True),
+])
+def test_multi_fused_equals_separate_and_oracle(lens, Hk, Hv, h0):
+    p = inputs.prefill_inputs(lens, Hk, Hv, 128, 128, dtype=torch.bfloat16, seed=23,
+                              initial_state_std=0.02 if h0 else None)
+    o1, f1, fused1 = run(p, 1)
+    o0, f0, fused0 = run(p, 0)
+    assert fused1 == 2 and fused0 == 0
+    assert torch.equal(o1, o0), "outputs differ between the fused and separate kernels"
+    assert torch.equal(f1, f0), "final states differ"
+    o_ref, f_ref, vh = oracle_prefill(p)
+    e_o, e_f = rel(f64(o1[:, vh]), o_ref), rel(f64(f1[:, vh]), f_ref)
+    print(f"[parity] fused per head N={len(lens)} {Hk}/{Hv}: out {e_o:.3e} final {e_f:.3e}")
+    assert e_o <= TOL_BF16 and e_f <= TOL_BF16
+
+
+def test_multi_fused_chosen_when_the_recurrences_do_not_fit():
+    """By default a batch whose (sequence, value head) recurrences do not fit
+    beside prep takes the per-head fused variant, long or short sequences
+    alike; with more value heads than that variant leaves room for
+    (Hv + 16 > 152 SMs) it takes the separate kernels."""
+    for lens in ([1500, 900, 2600, 1200], [300] * 8):
+        p = inputs.prefill_inputs(lens, 16, 48, 128, 128, dtype=torch.bfloat16, seed=24)
+        _, _, fused = run(p, 2)
+        assert fused == 2, lens
+    p = inputs.prefill_inputs([300, 200], 16, 144, 128, 128, dtype=torch.bfloat16, seed=24)
+    _, _, fused = run(p, 2)
+    assert fused == 0
 
 
 def test_fused_mode_query_and_default():
