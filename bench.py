@@ -704,10 +704,11 @@ def main(argv=None):
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--ref-tokens", type=int, default=4000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fused-mode", type=int, choices=(0, 1, 2), default=2,
+    ap.add_argument("--fused-mode", type=int, choices=(0, 1, 2, 3), default=2,
                     help="when the prefill uses its fused prep + recurrence kernel "
                          "(gdn_prefill_fused_mode: 0 never, 1 whenever it fits, "
-                         "2 by the library's cost model, its default)")
+                         "2 by the library's cost model, its default, 3 the variant with "
+                         "one recurrence per value head whenever it fits)")
     ap.add_argument("--prefill-case", default=None, metavar="LENS",
                     help="time one packed prefill batch alone (comma-separated sequence "
                          "lengths, 16/48 heads) instead of the bench, for profiling")

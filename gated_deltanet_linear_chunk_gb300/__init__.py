@@ -220,7 +220,8 @@ def gdn_chunk_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 def gdn_prefill_fused_mode(mode: int = -1) -> int:
     """Sets when prefills use the fused prep + recurrence kernel (0 never,
-    1 whenever possible, 2 when expected faster; default 2) and returns the
+    1 whenever possible, 2 when expected faster, 3 the variant with one
+    recurrence per value head whenever possible; default 2) and returns the
     previous mode; -1 only queries."""
     return int(library().gdn_prefill_fused_mode(int(mode)))
 

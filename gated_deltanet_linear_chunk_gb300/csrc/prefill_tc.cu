@@ -2044,7 +2044,8 @@ void time_fused(const Timing *tm, int fused) {
 }
 
 // Fused path mode (gdn_prefill_fused_mode): 0 off, 1 whenever it can run,
-// 2 when the cost model below expects it to be faster.
+// 2 when the cost model below expects it to be faster, 3 the variant with one
+// recurrence per value head whenever it can run.
 std::atomic<int> g_fused_mode{2};
 
 constexpr int kMaxDevices = 64;
@@ -2052,7 +2053,7 @@ constexpr int kMaxDevices = 64;
 }  // namespace
 
 int prefill_fused_mode(int mode) {
-    if (mode >= 0 && mode <= 2) return g_fused_mode.exchange(mode);
+    if (mode >= 0 && mode <= 3) return g_fused_mode.exchange(mode);
     return g_fused_mode.load();
 }
 
@@ -2228,17 +2229,35 @@ bool fused_pays(const gdn_problem &p, int grid) {
     return std::max(prep_f, chain + kPrepItemUs) < prep_s + chain + 5.0;
 }
 
-// Whether the kMulti fused kernel should be used for a batch whose N x Hv
-// recurrences do not fit beside prep: whenever its Hv recurrences do.  Its
-// recurrence runs every chunk of the batch in turn, with a restart per
-// sequence, while prep runs on the other SMs; the separate kernels run prep,
-// then the (sequence, value head) recurrences side by side, bound by HBM and
-// by the longest sequence.  Measured on GB300 at 16/48 heads it was the
-// faster of the two for every batch tried: 8 sequences of 512 to 32768
-// tokens (1.51 against 1.86 ms), 4 x 2000, 8 x 1024, 16 x 512, 64 x 128,
-// 512 x 16 and 2000 x 4 tokens, and mixes of long and one-token sequences.
+// Whether the kMulti fused kernel should beat the separate kernels, from
+// rates measured on GB300 (16/48 heads, d = 128, L2 flushed; each fits the
+// measured times of 2-2000 sequences within about 10 %), in µs:
+//   separate: prep 5 + 12.5 per wave of 5 x SMs items; then the (sequence,
+//     value head) recurrences, ceil(N Hv / SMs) waves of the mean sequence's
+//     chunks, each chunk max(1.25, 0.019 x the recurrences running at once
+//     - 0.3) (HBM-bound when many run), plus 2 per wave and 5;
+//   kMulti: 20 + per chunk of the batch max(1.25, the prep time of its Hv
+//     items on the 4 (SMs - Hv) units at 12.5 each).
+// The host does not know the lengths (cu_seqlens is on the device): the
+// chunk count is taken as ceil(T / 64) + (N - 1) / 4, and the longest
+// sequence as the mean one, which understates the separate recurrence of a
+// batch of unequal lengths.  kMulti needs an estimate 5 % below the other.
 bool multi_pays(const gdn_problem &p, int grid) {
-    return p.num_v_heads + 16 <= grid && (int64_t)p.num_seqs * p.num_v_heads + 16 > grid;
+    const int64_t N = p.num_seqs, Hv = p.num_v_heads;
+    if (Hv + 16 > grid || N < 2) return false;
+    const double chunks = (double)((p.total_tokens + C - 1) / C) + (double)(N - 1) / 4.0;
+    const double items = chunks * (double)Hv;
+    const double prep_s = 5.0 + 12.5 * items / (double)(kPrepCtasPerSm * grid);
+    const int64_t pairs = N * Hv;
+    const double waves = (double)((pairs + grid - 1) / grid);
+    const double conc = (double)std::min<int64_t>(pairs, grid);
+    const double mean_chunks = (double)((p.total_tokens / N + C - 1) / C);
+    const double step_s = std::max(1.25, 0.019 * conc - 0.3);
+    const double chain_s = 5.0 + waves * (mean_chunks * step_s + 2.0);
+    const double step_m =
+        std::max(1.25, 12.5 * (double)Hv / (double)(kPrepUnits * (grid - Hv)));
+    const double multi = 20.0 + chunks * step_m;
+    return multi < 0.95 * (prep_s + chain_s);
 }
 
 // Chunk table, then the fused kernel: prep and the recurrence in one launch.
@@ -2310,12 +2329,14 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     const bool plain = snaps || p.total_tokens == 0 || mode == 0;
     const int grid = plain ? 0 : fused_grid<false>();
     // Fused with one recurrence per (sequence, value head) when they leave SMs
-    // for prep, else (kMulti) one per value head over all sequences.
+    // for prep (mode 2: and the cost model prefers it), else fused with one
+    // per value head over all sequences (kMulti; mode 1: when the first does
+    // not fit, mode 2: when its cost model prefers it, mode 3: always).
     const bool fits = (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid;
-    const bool one = grid > 0 && (mode == 1 ? fits : fused_pays(p, grid));
-    const int grid_m = (plain || one || fits) ? 0 : fused_grid<true>();
-    const bool multi = grid_m > 0 &&
-                       (mode == 1 ? p.num_v_heads + 16 <= grid_m : multi_pays(p, grid_m));
+    const bool one = mode != 3 && grid > 0 && (mode == 1 ? fits : fused_pays(p, grid));
+    const int grid_m = (plain || one || (fits && mode == 1)) ? 0 : fused_grid<true>();
+    const bool multi = grid_m > 0 && (mode == 2 ? multi_pays(p, grid_m)
+                                                : p.num_v_heads + 16 <= grid_m);
     if (one || multi) {
         gdn_status st = launch_table(p, w, t, cu, 0, true, stream, tm, !multi);
         if (st != GDN_OK) return st;

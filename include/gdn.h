@@ -134,10 +134,10 @@ GDN_API size_t gdn_chunk_prefill_workspace_size(const gdn_problem *problem);
  * through every sequence in turn (restarting from each sequence's initial
  * state), with prep publishing the chunks in their packed order.  Otherwise
  * prep and the recurrence are separate kernels.  The results are the same
- * every way.  By default the fused kernel is used when a cost model of the
- * paths expects it to be faster (long sequences with few (sequence, value
- * head) pairs), and the per-head variant whenever the first does not fit
- * and it does; see gdn_prefill_fused_mode.
+ * every way.  By default either fused variant is used when a cost model of
+ * the paths expects it to be faster: the first for long sequences with few
+ * (sequence, value head) pairs, the per-head one for batches whose
+ * recurrences would run in several waves; see gdn_prefill_fused_mode.
  */
 GDN_API gdn_status gdn_chunk_prefill(const gdn_problem *problem,
                                      const void *q, const void *k, const void *v,
@@ -415,7 +415,9 @@ GDN_API gdn_status gdn_chunk_prefill_timed(const gdn_problem *problem,
 /*
  * Choice of the fused prep + recurrence kernel for later prefills (process
  * wide, an atomic integer): 0 never, 1 whenever it can run, 2 when expected
- * to be faster (the default).  Any other value only queries.  Returns the
+ * to be faster (the default), 3 the variant with one recurrence per value
+ * head whenever it can run (Hv + 16 <= SMs), even where the (sequence, value
+ * head) recurrences would fit.  Any other value only queries.  Returns the
  * previous mode.
  */
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode);

@@ -205,10 +205,12 @@ def test_timed_prefill_argument_errors(lib):
 def test_fused_mode_needs_no_device(lib):
     """The mode switch is a plain atomic: set, query, restore."""
     old = lib.gdn_prefill_fused_mode(-1)
-    assert old in (0, 1, 2)
+    assert old in (0, 1, 2, 3)
     assert lib.gdn_prefill_fused_mode(0) == old
-    assert lib.gdn_prefill_fused_mode(9) == 0
-    assert lib.gdn_prefill_fused_mode(old) == 0
+    assert lib.gdn_prefill_fused_mode(3) == 0
+    assert lib.gdn_prefill_fused_mode(9) == 3
+    assert lib.gdn_prefill_fused_mode(4) == 3
+    assert lib.gdn_prefill_fused_mode(old) == 3
 
 
 def scan(lib, p, L, out=A + 24576):

@@ -83,23 +83,27 @@ def test_multi_fused_equals_separate_and_oracle(lens, Hk, Hv, h0):
     assert e_o <= TOL_BF16 and e_f <= TOL_BF16
 
 
-def test_multi_fused_chosen_when_the_recurrences_do_not_fit():
-    """By default a batch whose (sequence, value head) recurrences do not fit
-    beside prep takes the per-head fused variant, long or short sequences
-    alike; with more value heads than that variant leaves room for
-    (Hv + 16 > 152 SMs) it takes the separate kernels."""
-    for lens in ([1500, 900, 2600, 1200], [300] * 8):
+def test_default_choice_of_the_per_head_variant():
+    """The default (mode 2) takes the per-head fused variant where its cost
+    model expects it to be faster than the separate kernels: several waves of
+    (sequence, value head) recurrences; not for three equal sequences, whose
+    144 recurrences run in one wave; never with more value heads than it
+    leaves room for (Hv + 16 > 152 SMs).  Mode 3 takes it whenever it can
+    run."""
+    for lens, want in (([1500, 900, 2600, 1200], 2), ([1024] * 8, 2), ([1000] * 3, 0)):
         p = inputs.prefill_inputs(lens, 16, 48, 128, 128, dtype=torch.bfloat16, seed=24)
         _, _, fused = run(p, 2)
-        assert fused == 2, lens
+        assert fused == want, lens
+    p = inputs.prefill_inputs([1000] * 3, 16, 48, 128, 128, dtype=torch.bfloat16, seed=24)
+    assert run(p, 3)[2] == 2
     p = inputs.prefill_inputs([300, 200], 16, 144, 128, 128, dtype=torch.bfloat16, seed=24)
-    _, _, fused = run(p, 2)
-    assert fused == 0
+    assert run(p, 2)[2] == 0 and run(p, 3)[2] == 0
+    gdn.gdn_prefill_fused_mode(2)
 
 
 def test_fused_mode_query_and_default():
     old = gdn.gdn_prefill_fused_mode(-1)
-    assert old in (0, 1, 2)
+    assert old in (0, 1, 2, 3)
     assert gdn.gdn_prefill_fused_mode(2) == old
     assert gdn.gdn_prefill_fused_mode(7) == 2   # out of range: query only
     p = inputs.prefill_inputs([4000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
