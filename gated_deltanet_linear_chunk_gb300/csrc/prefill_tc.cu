@@ -365,21 +365,6 @@ struct alignas(1024) PrepSmem {
     int fact;       // the chunk's A and P factorise (gamma_L >= kFactorGammaMin)
 };
 
-// What a persistent prep unit keeps beside its PrepSmem so that each item
-// starts without waiting on memory: the second half of W^T's staging (W^T
-// goes to ab and wt_hi, so the K and Q atoms take the next item's tiles as
-// soon as this item's W^T MMA has read them), the next item's g and beta
-// (copied by cp.async during this item, by item parity; 0 past the end), and
-// the items up to two ahead with their chunk-table entries (by the unit's
-// item count mod 4).
-struct alignas(1024) PrepAhead {
-    uint8_t wt_hi[kTile];
-    float gs[2][C];
-    float bs[2][C];
-    int4 loc[4];  // {chunk, value head, first token, length}
-    int idx[4];   // item number, -1 past the last
-};
-
 // Row r of A's fp32 diagonal 16 x 16 block b in ab: 16 floats; blocks 260
 // floats apart (so that rows of two blocks read at once fall in different
 // banks).
@@ -446,29 +431,6 @@ __device__ __forceinline__ void decayed8(const PrepSmem &sm, uint32_t taddr, int
         else decayed8<false>(sm, taddr, i0, last, s, rs, gr, a);       \
     } while (0)
 
-// L2 prefetch of what an item will load: its K and Q tiles and its g and
-// beta values (64 tokens, one value head: strided, so every line is fetched
-// separately).  Called by one full warp.
-__device__ __forceinline__ void prep_prefetch(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                                              const float *g, const float *beta, int tok0, int L,
-                                              int Hv, int h, int hk) {
-    const int lane = threadIdx.x & 31;
-    if (lane == 0) {
-        tma_prefetch_3d(tm_k, 0, hk, tok0);
-        tma_prefetch_3d(tm_k, 64, hk, tok0);
-        tma_prefetch_3d(tm_q, 0, hk, tok0);
-        tma_prefetch_3d(tm_q, 64, hk, tok0);
-    }
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        const int t = 2 * lane + s;
-        if (t < L) {
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(g + (size_t)(tok0 + t) * Hv + h));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + (size_t)(tok0 + t) * Hv + h));
-        }
-    }
-}
-
 // The unit's wait for an mbarrier phase: warp 0 polls (bounded), then the
 // whole unit meets at its named barrier, which also ORs the failure flags.
 // True when the unit must stop.
@@ -479,12 +441,11 @@ __device__ __forceinline__ bool unit_wait(uint64_t *bar, uint32_t parity, int wa
 }
 
 // Makes an item's slot visible device-wide and publishes its ready flag
-// (the thread that issued the slot's bulk copies, which are all but the
-// kNewer most recent groups; every other thread's slot writes are ordered
-// before a unit barrier this thread has passed since).
-template <int kNewer>
+// (the thread that issued the slot's bulk copies, all of them this thread's
+// committed groups; every other thread's slot writes are ordered before a
+// unit barrier this thread has passed since).
 __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
-    bulk_wait_group<kNewer>();
+    bulk_wait_group<0>();
     fence_proxy_async_global();
     __threadfence();
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(epoch) : "memory");
@@ -501,13 +462,16 @@ __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
 // loop.
 // `relinquish`: give up the CTA's TMEM allocation permit after allocating
 // (only when the CTA allocates nothing after this unit).  kLoop units also
-// take `ahead` (see PrepAhead) and `ticket`: their first two items are item0
-// and item0 + stride (the grid's first two rounds, in order), the later ones
-// are drawn one at a time from *ticket (item = dyn0 + ticket, in order, while
-// items remain), so that a unit slowed down holds up at most the two items
-// it has drawn.  Each item is drawn two items ahead (the ticket, the prep
-// order and the chunk table read a few phases apart), and its tiles, g and
-// beta are in flight during the item before.
+// take `ticket`: their first two items are item0 and item0 + stride (the
+// grid's first two rounds, in order), the later ones are drawn one at a time
+// from *ticket (item = dyn0 + ticket, in order, while items remain), so that
+// a unit slowed down holds up only the item it is on.  The next item is drawn
+// during the current one (the ticket, the prep order and the chunk table read
+// a few phases apart) into the unit's two-entry ring `nxt`.  Every item's
+// flag is published as soon as its slot is written.  (A look-ahead that
+// loaded each item's tiles, g and beta during the item before, and deferred
+// each flag to the next item, was slower: the first pass of its larger code
+// through an SM cost more than it saved.)
 //
 // Per item:
 //   gamma = cumsum(g), b, e^gamma, e^{gamma_L - gamma};  [K; Q] K^T (M = 128);
@@ -529,8 +493,7 @@ __device__ __forceinline__ void prep_unit(
     const int4 *__restrict__ table, uint8_t *__restrict__ slots, float *__restrict__ gl,
     int *__restrict__ err, int N, int Hk, int Hv, int ltid, int bar, int bar2, int item0,
     int stride, int n_items, unsigned *flags, unsigned epoch, bool relinquish,
-    const int *__restrict__ porder = nullptr, PrepAhead *ahead = nullptr,
-    unsigned *ticket = nullptr, int dyn0 = 0) {
+    const int *__restrict__ porder = nullptr, unsigned *ticket = nullptr, int dyn0 = 0) {
     const int tid = ltid, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
     const int q4 = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of the physical warp
@@ -554,17 +517,9 @@ __device__ __forceinline__ void prep_unit(
         mbar_init(&sm.tma_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        if (kLoop) {
-            const int i0 = item0, i1 = item0 + stride;
-            const bool v0 = i0 < n_items && chunk_of(i0) < n_ch;
-            const bool v1 = i1 < n_items && chunk_of(i1) < n_ch;
-            ahead->idx[0] = v0 ? i0 : -1;
-            ahead->idx[1] = v1 ? i1 : -1;
-            if (v0) ahead->loc[0] = locate(i0);
-            if (v1) ahead->loc[1] = locate(i1);
-        } else if (item0 < n_items && chunk_of(item0) < n_ch) {
-            sm.nxt[0] = locate(item0);
-        }
+        // The first item's entry (chunk -1 when there is none).
+        sm.nxt[0] = (item0 < n_items && chunk_of(item0) < n_ch) ? locate(item0)
+                                                                 : make_int4(-1, 0, 0, 0);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem, kPrepTmemCols);
@@ -579,12 +534,10 @@ __device__ __forceinline__ void prep_unit(
     bool bad = false;
     uint32_t mph = 0, tph = 0;
     int it = 0;
-    int4 pend = make_int4(-1, 0, 0, 0);  // (copier) item whose flag is still to publish
-    bool tma_ahead = false;              // (kLoop) this item's tiles were issued by the last one
 #pragma unroll 1
     for (; !bad; ++it) {
-        if (kLoop ? ahead->idx[it & 3] < 0 : (item0 >= n_items || chunk_of(item0) >= n_ch)) break;
-        const int4 cur = kLoop ? ahead->loc[it & 3] : sm.nxt[0];
+        if (sm.nxt[it & 1].x < 0) break;
+        const int4 cur = sm.nxt[it & 1];
         const int ch = cur.x, h = cur.y, tok0 = cur.z, L = cur.w, hk = h / G;
         if (kDebug && !(ch >= 0 && ch < n_ch && h >= 0 && h < Hv && tok0 >= 0 && L >= 1 && L <= C)) {
             if (tid == 0) debug_fail(err, kErrIndex);  // (then the unit stops, as on a time-out)
@@ -592,13 +545,11 @@ __device__ __forceinline__ void prep_unit(
             break;
         }
         uint8_t *const slot = slots + ((size_t)ch * Hv + h) * kSlotBytes;
-        const bool more = kLoop && ahead->idx[(it + 1) & 3] >= 0;
-        // (warp 2, lane 0) the item after next: its number, whether it
+        // (kLoop: warp 2, lane 0) the next item: its number, whether it
         // exists, its chunk from the prep order and its chunk-table entry
         int item2 = 0, pch = 0;
         bool more2 = false;
-        int4 e2 = make_int4(0, 0, 0, 0);
-        if (tid == kCopier && !tma_ahead) {
+        if (tid == kCopier) {
             if (kLoop) {
                 // The previous item's bulk copies have read the tiles, and
                 // its generic accesses are ordered before the TMA writes.
@@ -613,14 +564,7 @@ __device__ __forceinline__ void prep_unit(
         }
         if (warp == 1) {
             // gamma, b and the decay factors while the tiles are in flight
-            // (kLoop: from the g and beta copied during the previous item).
-            if (kLoop && it > 0) {
-                const float *gs = ahead->gs[it & 1], *bs = ahead->bs[it & 1];
-                chunk_gamma_of(gs[2 * lane], gs[2 * lane + 1], bs[2 * lane], bs[2 * lane + 1],
-                               sm.gam, sm.beta, sm.eg, sm.dec, sm.einv);
-            } else {
-                chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec, sm.einv);
-            }
+            chunk_gamma(g, tok0, L, Hv, h, sm.gam, sm.beta, beta, sm.eg, sm.dec, sm.einv);
             float *slot_f = reinterpret_cast<float *>(slot);
             slot_f[kSlotEG / 4 + 2 * lane] = sm.eg[2 * lane];
             slot_f[kSlotEG / 4 + 2 * lane + 1] = sm.eg[2 * lane + 1];
@@ -632,33 +576,17 @@ __device__ __forceinline__ void prep_unit(
                 gl[(size_t)ch * Hv + h] = sm.eg[C - 1];
                 sm.fact = sm.gam[C - 1] >= kFactorGammaMin;
             }
-        } else if (warp == 2 && more) {
-            // The next item's g and beta into shared memory; the first load
-            // of the entry of the item after it (used two phases on).
-            const int4 nx = ahead->loc[(it + 1) & 3];
-            float *gs = ahead->gs[(it + 1) & 1], *bs = ahead->bs[(it + 1) & 1];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int t = 2 * lane + u;
-                if (t < nx.w) {
-                    cp_async4(gs + t, g + (size_t)(nx.z + t) * Hv + nx.y);
-                    cp_async4(bs + t, beta + (size_t)(nx.z + t) * Hv + nx.y);
-                } else {
-                    gs[t] = 0.f;
-                    bs[t] = 0.f;
-                }
-            }
-            cp_async_commit();
-            if (it == 0) prep_prefetch(tm_q, tm_k, g, beta, nx.z, nx.w, Hv, nx.y, nx.y / G);
-            if (lane == 0) {
-                item2 = dyn0 + (int)atomicAdd(ticket, 1u);
-                more2 = item2 < n_items && chunk_of(item2) < n_ch;
-            }
+        } else if (kLoop && warp == 2 && lane == 0) {
+            // The next item: the second static round, then the ticket (its
+            // value first read after the unit barrier below).
+            item2 = it == 0 ? item0 + stride : dyn0 + (int)atomicAdd(ticket, 1u);
         }
         if ((bad = unit_wait(&sm.tma_bar, tph, warp, bar, bad))) break;
         tph ^= 1;
-        tma_ahead = false;
-        if (warp == 2 && lane == 0 && more2) pch = porder ? porder[chunk_of(item2)] : chunk_of(item2);
+        if (kLoop && warp == 2 && lane == 0) {
+            more2 = item2 < n_items && chunk_of(item2) < n_ch;
+            if (more2) pch = porder ? porder[chunk_of(item2)] : chunk_of(item2);
+        }
         if (tid == 0) {
             tc_fence_after();
             const uint32_t base = smem_u32(sm.kq);
@@ -696,20 +624,11 @@ __device__ __forceinline__ void prep_unit(
             }
         }
         fence_proxy_async_smem();
-        // (kLoop: the previous item's W^T copies read ab and wt_hi, which the
-        // next phases write)
-        if (kLoop && tid == kCopier) bulk_wait_group_read<0>();
         named_barrier(bar, kPrepThreads);
         if (tid == kCopier) {
             bulk_store(slot + kSlotQ, sm.kq + kTile, kTile);
             bulk_store(slot + kSlotQ + kTile, sm.kq + 3 * kTile, kTile);
             bulk_commit_group();
-            // The previous item, a few thousand cycles after its last copies
-            // were issued (waiting for them at once would hold up the unit).
-            if (kLoop && flags && pend.x >= 0) {
-                publish_item<1>(flags + (size_t)pend.x * Hv + pend.y, epoch);
-                pend.x = -1;
-            }
         }
         // ---- A's four diagonal 16 x 16 blocks (fp32, into ab) from K K^T
         // (lanes 0-63), P from Q K^T (lanes 64-127, to the slot).  A warp's
@@ -799,7 +718,11 @@ __device__ __forceinline__ void prep_unit(
         // 16-31 x columns 0-15 and 48-63 x columns 32-47 it is C X1 of each
         // 32 x 32 diagonal block (C = its lower-left 16 x 16 block of A); the
         // rest of Y (from A's lower-left 32 x 32 block) is not used.
-        if (warp == 2 && lane == 0 && more2) e2 = table[pch];
+        if (kLoop && warp == 2 && lane == 0) {  // (the next item's entry, read at its start)
+            const int4 e2 = more2 ? table[pch] : make_int4(0, 0, 0, 0);
+            sm.nxt[(it + 1) & 1] = more2 ? make_int4(pch, item2 % Hv, e2.y, e2.z)
+                                         : make_int4(-1, 0, 0, 0);
+        }
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16(64, 64, false, true);
@@ -875,19 +798,6 @@ __device__ __forceinline__ void prep_unit(
         fence_proxy_async_smem();
         tc_fence_before();
         named_barrier(bar, kPrepThreads);
-        if (warp == 2 && more) {
-            // The item after next (or none): recorded, and its inputs into L2.
-            const bool v2 = __shfl_sync(0xffffffffu, more2, 0);
-            const int i2 = __shfl_sync(0xffffffffu, item2, 0);
-            if (v2) {
-                const int4 nx2 = make_int4(__shfl_sync(0xffffffffu, pch, 0), i2 % Hv,
-                                           __shfl_sync(0xffffffffu, e2.y, 0),
-                                           __shfl_sync(0xffffffffu, e2.z, 0));
-                if (lane == 0) ahead->loc[(it + 2) & 3] = nx2;
-                prep_prefetch(tm_q, tm_k, g, beta, nx2.z, nx2.w, Hv, nx2.y, nx2.y / G);
-            }
-            if (lane == 0) ahead->idx[(it + 2) & 3] = v2 ? i2 : -1;
-        }
         // ---- N = D' E  (M = 64, N = 64, K = 64)
         if (tid == 0) {
             tc_fence_after();
@@ -984,28 +894,10 @@ __device__ __forceinline__ void prep_unit(
         if ((bad = unit_wait(&sm.mma_bar, mph, warp, bar, bad))) break;
         mph ^= 1;
         tc_fence_after();
-        if (kLoop && more) {
-            // The W^T MMA has read the K atoms and T diag(b e^gamma); the Q
-            // atoms are dead once T diag(b)'s copy has read Q atom 1: the
-            // next item's tiles go now, beside this item's W^T read-back.
-            if (tid == kCopier) {
-                bulk_wait_group_read<0>();
-                fence_proxy_async_smem();
-                const int4 nx = ahead->loc[(it + 1) & 3];
-                const int nhk = nx.y / G;
-                mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
-                tma_load_3d(sm.kq + 0 * kTile, tm_k, 0, nhk, nx.z, &sm.tma_bar);
-                tma_load_3d(sm.kq + 1 * kTile, tm_q, 0, nhk, nx.z, &sm.tma_bar);
-                tma_load_3d(sm.kq + 2 * kTile, tm_k, 64, nhk, nx.z, &sm.tma_bar);
-                tma_load_3d(sm.kq + 3 * kTile, tm_q, 64, nhk, nx.z, &sm.tma_bar);
-            }
-            tma_ahead = true;
-        }
-        // W^T staged (16 KB), then copied: in K atom 0 + Q atom 0 (both
-        // dead), or (kLoop) in ab (rows 0-63) and wt_hi (rows 64-127).
+        // W^T staged (16 KB) in K atom 0 + Q atom 0 (both dead), then copied.
         {
-            uint8_t *const wt = kLoop ? (row < 64 ? sm.ab : ahead->wt_hi) : sm.kq;
-            const int wr = kLoop ? (row & 63) : row;
+            uint8_t *const wt = sm.kq;
+            const int wr = row;
             float y[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -1017,38 +909,19 @@ __device__ __forceinline__ void prep_unit(
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        // (the next item's g and beta are in shared memory before it starts)
-        if (kLoop && warp == 2) cp_async_wait_all();
         named_barrier(bar, kPrepThreads);
         if (tid == kCopier) {
-            if (kLoop) {
-                bulk_store(slot + kSlotWT, sm.ab, kTile);
-                bulk_store(slot + kSlotWT + kTile, ahead->wt_hi, kTile);
-            } else {
-                bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
-            }
+            bulk_store(slot + kSlotWT, sm.kq, 2 * kTile);
             bulk_commit_group();
-            if (flags && it == 0) {
-                // The first items gate the start of every recurrence: publish
-                // at once.  Later ones are published behind the next item's
-                // loads and copies, when their own copies have long finished.
-                publish_item<0>(flags + (size_t)ch * Hv + h, epoch);
-            } else {
-                pend = make_int4(ch, h, 0, 0);
-            }
+            // The recurrence may be waiting for this item: publish at once
+            // (the copier waits for its copies here; the next item's tiles
+            // are issued after it).
+            if (flags) publish_item(flags + (size_t)ch * Hv + h, epoch);
         }
         if (!kLoop) break;
     }
-    if (tid == kCopier) {
-        if (kLoop && flags && pend.x >= 0 && !bad)
-            publish_item<0>(flags + (size_t)pend.x * Hv + pend.y, epoch);
-        bulk_wait_group<0>();  // shared memory must outlive the copies
-    }
+    if (tid == kCopier) bulk_wait_group<0>();  // shared memory must outlive the copies
     if (bad && tid == 0) atomicCAS(err, (int)kErrNone, (int)kErrTimeout);  // (the first error stays)
-    // Copies started for an item that will not run (the unit stopped on a
-    // time-out): let them land before the memory is given up.
-    if (kLoop && warp == 2) cp_async_wait_all();
-    if (tma_ahead && warp == 0) warp_wait_poll(&sm.tma_bar, tph, 200000000ll);
     tc_fence_before();
     named_barrier(bar, kPrepThreads);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
@@ -1727,8 +1600,7 @@ constexpr int kFusedThreads = kPrepUnits * kPrepThreads;
 constexpr int kLocalChunks = kPrepUnits;  // chunks each recurrence preps itself (one round)
 static_assert(kFusedThreads >= kChainThreads, "the recurrence's warps fit the fused CTA");
 constexpr size_t kPrepUnitBytes = sizeof(PrepSmem);  // a multiple of 1024 (alignas)
-// A prep CTA: kPrepUnits PrepSmem, then each unit's PrepAhead.
-constexpr size_t kPrepCtaBytes = kPrepUnits * (kPrepUnitBytes + sizeof(PrepAhead));
+constexpr size_t kPrepCtaBytes = kPrepUnits * kPrepUnitBytes;  // a prep CTA's units
 constexpr size_t kFusedSmemBytes =
     (sizeof(ChainSmem) > kPrepCtaBytes ? sizeof(ChainSmem) : kPrepCtaBytes) + 1024;
 static_assert(kFusedSmemBytes <= 232448, "fused kernel shared memory");
@@ -1803,10 +1675,7 @@ gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         beta, chunk_off, table, slots, gl, err, N, Hk, Hv,
                         threadIdx.x - u * kPrepThreads, 1 + u, 1 + kPrepUnits + u,
                         s_first * Hv + kPrepUnits * pcta + u, n_units, n_items, flags, 1u, false,
-                        kMulti ? nullptr : porder,
-                        reinterpret_cast<PrepAhead *>(base + kPrepUnits * kPrepUnitBytes +
-                                                      u * sizeof(PrepAhead)),
-                        flags + n_items, s_first * Hv + 2 * n_units);
+                        kMulti ? nullptr : porder, flags + n_items, s_first * Hv + 2 * n_units);
     }
 }
 
