@@ -2082,10 +2082,15 @@ int fused_grid() {
 // on this GPU: a prep item (chunk, value head) takes kPrepItemUs on one of the
 // kPrepUnits units of a CTA in either kernel, a recurrence chunk step
 // kChainStepUs.  Fused: prep on the SMs the recurrences leave, the
-// recurrence following (it cannot finish before its last chunk is prepped).
-// Separate: prep on every SM, then the recurrence.  The longest sequence is
-// estimated as T / N tokens (as long as T for one sequence).
-constexpr double kPrepItemUs = 8.0, kChainStepUs = 1.3;
+// recurrence following (it cannot finish before its last chunk is prepped),
+// after kFusedStartUs: each recurrence's own first round of prep and the
+// prep units' first round, whose code runs cold on every SM.  Separate: prep
+// on every SM, then the recurrence.  The longest sequence is estimated as
+// T / N tokens (as long as T for one sequence).  (At 16/48 heads this puts
+// the crossover between 1472 and 2000 tokens of one sequence; measured it
+// lies between 1000 and 1408: separate against fused 50.8 / 51.9 µs at 1000
+// tokens, 61.1 / 60.1 at 1408, 81.6 / 71.3 at 2000, 30.3 / 38.5 at 352.)
+constexpr double kPrepItemUs = 8.0, kChainStepUs = 1.3, kFusedStartUs = 21.0;
 bool fused_pays(const gdn_problem &p, int grid) {
     const int64_t n_chain = (int64_t)p.num_seqs * p.num_v_heads;
     if (n_chain + 16 > grid) return false;
@@ -2095,7 +2100,7 @@ bool fused_pays(const gdn_problem &p, int grid) {
     const int64_t units_f = kPrepUnits * (grid - n_chain), units_s = kPrepCtasPerSm * (int64_t)grid;
     const double prep_f = kPrepItemUs * (double)((items + units_f - 1) / units_f);
     const double prep_s = kPrepItemUs * (double)((items + units_s - 1) / units_s);
-    return std::max(prep_f, chain + kPrepItemUs) < prep_s + chain + 5.0;
+    return std::max(prep_f, chain) + kFusedStartUs < prep_s + chain + 5.0;
 }
 
 // Whether the kMulti fused kernel should beat the separate kernels, from

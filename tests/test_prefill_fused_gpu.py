@@ -109,6 +109,9 @@ def test_fused_mode_query_and_default():
     p = inputs.prefill_inputs([4000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
     _, _, fused = run(p, 2)
     assert fused, "the cost model picks the fused kernel for one 4000-token sequence"
+    p = inputs.prefill_inputs([352], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
+    _, _, fused = run(p, 2)
+    assert not fused, "a short sequence does not repay the fused kernel's first prep round"
     p = inputs.prefill_inputs([2000, 2000], 16, 48, 128, 128, dtype=torch.bfloat16, seed=0)
     _, _, fused = run(p, 2)
     assert not fused, "two sequences x 48 heads leave too few SMs for prep"
