@@ -66,20 +66,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait with a suspend-time hint: the thread may sleep in hardware (not
-// taking issue slots) until the phase completes or about `ns` nanoseconds pass.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase with the given parity to complete; gives up after
 // about `limit` clock cycles and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
@@ -90,51 +76,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
         if (clock64() - t0 > limit) return false;
     }
     return true;
-}
-
-// Warp-cooperative bounded wait: only lane 0 polls the barrier, sleeping in
-// hardware between polls (a spinning warp would take issue slots from the
-// working warps of its sub-partition); the time limit and the abort flag are
-// checked after every poll (a short loop keeps the callers' code small), and
-// the whole warp leaves together.  Returns false on time-out or when *abort
-// is set.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          long long limit = 4000000000ll) {
-    uint32_t ok = 1;
-    if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
-        const long long t0 = clock64();
-#pragma unroll 1
-        while (!mbar_try_wait_sleep(bar, parity, 100000)) {
-            if (clock64() - t0 > limit || (abort && *abort)) {
-                if (abort) *abort = 1;
-                ok = 0;
-                break;
-            }
-        }
-    }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Warp-cooperative bounded wait without the suspend hint (for the warps that
-// issue copies and MMAs, where wake-up latency matters): lane 0 polls, checking
-// the clock limit and the abort flag on every poll (a short loop keeps the
-// callers' code small), and the warp leaves together.  Returns false on
-// time-out or when *abort is set.
-__device__ __forceinline__ bool warp_wait_spin(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                               long long limit = 4000000000ll) {
-    uint32_t ok = 1;
-    if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
-        const long long t0 = clock64();
-#pragma unroll 1
-        while (!mbar_try_wait(bar, parity)) {
-            if (clock64() - t0 > limit || (abort && *abort)) {
-                if (abort) *abort = 1;
-                ok = 0;
-                break;
-            }
-        }
-    }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Bounded wait of a whole warp, every lane polling try_wait without a
@@ -190,16 +131,6 @@ __device__ __forceinline__ bool warp_wait_lean(uint64_t *bar, uint32_t parity, v
     return true;
 }
 
-// Register budget of the executing warpgroup (all four warps execute it).
-// The increase waits until enough registers of the CTA's launch allocation
-// are free, so the budgets of all warpgroups must sum to at most that.
-template <int N> __device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N> __device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Waits (bounded, every lane polling with an acquire load at device scope)
 // until the 32-bit flag written by another CTA of the grid is nonzero, then
 // orders the async proxy (TMA and bulk copies this thread issues next) after
@@ -226,25 +157,6 @@ __device__ __forceinline__ bool wait_ready(const unsigned *flag, volatile int *a
     return true;
 }
 
-// Single-thread bounded wait for the latency-critical roles (TMA producer,
-// MMA issuer): plain polling, no suspend hint, time limit checked every 256
-// polls.
-__device__ __forceinline__ bool thread_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                            long long limit = 4000000000ll) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 0) {
-            if (abort && *abort) return false;
-            if (clock64() - t0 > limit) {
-                if (abort) *abort = 1;
-                return false;
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y,
                                             int z, uint64_t *bar) {
@@ -269,39 +181,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
                  "r"(bytes)
                  : "memory");
-}
-
-// Warp-uniform variants: every lane calls them with the same arguments and
-// one elected lane issues the copy (keeps the warp converged).
-__device__ __forceinline__ void tma_load_3d_w(void *dst, const CUtensorMap *map, int x, int y,
-                                              int z, uint64_t *bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];\n\t}" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_w(void *dst, const void *src, uint32_t bytes,
-                                            uint64_t *bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];\n\t}" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t *bar, uint32_t bytes) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-        "r"(bytes)
-        : "memory");
 }
 
 // Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
@@ -426,31 +305,6 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-uniform issue: every lane of the warp executes these with the same
-// operands and one elected lane issues the MMA (keeps the descriptors in
-// uniform registers and the warp converged).
-__device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

@@ -45,16 +45,25 @@ def probe(tmp_path_factory):
 
 
 def run(probe, mode, limit=LIMIT):
-    out = torch.full((8,), -1, dtype=torch.int32, device="cuda")
+    out = torch.full((9,), -1, dtype=torch.int32, device="cuda")  # (out[8]: the ready flag)
     assert probe.wait_probe_run(mode, limit, out.data_ptr()) == 0
     o = out.cpu().tolist()
     return [dict(ok=o[4 * w], abort=o[4 * w + 1], kcycles=o[4 * w + 2]) for w in range(2)]
 
 
-@pytest.mark.parametrize("mode", [0, 1, 3])
+@pytest.mark.parametrize("mode", [1, 3])
 def test_bounded_wait_gives_up_and_raises_abort(probe, mode):
+    """The ready-flag wait (1) and the all-lane mbarrier wait (3)."""
     for w in run(probe, mode):
         assert w["ok"] == 0 and w["abort"] == 1
+        assert w["kcycles"] * 1024 >= LIMIT - 1024
+
+
+def test_polling_wait_gives_up(probe):
+    """The prep units' polling wait reports the time-out to its caller (which
+    raises the error itself) and leaves the abort flag alone."""
+    for w in run(probe, 0):
+        assert w["ok"] == 0 and w["abort"] == 0
         assert w["kcycles"] * 1024 >= LIMIT - 1024
 
 
@@ -68,7 +77,7 @@ def test_abort_releases_the_other_waiters(probe, mode):
 
 
 def test_context_usable_after_time_outs(probe):
-    run(probe, 0)
+    run(probe, 3)
     p = inputs.prefill_inputs([100], 1, 3, 128, 128, dtype=torch.bfloat16, seed=11)
     check_prefill(p, TOL_BF16)
     assert gdn.gdn_chunk_prefill_device_status() == gdn.GDN_OK
