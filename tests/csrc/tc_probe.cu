@@ -35,6 +35,32 @@
 
 using namespace gdn::ptx;
 
+// (probe only) Warp-uniform issue: every lane of the warp executes these with the same
+// operands and one elected lane issues the MMA (keeps the descriptors in
+// uniform registers and the warp converged).
+__device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+
 namespace {
 
 // Stores element (row, col) of a bf16 tile held as 64-column swizzled atoms
@@ -72,7 +98,7 @@ __device__ void time_groups(uint32_t a0, uint32_t b0, uint32_t tmem, uint64_t *b
                 mma_bf16_w(tmem, a_mn ? ad + 128 * (r % 4) : ad + 2 * (r % 4), b, id, r > 0);
         }
         mma_commit_w(bar);
-        warp_wait(bar, phase & 1, nullptr);
+        warp_wait_poll(bar, phase & 1);
         ++phase;
         const long long t1 = clock64();
         best = min(best, t1 - t0);
@@ -93,7 +119,7 @@ __device__ void time_chains(uint32_t a0, uint32_t b0, uint32_t tmem, uint64_t *b
         mma_bf16_w(tmem + (r % chains) * Nn, ad + 2 * (r % 4), bd + 2 * (r % 4), id, r >= chains);
     const long long t1 = clock64();
     mma_commit_w(bar);
-    warp_wait(bar, V & 1, nullptr);
+    warp_wait_poll(bar, V & 1);
     const long long t2 = clock64();
     if ((threadIdx.x & 31) == 0) {
         d[2 * V] = (float)(t1 - t0);
@@ -125,7 +151,7 @@ __device__ void time_variant(int mode, uint32_t a0, uint32_t b0, uint32_t tmem, 
     }
     const long long t1 = clock64();
     if (warp_mode) mma_commit_w(bar); else mma_commit(bar);
-    if (warp_mode) warp_wait(bar, V & 1, nullptr); else mbar_wait(bar, V & 1, 2000000000ll);
+    if (warp_mode) warp_wait_poll(bar, V & 1); else mbar_wait(bar, V & 1, 2000000000ll);
     const long long t2 = clock64();
     if ((threadIdx.x & 31) == 0) {
         d[2 * V] = (float)(t1 - t0);
