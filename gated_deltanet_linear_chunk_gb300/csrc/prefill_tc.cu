@@ -443,11 +443,13 @@ __device__ __forceinline__ bool unit_wait(uint64_t *bar, uint32_t parity, int wa
 // Makes an item's slot visible device-wide and publishes its ready flag
 // (the thread that issued the slot's bulk copies, all of them this thread's
 // committed groups; every other thread's slot writes are ordered before a
-// unit barrier this thread has passed since).
+// unit barrier this thread has passed since).  The copies are complete and
+// ordered before the flag by the proxy fence; the release store at device
+// scope carries them, and, through the barrier, the other threads' writes, to
+// a reader that acquires the flag (no further fence is needed).
 __device__ __forceinline__ void publish_item(unsigned *flag, unsigned epoch) {
     bulk_wait_group<0>();
     fence_proxy_async_global();
-    __threadfence();
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(epoch) : "memory");
 }
 
