@@ -28,7 +28,8 @@ __all__ = [
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_status_string",
     "gdn_version", "gdn_chunk_prefill_device_status", "gdn_decode_step_half_state",
     "gdn_verify_step", "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_snapshot_slots",
-    "gdn_chunk_prefill_timed", "gdn_prefill_fused_mode", "gdn_chunk_prefill_host",
+    "gdn_chunk_prefill_timed", "gdn_prefill_fused_mode", "gdn_prefill_path",
+    "gdn_chunk_prefill_host",
     "gdn_chunk_prefill_scan",
     "gdn_chunk_prefill_scan_workspace_size", "Problem",
     "GDN_BF16", "GDN_F32",
@@ -143,6 +144,8 @@ def _load(path: str) -> ctypes.CDLL:
     lib.gdn_chunk_prefill_host.argtypes = [PP, ctypes.c_int32] + [P] * 16 + [P]
     lib.gdn_prefill_fused_mode.restype = ctypes.c_int32
     lib.gdn_prefill_fused_mode.argtypes = [ctypes.c_int32]
+    lib.gdn_prefill_path.restype = ctypes.c_int32
+    lib.gdn_prefill_path.argtypes = [PP, ctypes.c_int32, ctypes.c_int32]
     return lib
 
 
@@ -224,6 +227,17 @@ def gdn_prefill_fused_mode(mode: int = -1) -> int:
     recurrence per value head whenever possible; default 2) and returns the
     previous mode; -1 only queries."""
     return int(library().gdn_prefill_fused_mode(int(mode)))
+
+
+def gdn_prefill_path(num_seqs: int, total_tokens: int, Hk: int, Hv: int, dk: int = 128,
+                     dv: int = 128, sms: int = 152, mode: int = -1,
+                     dtype=torch.bfloat16) -> int:
+    """Which kernels a prefill of this size would run on a GPU with `sms` SMs
+    (see ``gdn_prefill_path`` in include/gdn.h): 0 separate, 1 fused, 2 fused
+    with one recurrence per value head; -1 without the tensor-core path.
+    Needs no device."""
+    p = make_problem(num_seqs, total_tokens, Hk, Hv, dk, dv, dtype)
+    return int(library().gdn_prefill_path(ctypes.byref(p), int(sms), int(mode)))
 
 
 def gdn_status_string(code: int) -> str:

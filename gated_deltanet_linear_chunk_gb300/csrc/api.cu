@@ -277,6 +277,13 @@ GDN_API gdn_status gdn_chunk_prefill_prep_layout(const gdn_problem *problem, int
 
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode) { return gdn::prefill_fused_mode(mode); }
 
+GDN_API int32_t gdn_prefill_path(const gdn_problem *problem, int32_t sms, int32_t mode) {
+    if (check_problem(problem) != GDN_OK || sms < 0 || !gdn::prefill_tc_supported(*problem))
+        return -1;
+    if (mode < 0 || mode > 3) mode = gdn::prefill_fused_mode(-1);
+    return gdn::prefill_path(*problem, sms, sms, mode);
+}
+
 GDN_API const char *gdn_status_string(gdn_status status) {
     switch (status) {
         case GDN_OK: return "GDN_OK";

@@ -97,9 +97,15 @@ gdn_status launch_prefill_scan(const gdn_problem &p, int chunks_per_group, const
                                const int32_t *cu, const float *h0, void *out, float *hT,
                                cudaStream_t stream);
 
-// Fused prep + recurrence mode: sets it (0, 1, 2) and returns the old one;
+// Fused prep + recurrence mode: sets it (0, 1, 2, 3) and returns the old one;
 // any other value only queries.
 int prefill_fused_mode(int mode);
+
+// The kernels a tensor-core prefill of `p` runs in fused mode `mode`, with
+// the fused kernels' variants able to use `grid` and `grid_m` SMs (0: not at
+// all): 0 separate prep and recurrence, 1 fused, 2 fused with one recurrence
+// per value head.
+int prefill_path(const gdn_problem &p, int grid, int grid_m, int mode);
 
 // events: null, or four caller-created events recorded on `stream` before
 // the chunk table, after it, after prep and after the recurrence; *fused

@@ -2136,6 +2136,28 @@ bool multi_pays(const gdn_problem &p, int grid) {
     return multi < 0.95 * (prep_s + chain_s);
 }
 
+}  // namespace
+
+// The kernels a prefill of `p` runs: 0 the separate prep and recurrence
+// kernels, 1 the fused kernel with one recurrence per (sequence, value head),
+// 2 the fused kernel with one recurrence per value head over all sequences;
+// `grid` and `grid_m` are the SMs the two fused variants can use (0: they
+// cannot run).  Fused with one recurrence per (sequence, value head) when
+// they leave 16 SMs for prep (mode 2: and its cost model prefers it), else
+// the per-head variant (mode 1: when the first does not fit, mode 2: when its
+// cost model prefers it, mode 3: whenever it fits).
+int prefill_path(const gdn_problem &p, int grid, int grid_m, int mode) {
+    if (p.total_tokens == 0 || mode == 0 || p.num_seqs <= 0) return 0;
+    const bool fits = (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid;
+    if (mode != 3 && grid > 0 && (mode == 1 ? fits : fused_pays(p, grid))) return 1;
+    if (fits && mode == 1) return 0;
+    if (grid_m > 0 && (mode == 2 ? multi_pays(p, grid_m) : p.num_v_heads + 16 <= grid_m))
+        return 2;
+    return 0;
+}
+
+namespace {
+
 // Chunk table, then the fused kernel: prep and the recurrence in one launch.
 // False when the launch was refused (the caller then runs the separate
 // kernels; the chunk table is already in place).
@@ -2204,16 +2226,10 @@ gdn_status launch_prefill_tc(const gdn_problem &p, const void *q, const void *k,
     const int mode = prefill_fused_mode(-1);
     const bool plain = snaps || p.total_tokens == 0 || mode == 0;
     const int grid = plain ? 0 : fused_grid<false>();
-    // Fused with one recurrence per (sequence, value head) when they leave SMs
-    // for prep (mode 2: and the cost model prefers it), else fused with one
-    // per value head over all sequences (kMulti; mode 1: when the first does
-    // not fit, mode 2: when its cost model prefers it, mode 3: always).
-    const bool fits = (int64_t)p.num_seqs * p.num_v_heads + 16 <= grid;
-    const bool one = mode != 3 && grid > 0 && (mode == 1 ? fits : fused_pays(p, grid));
-    const int grid_m = (plain || one || (fits && mode == 1)) ? 0 : fused_grid<true>();
-    const bool multi = grid_m > 0 && (mode == 2 ? multi_pays(p, grid_m)
-                                                : p.num_v_heads + 16 <= grid_m);
-    if (one || multi) {
+    const int grid_m = plain ? 0 : fused_grid<true>();
+    const int path = plain ? 0 : prefill_path(p, grid, grid_m, mode);
+    const bool multi = path == 2;
+    if (path != 0) {
         gdn_status st = launch_table(p, w, t, cu, 0, true, stream, tm, !multi);
         if (st != GDN_OK) return st;
         time_mark(tm, 2, stream);  // (no separate prep launch)

@@ -423,6 +423,20 @@ GDN_API gdn_status gdn_chunk_prefill_timed(const gdn_problem *problem,
 GDN_API int32_t gdn_prefill_fused_mode(int32_t mode);
 
 /*
+ * Which kernels gdn_chunk_prefill would run for `problem` on a GPU with
+ * `sms` SMs on which the fused kernels fit one CTA per SM (GB300: 152), in
+ * fused mode `mode` (0-3 as gdn_prefill_fused_mode; any other value: the
+ * current mode): 0 separate prep and recurrence kernels, 1 the fused kernel
+ * with one recurrence per (sequence, value head), 2 the fused kernel with one
+ * recurrence per value head over all sequences.  The choice uses only the
+ * problem's sizes (total tokens and sequence count, not the lengths, which
+ * are on the device).  A diagnostic: it needs no device and launches nothing.
+ * Returns -1 for an invalid descriptor, a negative `sms`, or a configuration
+ * without the tensor-core path (not bf16 with dk = dv = 128).
+ */
+GDN_API int32_t gdn_prefill_path(const gdn_problem *problem, int32_t sms, int32_t mode);
+
+/*
  * Diagnostics for tests of the intra-chunk prep on its own (the pages compare
  * every kernel of the chunked layer with a reference separately: page
  * "cf-1.com", section "精度").  Only for bf16 q/k/v with dk = dv = 128

@@ -128,3 +128,18 @@ def test_timed_call_equals_plain_call():
     o2, f2, _, _ = gdn.gdn_chunk_prefill_timed(*args, h0, output_final_state=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+@pytest.mark.parametrize("lens,Hk,Hv", [
+    ([4000], 16, 48), ([300], 16, 48), ([2000, 2000], 16, 48), ([1024] * 8, 16, 48),
+    ([700, 64], 2, 6),
+])
+def test_path_diagnostic_matches_the_call(lens, Hk, Hv):
+    """gdn_prefill_path (sizes only, no device) names the kernels a real call
+    runs on this GPU, in the default mode and with the per-head variant forced."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = inputs.prefill_inputs(lens, Hk, Hv, 128, 128, dtype=torch.bfloat16, seed=25)
+    for mode in (2, 3):
+        _, _, ran = run(p, mode)
+        assert gdn.gdn_prefill_path(len(lens), sum(lens), Hk, Hv, sms=sms, mode=mode) == ran
+    gdn.gdn_prefill_fused_mode(2)
