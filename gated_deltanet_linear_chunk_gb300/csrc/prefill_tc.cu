@@ -1591,13 +1591,15 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // ------------------------------------------------------------------ fused prep + recurrence
 // One persistent cooperative launch, one CTA of 512 threads per SM (up to 128
 // registers a thread: the recurrence's warps compile as in the separate
-// kernel).  CTAs below n_chain run the recurrence of one (sequence, value
-// head) each (warps 0-13, 14-15 idle); the others run four prep units each
-// over the (chunk, value head) items in chunk order, publishing a ready flag
-// per item, and the recurrence waits for the flag of each chunk before
-// loading it.  Prep never waits for the recurrence and all CTAs are resident
-// (cooperative launch), so every wait ends.  Prep runs on the SMs the
-// recurrence leaves idle, during the recurrence instead of before it.
+// kernel).  CTAs below n_chain run a recurrence each (warps 0-13, 14-15
+// idle): of one (sequence, value head), or (kMulti) of one value head over
+// every sequence in turn.  The others run four prep units each over the
+// (chunk, value head) items in the prep order, each unit publishing an item's
+// ready flag as soon as its slot is written, and the recurrence waits for the
+// flag of each chunk before loading it.  Prep never waits for the recurrence
+// and all CTAs are resident (cooperative launch), so every wait ends.  Prep
+// runs on the SMs the recurrence leaves idle, during the recurrence instead
+// of before it.
 constexpr int kFusedThreads = kPrepUnits * kPrepThreads;
 constexpr int kLocalChunks = kPrepUnits;  // chunks each recurrence preps itself (one round)
 static_assert(kFusedThreads >= kChainThreads, "the recurrence's warps fit the fused CTA");
