@@ -27,10 +27,10 @@
  * Ownership and threading: the caller owns every buffer.  The library never
  * allocates device memory, never frees, never synchronises, and launches only
  * on the given stream.  Calls are reentrant.  The process-wide state is:
- *   - per device, an attribute cache (SM count, whether the fused prefill
- *     kernel fits and its launch attribute, the resident CTAs of the
- *     persistent decode kernels and their shared-memory attribute), filled
- *     once per device and kernel under a lock;
+ *   - per device, an attribute cache (SM count, whether each variant of the
+ *     fused prefill kernel fits and its launch attribute, the resident CTAs
+ *     of the persistent decode kernels and their shared-memory attribute),
+ *     filled once per device and kernel under a lock;
  *   - the fused-path mode of gdn_prefill_fused_mode (an atomic integer);
  *   - per device, the upload and download streams of gdn_chunk_prefill_host
  *     (created at its first call on that device);
